@@ -1,0 +1,390 @@
+"""CCA prefill benchmark: global-aware pooling + fused core/local attention.
+
+One step = one full prefill pass (cca_pool then cca_attn_fwd) over one batch
+of synthetic inputs already resident in HBM.  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload mha32k|mha128k|gqa64k]
+                  [--impl cca|reference] [--no-e2e] [--no-cpu-baseline]
+
+Under torchrun (N > 1) every rank runs an independent replica of the workload
+on its own GPU (no data-path collective: batches are independent), so the
+scaling is weak; the only collectives are the timing barrier and the
+max-over-ranks of the elapsed time.  `--impl reference` times the fp64 CPU
+oracle on a bounded sample of the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from sparse_long_context_cca_gb300 import workloads as W  # noqa: E402
+
+WORKLOADS = {"mha32k": W.MHA_32K, "mha128k": W.MHA_128K, "gqa64k": W.GQA_64K}
+METRIC = "CCA prefill tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129e6
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        hbm = d.get("hbm_gbs") or d.get("hbm_GBps")
+        tf = d.get("bf16_tflops")
+        tfs = d.get("bf16_tflops_sustained", tf)
+        if hbm and tf:
+            return {"hbm_gbs": float(hbm), "bf16_tflops": float(tf),
+                    "bf16_tflops_sustained": float(tfs)}, "measured"
+    except (OSError, ValueError):
+        pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+class ClockSampler:
+    """Samples nvidia-smi SM clocks and throttle reasons while the timed region runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.25)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def kernel_sha(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(kernel_file: str, workload_key: str):
+    """Per-launch DRAM bytes recorded from an ncu capture of this kernel source,
+    or None when no capture exists for the current source."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    try:
+        lines = open(path).read().splitlines()
+    except OSError:
+        return None
+    sha = kernel_sha(kernel_file)
+    for ln in lines:
+        parts = ln.split()
+        if len(parts) >= 4 and not ln.startswith("#") and parts[0] == workload_key and parts[1] == sha:
+            return float(parts[2]) + float(parts[3])
+    return None
+
+
+def time_steps(fn, steps, stream):
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        fn()
+    end.record(stream)
+    return start, end
+
+
+def run_cca(args, rank, world, local):
+    from sparse_long_context_cca_gb300 import api
+    from sparse_long_context_cca_gb300.inputs import make_qkv
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    api.load_library()
+    wl = WORKLOADS[args.workload]
+    peaks, peak_src = load_peaks()
+    stream = torch.cuda.current_stream()
+
+    def measure(wl, steps, warmup):
+        Q, K, V = make_qkv(wl, dev)
+        G = wl.N // wl.g
+        Kc = torch.empty((wl.B, wl.Hkv, G, wl.d), dtype=Q.dtype, device=dev)
+        Vc = torch.empty_like(Kc)
+        O = torch.empty_like(Q)
+        LSE = torch.empty((wl.B, wl.Hq, wl.N), dtype=torch.float32, device=dev)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+               torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+
+        def step(e=None):
+            if e is not None:
+                e[0].record(stream)
+            api.cca_pool(Q, K, V, wl.g, Kc, Vc, stream=stream)
+            if e is not None:
+                e[1].record(stream)
+            api.cca_attn_fwd(Q, K, V, Kc, Vc, wl.g, wl.w, O, LSE, stream=stream)
+            if e is not None:
+                e[2].record(stream)
+
+        for _ in range(warmup):
+            step()
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for k in range(steps):
+            step(ev[k])
+        t1.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        total_ms = t0.elapsed_time(t1)
+        pool_ms = [a.elapsed_time(b) for a, b, _ in ev]
+        attn_ms = [b.elapsed_time(c) for _, b, c in ev]
+        assert torch.isfinite(LSE).all()
+        del Q, K, V, O, LSE, Kc, Vc
+        torch.cuda.empty_cache()
+        return total_ms, statistics.mean(pool_ms), statistics.mean(attn_ms)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    total_ms, pool_ms, attn_ms = measure(wl, args.steps, args.warmup)
+    clocks = sampler.stop()
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    tokens_per_step = wl.B * wl.N * world
+    value = tokens_per_step / (ms_per_step / 1e3)
+    flops = W.attn_flops(wl)
+    pbytes = W.pool_bytes(wl)
+    attn_tflops = flops / (attn_ms / 1e3) / 1e12
+    pool_gbs = pbytes / (pool_ms / 1e3) / 1e9
+    kfile = os.path.join(ROOT, "sparse_long_context_cca_gb300", "csrc", "attn_tc.cu")
+    pfile = os.path.join(ROOT, "sparse_long_context_cca_gb300", "csrc", "pool.cu")
+    out = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded normal Q/K/V, 1% heavy-hitter keys)",
+        "config": {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "N": wl.N, "d": wl.d,
+                   "g": wl.g, "w": wl.w, "global_batch": wl.B * world, "seq_len": wl.N,
+                   "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (%.0f MB of Q/K/V vs 129 MB), no flush" % (
+                       3 * wl.B * wl.Hq * wl.N * wl.d * 2 / 1e6)},
+        "attn_eff_tflops": attn_tflops,
+        "attn_ms": attn_ms, "pool_ms": pool_ms,
+        "pool_gbs": pool_gbs,
+        "roofline": {"bound": "tensor", "kernel": "attn_bf16_tc_kernel", "achieved": attn_tflops,
+                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": attn_tflops / peaks["bf16_tflops"],
+                     "peak_source": f"{peak_src} dense bf16 (burst)",
+                     "traffic": recorded_traffic(kfile, args.workload),
+                     "algorithmic_unit": "4*d FLOP per (query, visible key, head): %.4g FLOP per launch" % flops},
+        "pool_roofline": {"bound": "hbm", "kernel": "pool_kernel", "achieved": pool_gbs,
+                          "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": pool_gbs / peaks["hbm_gbs"],
+                          "peak_source": f"{peak_src} copy bandwidth",
+                          "traffic": recorded_traffic(pfile, args.workload),
+                          "algorithmic_bytes": pbytes},
+        "clocks": clocks,
+        "gpu_launches": 2 * args.steps,
+    }
+    if args.also_128k and wl is not W.MHA_128K:
+        tot, pm, am = measure(W.MHA_128K, max(3, args.steps // 4), 3)
+        wl2 = W.MHA_128K
+        out["mha128k"] = {"workload": wl2.name, "tokens_per_s": wl2.B * wl2.N / (tot / max(3, args.steps // 4) / 1e3),
+                          "attn_ms": am, "pool_ms": pm,
+                          "attn_eff_tflops": W.attn_flops(wl2) / (am / 1e3) / 1e12,
+                          "attn_frac": W.attn_flops(wl2) / (am / 1e3) / 1e12 / peaks["bf16_tflops"],
+                          "pool_gbs": W.pool_bytes(wl2) / (pm / 1e3) / 1e9,
+                          "pool_frac": W.pool_bytes(wl2) / (pm / 1e3) / 1e9 / peaks["hbm_gbs"]}
+        out["gpu_launches"] += 2 * max(3, args.steps // 4)
+    if not args.no_e2e:
+        out["e2e"] = e2e(wl, dev, stream, max(3, args.steps // 2), world)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
+    return out
+
+
+def e2e(wl, dev, stream, steps, world):
+    """Same metric through the public API with host buffers: pinned host -> device
+    copy of Q, K, V, the prefill, and a device -> host read of O and LSE, every step."""
+    from sparse_long_context_cca_gb300 import api
+    from sparse_long_context_cca_gb300.inputs import make_qkv
+    Qd, Kd, Vd = make_qkv(wl, dev)
+    hQ, hK, hV = (t.cpu().pin_memory() for t in (Qd, Kd, Vd))
+    del Qd, Kd, Vd
+    Q = torch.empty(hQ.shape, dtype=hQ.dtype, device=dev)
+    K = torch.empty(hK.shape, dtype=hK.dtype, device=dev)
+    V = torch.empty(hV.shape, dtype=hV.dtype, device=dev)
+    G = wl.N // wl.g
+    out = (torch.empty_like(Q), torch.empty((wl.B, wl.Hq, wl.N), dtype=torch.float32, device=dev),
+           torch.empty((wl.B, wl.Hkv, G, wl.d), dtype=Q.dtype, device=dev),
+           torch.empty((wl.B, wl.Hkv, G, wl.d), dtype=Q.dtype, device=dev))
+    hO = torch.empty(out[0].shape, dtype=out[0].dtype).pin_memory()
+    hL = torch.empty(out[1].shape, dtype=torch.float32).pin_memory()
+
+    def step():
+        Q.copy_(hQ, non_blocking=True)
+        K.copy_(hK, non_blocking=True)
+        V.copy_(hV, non_blocking=True)
+        api.cca_prefill(Q, K, V, wl.g, wl.w, out=out, stream=stream)
+        hO.copy_(out[0], non_blocking=True)
+        hL.copy_(out[1], non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    torch.cuda.synchronize()
+    dt = (time.perf_counter() - t0) / steps
+    h2d = sum(t.numel() * t.element_size() for t in (hQ, hK, hV))
+    d2h = hO.numel() * hO.element_size() + hL.numel() * 4
+    return {"value": wl.B * wl.N * world / dt, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": dt * 1e3, "steps": steps}
+
+
+def oracle_sample(wl, seconds_budget):
+    """Times the fp64 oracle on whole heads of the workload (pooling of the head's
+    KV head + attention of every row), as many heads as fit the budget.
+    Returns (tokens/s scaled to all heads, threads, description)."""
+    import oracle
+    from sparse_long_context_cca_gb300.inputs import make_qkv
+    small = wl.small(B=1, Hq=wl.Hq // wl.Hkv, Hkv=1)  # one KV head with its query heads
+    Q, K, V = make_qkv(small, "cpu")
+    q, k, v = oracle.widen(Q[:, :1]), oracle.widen(K), oracle.widen(V)
+    heads_done = 0
+    t_used = 0.0
+    while True:
+        t0 = time.perf_counter()
+        Kc, Vc = oracle.pool(oracle.widen(Q), k, v, wl.g)
+        oracle.attn(q, k, v, Kc, Vc, wl.g, wl.w)
+        t_used += time.perf_counter() - t0
+        heads_done += 1
+        if t_used >= seconds_budget or heads_done >= wl.B * wl.Hq:
+            break
+    per_head = t_used / heads_done
+    step_seconds = per_head * wl.B * wl.Hq
+    desc = (f"{heads_done} whole head(s) of {wl.name} (pooling of its KV head + all {wl.N} rows), "
+            f"{t_used:.1f} s, scaled by {wl.B * wl.Hq}/{heads_done} heads")
+    return wl.B * wl.N / step_seconds, oracle.threads(), desc, step_seconds
+
+
+def cpu_baseline(wl, seconds):
+    v, cores, desc, _ = oracle_sample(wl, seconds)
+    return {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    wl = WORKLOADS[args.workload]
+    vals = []
+    for _ in range(args.warmup):
+        oracle_sample(wl, 0.0)
+    desc = cores = None
+    for _ in range(args.steps):
+        v, cores, desc, _ = oracle_sample(wl, 0.0)
+        vals.append(v)
+    value = statistics.mean(vals)
+    return {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": wl.B * wl.N / value * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "N": wl.N, "d": wl.d,
+                       "g": wl.g, "w": wl.w, "parallelism": "cpu oracle, rank 0"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": "each step: " + desc},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="mha32k")
+    ap.add_argument("--impl", choices=["cca", "reference"], default="cca")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-128k", dest="also_128k", action="store_false")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    out = run_cca(args, rank, world, local)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,121 @@
+/*
+ * cca.h - C ABI of libcca.so: prefill forward of Core Context Aware (CCA)
+ * attention on an sm_103a GPU.
+ *
+ * The method ("Core Context Aware Transformers for Long Context Language
+ * Modeling", ICML 2025) replaces self-attention over N tokens by two steps:
+ *
+ *  1. Global-aware pooling (Method section, pooling equation
+ *     c_i = softmax(Q_{ig} K'_{I_i}^T / sqrt(d)) X^G_{I_i}): the sequence is cut
+ *     into N/g non-overlapping groups of g tokens; each group becomes one core
+ *     key and one core value, the softmax-weighted sum of the group's keys and
+ *     values, weighted by the logits of the group's last query against the
+ *     group's keys.
+ *  2. Fused attention (Method section, fusion equation
+ *     Att_i = softmax(Q_i [K^G_{T_i}; K^L_{U_i}]^T / sqrt(d)) [V^G_{T_i}; V^L_{U_i}]):
+ *     query i takes ONE softmax over the core tokens of the groups that lie
+ *     entirely before its local window, followed by the raw tokens of the
+ *     window.
+ *
+ * Index conventions (0-indexed; the pages leave them open):
+ *   lo(i)      = max(0, i - w + 1)            first token of i's window
+ *   window     = tokens [lo(i), i]           (n_loc = min(w, i + 1) tokens)
+ *   core j     visible to i iff (j + 1) * g <= lo(i)   (n_core = lo(i) / g)
+ *   group j    = tokens [j*g, (j+1)*g - 1], scored by the query of token (j+1)*g - 1
+ *   GQA        query head h reads KV head h / (Hq / Hkv); a KV head's pooling
+ *              logit is the mean of the logits of its Hq/Hkv query heads,
+ *              taken before the group softmax.
+ *   scale      tau = 1/sqrt(d) unless params.scale > 0; the same tau is used by
+ *              both steps.  LSE is the natural log-sum-exp of the tau-scaled
+ *              logits over the visible set.
+ *
+ * Layouts (all contiguous, row-major, d innermost; element type = dtype):
+ *   Q  [B, Hq,  N,   d]      K, V   [B, Hkv, N,   d]
+ *   Kc [B, Hkv, N/g, d]      Vc     [B, Hkv, N/g, d]
+ *   O  [B, Hq,  N,   d]      LSE    [B, Hq,  N]  (always fp32)
+ *
+ * Ownership and execution: the caller allocates and owns every buffer; all
+ * pointers except `params` are DEVICE pointers (16-byte aligned).  The library
+ * keeps no allocation and no state between calls.  Calls are asynchronous on
+ * `stream` (a cudaStream_t, NULL = legacy default stream); results are
+ * defined after the stream reaches the call.  Arithmetic: bf16 inputs with
+ * fp32 accumulation and fp32 softmax, outputs rounded to nearest even; f32
+ * inputs computed in fp32 throughout.
+ *
+ * Errors: the return value reports host-side checks and the launch.  Nothing
+ * is launched and nothing is written when a check fails.  A device-side
+ * give-up (a pipeline wait that exceeded its time limit) is reported by
+ * writing CCA_ERR_TIMEOUT into *params.dev_status when that pointer is set
+ * (a caller-owned device int32 that the caller zeroes); the kernel then
+ * returns without hanging and its outputs are unspecified.
+ */
+#ifndef CCA_H_
+#define CCA_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define CCA_ABI_VERSION 1
+
+enum cca_status {
+    CCA_OK = 0,
+    CCA_ERR_INVALID_ARG = -1, /* null/misaligned pointer, bad size, N % g != 0, Hq % Hkv != 0 */
+    CCA_ERR_UNSUPPORTED = -2, /* dtype/d combination not built, or the device is not sm_103 */
+    CCA_ERR_CUDA = -3,        /* a CUDA runtime/driver call or the launch failed */
+    CCA_ERR_TIMEOUT = -4      /* written to dev_status by a kernel that gave up waiting */
+};
+
+enum cca_dtype {
+    CCA_BF16 = 0, /* bfloat16 storage, fp32 accumulation */
+    CCA_F32 = 1   /* float32 storage and arithmetic */
+};
+
+typedef struct cca_params {
+    int32_t B;          /* batch                                  >= 1 */
+    int32_t Hq;         /* query heads                            >= 1, multiple of Hkv */
+    int32_t Hkv;        /* key/value heads                        >= 1 */
+    int32_t N;          /* tokens per sequence                    >= 1, multiple of g */
+    int32_t d;          /* head dimension: 64 or 128 (bf16 attention: 128 only) */
+    int32_t g;          /* group size                             >= 1 */
+    int32_t w;          /* local window                           >= 1 (w >= N allowed) */
+    int32_t dtype;      /* enum cca_dtype */
+    float scale;        /* softmax scale; <= 0 selects 1/sqrt(d) */
+    int32_t *dev_status;/* optional device int32, see "Errors" above */
+} cca_params_t;
+
+/*
+ * cca_pool - global-aware pooling (pooling equation of the Method section).
+ * Reads Q (only the last token of every group is used), K and V; writes
+ * Kc[b, kv, j, :] = sum_t a_t K[b, kv, j*g + t, :] and the same for Vc, with
+ * a = softmax_t(tau * mean_{h in kv} Q[b, h, (j+1)*g - 1, :] . K[b, kv, j*g + t, :]).
+ * Supported: dtype bf16 or f32, d in {64, 128}, any g >= 1.
+ */
+int cca_pool(const void *Q, const void *K, const void *V, void *Kc, void *Vc,
+             const cca_params_t *params, void *stream);
+
+/*
+ * cca_attn_fwd - fused core/local attention (fusion equation of the Method
+ * section).  For every (b, h, i): one softmax over the logits tau*Q_i.Kc_j for
+ * visible cores j < lo(i)/g followed by tau*Q_i.K_m for m in [lo(i), i];
+ * O_i = the softmax-weighted sum of the matching Vc_j and V_m rows;
+ * LSE_i = log-sum-exp of the same logits.  Kc/Vc are the outputs of cca_pool
+ * (or any caller-supplied core tokens of that shape).
+ * Supported: bf16 with d = 128 (tensor-core kernel), f32 with d in {64, 128}.
+ */
+int cca_attn_fwd(const void *Q, const void *K, const void *V, const void *Kc, const void *Vc,
+                 void *O, float *LSE, const cca_params_t *params, void *stream);
+
+/* Static English text for a status code (never NULL). */
+const char *cca_status_string(int status);
+
+/* CCA_ABI_VERSION of the loaded library. */
+int cca_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CCA_H_ */

@@ -1,0 +1,180 @@
+"""Thin Python binding of libcca.so (include/cca.h), argument marshalling only.
+
+Every step of the computation runs in the library's CUDA kernels; this module
+allocates outputs with torch (device memory is plumbing), checks that tensors
+match the C ABI's layout, and forwards raw device pointers.  There is no
+fallback: if the library is missing or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+CCA_OK = 0
+CCA_ERR_INVALID_ARG = -1
+CCA_ERR_UNSUPPORTED = -2
+CCA_ERR_CUDA = -3
+CCA_ERR_TIMEOUT = -4
+CCA_BF16 = 0
+CCA_F32 = 1
+
+_DTYPE = {torch.bfloat16: CCA_BF16, torch.float32: CCA_F32}
+
+
+class CcaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+        self.status = status
+
+
+class CcaParams(ctypes.Structure):
+    """Mirror of cca_params_t."""
+    _fields_ = [("B", ctypes.c_int32), ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32),
+                ("N", ctypes.c_int32), ("d", ctypes.c_int32), ("g", ctypes.c_int32),
+                ("w", ctypes.c_int32), ("dtype", ctypes.c_int32), ("scale", ctypes.c_float),
+                ("dev_status", ctypes.c_void_p)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+EXPORTED = ["cca_pool", "cca_attn_fwd", "cca_status_string", "cca_abi_version",
+            "cca_test_set_wait_limit_ns", "cca_test_skip_q_load"]
+
+
+def library_path() -> str:
+    return os.environ.get("CCA_LIBRARY", _build.LIB)
+
+
+def load_library():
+    """Load libcca.so; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"libcca.so not found at {path}: build it first "
+                               "(python -c 'import __graft_entry__ as g; g.build()')")
+        lib = ctypes.CDLL(path)
+        vp = ctypes.c_void_p
+        pp = ctypes.POINTER(CcaParams)
+        lib.cca_pool.argtypes = [vp, vp, vp, vp, vp, pp, vp]
+        lib.cca_pool.restype = ctypes.c_int
+        lib.cca_attn_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, pp, vp]
+        lib.cca_attn_fwd.restype = ctypes.c_int
+        lib.cca_status_string.argtypes = [ctypes.c_int]
+        lib.cca_status_string.restype = ctypes.c_char_p
+        lib.cca_abi_version.argtypes = []
+        lib.cca_abi_version.restype = ctypes.c_int
+        lib.cca_test_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
+        lib.cca_test_set_wait_limit_ns.restype = None
+        lib.cca_test_skip_q_load.argtypes = [ctypes.c_int]
+        lib.cca_test_skip_q_load.restype = None
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().cca_status_string(int(status)).decode()
+
+
+def make_params(B, Hq, Hkv, N, d, g, w, dtype, scale=0.0, dev_status=None) -> CcaParams:
+    return CcaParams(int(B), int(Hq), int(Hkv), int(N), int(d), int(g), int(w), int(dtype),
+                     float(scale), dev_status)
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(t: torch.Tensor, name: str, dtype, shape):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _dims(Q, K):
+    if Q.dim() != 4 or K.dim() != 4:
+        raise ValueError("Q and K must be [B, H, N, d]")
+    B, Hq, N, d = Q.shape
+    Hkv = K.shape[1]
+    return B, Hq, Hkv, N, d
+
+
+def cca_pool(Q, K, V, g: int, Kc=None, Vc=None, scale: float = 0.0, stream=None):
+    """Global-aware pooling: returns (Kc, Vc), each [B, Hkv, N/g, d]."""
+    lib = load_library()
+    B, Hq, Hkv, N, d = _dims(Q, K)
+    if Q.dtype not in _DTYPE:
+        raise ValueError(f"unsupported dtype {Q.dtype}")
+    _check(Q, "Q", Q.dtype, (B, Hq, N, d))
+    _check(K, "K", Q.dtype, (B, Hkv, N, d))
+    _check(V, "V", Q.dtype, (B, Hkv, N, d))
+    G = N // g if g > 0 else 0
+    if Kc is None:
+        Kc = torch.empty((B, Hkv, G, d), dtype=Q.dtype, device=Q.device)
+    if Vc is None:
+        Vc = torch.empty((B, Hkv, G, d), dtype=Q.dtype, device=Q.device)
+    _check(Kc, "Kc", Q.dtype, (B, Hkv, G, d))
+    _check(Vc, "Vc", Q.dtype, (B, Hkv, G, d))
+    prm = make_params(B, Hq, Hkv, N, d, g, 1, _DTYPE[Q.dtype], scale)
+    st = lib.cca_pool(Q.data_ptr(), K.data_ptr(), V.data_ptr(), Kc.data_ptr(), Vc.data_ptr(),
+                      ctypes.byref(prm), _stream_handle(stream))
+    if st != CCA_OK:
+        raise CcaError(st, "cca_pool")
+    return Kc, Vc
+
+
+def cca_attn_fwd(Q, K, V, Kc, Vc, g: int, w: int, O=None, LSE=None, scale: float = 0.0,
+                 dev_status=None, stream=None):
+    """Fused core/local attention: returns (O [B,Hq,N,d], LSE [B,Hq,N] fp32)."""
+    lib = load_library()
+    B, Hq, Hkv, N, d = _dims(Q, K)
+    if Q.dtype not in _DTYPE:
+        raise ValueError(f"unsupported dtype {Q.dtype}")
+    G = N // g if g > 0 else 0
+    _check(Q, "Q", Q.dtype, (B, Hq, N, d))
+    _check(K, "K", Q.dtype, (B, Hkv, N, d))
+    _check(V, "V", Q.dtype, (B, Hkv, N, d))
+    _check(Kc, "Kc", Q.dtype, (B, Hkv, G, d))
+    _check(Vc, "Vc", Q.dtype, (B, Hkv, G, d))
+    if O is None:
+        O = torch.empty_like(Q)
+    if LSE is None:
+        LSE = torch.empty((B, Hq, N), dtype=torch.float32, device=Q.device)
+    _check(O, "O", Q.dtype, (B, Hq, N, d))
+    _check(LSE, "LSE", torch.float32, (B, Hq, N))
+    status_ptr = None
+    if dev_status is not None:
+        _check(dev_status, "dev_status", torch.int32, (1,))
+        status_ptr = dev_status.data_ptr()
+    prm = make_params(B, Hq, Hkv, N, d, g, w, _DTYPE[Q.dtype], scale, status_ptr)
+    st = lib.cca_attn_fwd(Q.data_ptr(), K.data_ptr(), V.data_ptr(), Kc.data_ptr(), Vc.data_ptr(),
+                          O.data_ptr(), LSE.data_ptr(), ctypes.byref(prm), _stream_handle(stream))
+    if st != CCA_OK:
+        raise CcaError(st, "cca_attn_fwd")
+    return O, LSE
+
+
+def cca_prefill(Q, K, V, g: int, w: int, scale: float = 0.0, out=None, stream=None):
+    """Both steps of CCA prefill: pooling, then fused attention.
+    Returns (O, LSE, Kc, Vc).  `out` may hold preallocated (O, LSE, Kc, Vc)."""
+    O = LSE = Kc = Vc = None
+    if out is not None:
+        O, LSE, Kc, Vc = out
+    Kc, Vc = cca_pool(Q, K, V, g, Kc, Vc, scale, stream)
+    O, LSE = cca_attn_fwd(Q, K, V, Kc, Vc, g, w, O, LSE, scale, None, stream)
+    return O, LSE, Kc, Vc

@@ -1,0 +1,122 @@
+// C ABI front end of libcca.so (declared in include/cca.h): argument checks,
+// dtype/shape dispatch and launch.  Every check runs on the host before any
+// CUDA call, so a rejected call launches nothing and writes nothing.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "../../include/cca.h"
+#include "internal.h"
+
+namespace cca {
+extern unsigned long long g_wait_limit_ns;
+extern int g_skip_q_load;
+}  // namespace cca
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_shape(const cca_params_t *p, bool need_w) {
+    if (p == nullptr) return CCA_ERR_INVALID_ARG;
+    if (p->B < 1 || p->Hq < 1 || p->Hkv < 1 || p->N < 1 || p->d < 1 || p->g < 1) return CCA_ERR_INVALID_ARG;
+    if (need_w && p->w < 1) return CCA_ERR_INVALID_ARG;
+    if (p->Hq % p->Hkv != 0 || p->N % p->g != 0) return CCA_ERR_INVALID_ARG;
+    if (p->dtype != CCA_BF16 && p->dtype != CCA_F32) return CCA_ERR_INVALID_ARG;
+    if (!(p->scale == p->scale) || isinf(p->scale)) return CCA_ERR_INVALID_ARG;
+    // Element counts of the largest tensor must fit the kernels' 64-bit indexing and
+    // row counts the 32-bit tensor-map coordinates.
+    const double elems = static_cast<double>(p->B) * p->Hq * p->N * p->d;
+    if (elems > 9.0e15) return CCA_ERR_INVALID_ARG;
+    if (p->d != 64 && p->d != 128) return CCA_ERR_UNSUPPORTED;
+    return CCA_OK;
+}
+
+cca::Shape to_shape(const cca_params_t *p) {
+    cca::Shape s;
+    s.B = p->B;
+    s.Hq = p->Hq;
+    s.Hkv = p->Hkv;
+    s.N = p->N;
+    s.d = p->d;
+    s.g = p->g;
+    s.w = p->w;
+    s.scale = p->scale > 0.f ? p->scale : 1.0f / sqrtf(static_cast<float>(p->d));
+    return s;
+}
+
+// The kernels are built for sm_103a only.
+int check_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return CCA_ERR_CUDA;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return CCA_ERR_CUDA;
+    if (major != 10 || minor != 3) return CCA_ERR_UNSUPPORTED;
+    return CCA_OK;
+}
+
+int from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return CCA_OK;
+    if (e == cudaErrorNotSupported) return CCA_ERR_UNSUPPORTED;
+    return CCA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int cca_pool(const void *Q, const void *K, const void *V, void *Kc, void *Vc, const cca_params_t *params,
+             void *stream) {
+    int st = check_shape(params, false);
+    if (st != CCA_OK) return st;
+    const void *ptrs[5] = {Q, K, V, Kc, Vc};
+    for (const void *q : ptrs)
+        if (q == nullptr || !aligned16(q)) return CCA_ERR_INVALID_ARG;
+    if ((st = check_device()) != CCA_OK) return st;
+    return from_cuda(cca::launch_pool(params->dtype, Q, K, V, Kc, Vc, to_shape(params),
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+int cca_attn_fwd(const void *Q, const void *K, const void *V, const void *Kc, const void *Vc, void *O, float *LSE,
+                 const cca_params_t *params, void *stream) {
+    int st = check_shape(params, true);
+    if (st != CCA_OK) return st;
+    const void *ptrs[7] = {Q, K, V, Kc, Vc, O, LSE};
+    for (const void *q : ptrs)
+        if (q == nullptr || !aligned16(q)) return CCA_ERR_INVALID_ARG;
+    if (params->dev_status != nullptr && (reinterpret_cast<uintptr_t>(params->dev_status) & 3u) != 0)
+        return CCA_ERR_INVALID_ARG;
+    if (params->dtype == CCA_BF16 && params->d != 128) return CCA_ERR_UNSUPPORTED;
+    if ((st = check_device()) != CCA_OK) return st;
+    const cca::Shape s = to_shape(params);
+    cudaStream_t strm = static_cast<cudaStream_t>(stream);
+    if (params->dtype == CCA_F32)
+        return from_cuda(cca::launch_attn_f32(static_cast<const float *>(Q), static_cast<const float *>(K),
+                                              static_cast<const float *>(V), static_cast<const float *>(Kc),
+                                              static_cast<const float *>(Vc), static_cast<float *>(O), LSE, s,
+                                              strm));
+    return from_cuda(cca::launch_attn_bf16_tc(Q, K, V, Kc, Vc, O, LSE, s, params->dev_status, strm));
+}
+
+const char *cca_status_string(int status) {
+    switch (status) {
+        case CCA_OK: return "ok";
+        case CCA_ERR_INVALID_ARG: return "invalid argument";
+        case CCA_ERR_UNSUPPORTED: return "unsupported dtype/head-dim combination or device";
+        case CCA_ERR_CUDA: return "CUDA error";
+        case CCA_ERR_TIMEOUT: return "device pipeline wait timed out";
+        default: return "unknown status";
+    }
+}
+
+int cca_abi_version(void) { return CCA_ABI_VERSION; }
+
+// Test hooks for the bounded-wait path of the bf16 attention kernel: set the
+// per-wait time limit, and make later launches skip the Q-tile load so that
+// the MMA issuer's first wait runs out.  Not part of the public header.
+void cca_test_set_wait_limit_ns(unsigned long long ns) { cca::g_wait_limit_ns = ns; }
+void cca_test_skip_q_load(int on) { cca::g_skip_q_load = on ? 1 : 0; }
+
+}  // extern "C"

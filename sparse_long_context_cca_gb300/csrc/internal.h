@@ -1,0 +1,30 @@
+// Internal interface between the C-ABI front end (cca_api.cu) and the kernel
+// translation units.  Arguments are already validated when these are called.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace cca {
+
+struct Shape {
+    int B, Hq, Hkv, N, d, g, w;
+    float scale;  // resolved softmax scale (> 0)
+};
+
+// Global-aware pooling. dtype: 0 = bf16, 1 = f32.
+cudaError_t launch_pool(int dtype, const void *Q, const void *K, const void *V, void *Kc, void *Vc,
+                        const Shape &s, cudaStream_t stream);
+
+// fp32 fused attention on CUDA cores (any supported d).
+cudaError_t launch_attn_f32(const float *Q, const float *K, const float *V, const float *Kc,
+                            const float *Vc, float *O, float *LSE, const Shape &s,
+                            cudaStream_t stream);
+
+// bf16 fused attention on the tcgen05 tensor cores (d = 128).
+// Returns cudaErrorNotSupported when the tensor-map encoder is unavailable.
+cudaError_t launch_attn_bf16_tc(const void *Q, const void *K, const void *V, const void *Kc,
+                                const void *Vc, void *O, float *LSE, const Shape &s,
+                                int32_t *dev_status, cudaStream_t stream);
+
+}  // namespace cca

@@ -1,0 +1,101 @@
+"""Host-only checks of the C ABI: the library loads, exports every function
+include/*.h declares, and rejects bad arguments before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from sparse_long_context_cca_gb300 import api
+from sparse_long_context_cca_gb300 import build as cbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    cbuild.build()
+    return api.load_library()
+
+
+def declared_functions():
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for f in os.listdir(inc):
+        if f.endswith(".h"):
+            src = open(os.path.join(inc, f)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(cca_\w+)\s*\(", src))
+    return sorted(names)
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert {"cca_pool", "cca_attn_fwd", "cca_status_string"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(api.EXPORTED) == set(names)
+
+
+def test_abi_version_and_strings(lib):
+    assert lib.cca_abi_version() == 1
+    for code in (0, -1, -2, -3, -4, 7):
+        assert isinstance(api.status_string(code), str) and api.status_string(code)
+
+
+# Fake, 16-byte aligned pointers: every call below must be rejected on the host
+# before any CUDA call, so they are never dereferenced.
+P = [0x1000 * (k + 1) for k in range(7)]
+
+
+def call_pool(lib, **kw):
+    base = dict(B=1, Hq=2, Hkv=2, N=256, d=128, g=16, w=32, dtype=api.CCA_BF16)
+    base.update(kw)
+    prm = api.make_params(**base)
+    ptrs = kw.pop("_ptrs", P[:5]) if "_ptrs" in kw else P[:5]
+    return lib.cca_pool(*ptrs, ctypes.byref(prm), None)
+
+
+def call_attn(lib, ptrs=None, **kw):
+    base = dict(B=1, Hq=2, Hkv=2, N=256, d=128, g=16, w=32, dtype=api.CCA_BF16)
+    base.update(kw)
+    prm = api.make_params(**base)
+    ptrs = ptrs or P
+    return lib.cca_attn_fwd(*ptrs, ctypes.byref(prm), None)
+
+
+@pytest.mark.parametrize("kw", [dict(N=250), dict(g=0), dict(w=0), dict(B=0), dict(Hq=3, Hkv=2),
+                                dict(Hkv=0), dict(N=0), dict(dtype=5), dict(scale=float("nan"))])
+def test_attn_rejects_bad_shapes(lib, kw):
+    assert call_attn(lib, **kw) == api.CCA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw", [dict(N=250), dict(g=0), dict(Hq=3, Hkv=2), dict(dtype=9)])
+def test_pool_rejects_bad_shapes(lib, kw):
+    assert call_pool(lib, **kw) == api.CCA_ERR_INVALID_ARG
+
+
+def test_rejects_null_and_misaligned(lib):
+    for k in range(7):
+        bad = list(P)
+        bad[k] = 0
+        assert call_attn(lib, ptrs=bad) == api.CCA_ERR_INVALID_ARG
+        bad[k] = P[k] + 8
+        assert call_attn(lib, ptrs=bad) == api.CCA_ERR_INVALID_ARG
+    prm = api.make_params(1, 2, 2, 256, 128, 16, 32, api.CCA_BF16)
+    assert lib.cca_pool(P[0], 0, P[2], P[3], P[4], ctypes.byref(prm), None) == api.CCA_ERR_INVALID_ARG
+    assert lib.cca_pool(P[0], P[1] + 4, P[2], P[3], P[4], ctypes.byref(prm), None) == api.CCA_ERR_INVALID_ARG
+    assert lib.cca_attn_fwd(*P, None, None) == api.CCA_ERR_INVALID_ARG
+
+
+def test_unsupported_head_dims(lib):
+    assert call_attn(lib, d=96) == api.CCA_ERR_UNSUPPORTED
+    assert call_attn(lib, d=64, dtype=api.CCA_BF16) == api.CCA_ERR_UNSUPPORTED
+    assert call_pool(lib, d=256) == api.CCA_ERR_UNSUPPORTED
+
+
+def test_python_binding_requires_cuda_tensors(lib):
+    import torch
+    x = torch.zeros(1, 2, 16, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        api.cca_pool(x, x, x, 4)

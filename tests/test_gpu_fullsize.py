@@ -1,0 +1,71 @@
+"""Parity at the full workload sizes, in the launch configuration the benchmark
+times: the whole prefill runs on the GPU; the fp64 oracle recomputes sampled
+rows (boundary rows of the window/core edges and tiles plus random rows) of a
+few heads, and the sampled groups' core tokens."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity import BF16_LSE, BF16_O_MAX_REL, BF16_O_MEAN, check_cores
+from sparse_long_context_cca_gb300 import api
+from sparse_long_context_cca_gb300.inputs import make_qkv
+from sparse_long_context_cca_gb300.workloads import GQA_64K, MHA_32K, MHA_128K, sweep
+
+pytestmark = pytest.mark.gpu
+
+
+def sample_rows(N, g, w, rng, n_random):
+    edges = [0, 1, w - 2, w - 1, w, w + g - 2, w + g - 1, w + g, 127, 128, 129, N // 2, N - 129, N - 128,
+             N - 2, N - 1]
+    rows = {i for i in edges if 0 <= i < N}
+    rows |= set(rng.integers(0, N, size=n_random).tolist())
+    return sorted(rows)
+
+
+def check_workload(wl, heads, n_random=48):
+    torch.cuda.empty_cache()
+    Q, K, V = make_qkv(wl, "cuda")
+    O, LSE, Kc, Vc = api.cca_prefill(Q, K, V, wl.g, wl.w)
+    torch.cuda.synchronize()
+    assert torch.isfinite(LSE).all()
+    rng = np.random.default_rng(wl.seed)
+    r = wl.Hq // wl.Hkv
+    for (b, h) in heads:
+        kv = h // r
+        hs = slice(kv * r, (kv + 1) * r)
+        q = Q[b:b + 1, hs]
+        k = K[b:b + 1, kv:kv + 1]
+        v = V[b:b + 1, kv:kv + 1]
+        Kr, Vr = oracle.pool(q, k, v, wl.g)
+        groups = np.unique(np.concatenate([[0, wl.n_groups - 1], rng.integers(0, wl.n_groups, 64)]))
+        gi = torch.as_tensor(groups, device=Kc.device)
+        check_cores(Kc[b, kv, gi], Vc[b, kv, gi], Kr[0, 0, groups], Vr[0, 0, groups], Q.dtype,
+                    f"{wl.name} b{b} kv{kv}")
+        rows = sample_rows(wl.N, wl.g, wl.w, rng, n_random)
+        sel = [(0, h - kv * r, i) for i in rows]
+        Or, Lr = oracle.attn_rows(q, k, v, Kr, Vr, wl.g, wl.w, sel)
+        o = oracle.widen(O[b, h, rows])
+        err = np.abs(o - Or)
+        assert err.max() <= BF16_O_MAX_REL * np.abs(Or).max(), (wl.name, h, err.max())
+        assert err.mean() <= BF16_O_MEAN, (wl.name, h, err.mean())
+        lerr = np.abs(oracle.widen(LSE[b, h, rows]) - Lr)
+        assert lerr.max() <= BF16_LSE, (wl.name, h, lerr.max())
+    del Q, K, V, O, LSE, Kc, Vc
+
+
+def test_mha_32k():
+    check_workload(MHA_32K, [(0, 0), (0, 17), (0, 31)])
+
+
+def test_mha_128k():
+    check_workload(MHA_128K, [(0, 0), (0, 31)], n_random=32)
+
+
+def test_gqa_64k():
+    check_workload(GQA_64K, [(0, 0), (0, 5), (0, 31)])
+
+
+@pytest.mark.parametrize("wl", sweep(), ids=lambda w: w.name)
+def test_sweep(wl):
+    check_workload(wl, [(1, 7)], n_random=24)

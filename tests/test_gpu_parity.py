@@ -1,0 +1,119 @@
+"""GPU parity of the CUDA path (through the C ABI) with the fp64 CPU oracle,
+at sizes the oracle finishes in seconds that span several tiles and ragged
+tails, plus the method's edge cases."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity import check_cores, check_out
+from sparse_long_context_cca_gb300 import api
+from sparse_long_context_cca_gb300.inputs import make_qkv
+from sparse_long_context_cca_gb300.workloads import TINY_F32, Workload
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def cuda_lib():
+    assert torch.cuda.is_available(), "these tests need a GPU"
+    api.load_library()
+
+
+def wl(B, Hq, Hkv, N, d, g, w, dtype="bf16", seed=5, hh=0.01):
+    return Workload(f"test B{B} Hq{Hq} Hkv{Hkv} N{N} d{d} g{g} w{w} {dtype}", B, Hq, Hkv, N, d, g, w,
+                    dtype, seed, hh)
+
+
+POOL_CASES = [
+    wl(1, 2, 2, 256, 128, 16, 1), wl(2, 4, 2, 512, 128, 8, 1), wl(1, 2, 2, 192, 128, 64, 1),
+    wl(1, 1, 1, 96, 128, 1, 1), wl(1, 2, 2, 120, 128, 3, 1), wl(1, 4, 1, 256, 128, 32, 1),
+    wl(1, 2, 2, 256, 64, 16, 1), wl(1, 2, 2, 320, 128, 40, 1),
+    wl(1, 2, 2, 256, 64, 16, 1, "f32"), wl(1, 4, 2, 256, 128, 8, 1, "f32"), wl(1, 2, 2, 60, 64, 5, 1, "f32"),
+]
+
+
+@pytest.mark.parametrize("w", POOL_CASES, ids=lambda w: w.name)
+def test_pool_parity(w):
+    Q, K, V = make_qkv(w, "cuda")
+    Kc, Vc = api.cca_pool(Q, K, V, w.g)
+    torch.cuda.synchronize()
+    Kr, Vr = oracle.pool(Q, K, V, w.g)
+    check_cores(Kc, Vc, Kr, Vr, Q.dtype, w.name)
+
+
+ATTN_CASES = [
+    TINY_F32,
+    wl(1, 2, 2, 512, 64, 8, 100, "f32"),
+    wl(2, 4, 2, 384, 128, 16, 64, "f32"),
+    wl(1, 2, 2, 256, 128, 16, 32),          # tiny shape in bf16
+    wl(1, 2, 2, 1008, 128, 16, 160),        # ragged last query tile (1008 = 7*128 + 112)
+    wl(1, 2, 2, 384, 128, 16, 512),         # w >= N: causal attention, no cores
+    wl(1, 2, 2, 256, 128, 4, 1),            # w = 1: one local key per row
+    wl(1, 2, 2, 384, 128, 1, 64),           # g = 1: equal to causal attention
+    wl(1, 2, 2, 2048, 128, 64, 256),
+    wl(1, 8, 2, 1024, 128, 16, 128),        # GQA, r = 4
+    wl(2, 2, 2, 640, 128, 8, 96),           # B = 2, w not a multiple of the tile
+    wl(1, 2, 2, 4096, 128, 8, 256),         # several core tiles per query tile
+    wl(1, 2, 1, 1920, 128, 24, 300),        # g not a power of two, GQA r = 2
+    wl(1, 1, 1, 16, 128, 16, 4),            # a single group, N far below one tile
+]
+
+
+@pytest.mark.parametrize("w", ATTN_CASES, ids=lambda w: w.name)
+def test_prefill_parity(w):
+    Q, K, V = make_qkv(w, "cuda")
+    O, LSE, Kc, Vc = api.cca_prefill(Q, K, V, w.g, w.w)
+    torch.cuda.synchronize()
+    Or, Lr, Kr, Vr = oracle.prefill(Q, K, V, w.g, w.w)
+    check_cores(Kc, Vc, Kr, Vr, Q.dtype, w.name)
+    check_out(O, LSE, Or, Lr, Q.dtype, w.name + " end-to-end")
+    # attention alone, fed the GPU's own core tokens
+    Oa, La = oracle.attn(Q, K, V, Kc, Vc, w.g, w.w)
+    check_out(O, LSE, Oa, La, Q.dtype, w.name + " attention-only")
+
+
+@pytest.mark.parametrize("w", [wl(1, 2, 2, 1024, 128, 16, 128), wl(1, 2, 2, 512, 64, 16, 64, "f32")],
+                         ids=lambda w: w.name)
+def test_repeatable_bitwise(w):
+    """Two runs on the same inputs give identical bits (no races)."""
+    Q, K, V = make_qkv(w, "cuda")
+    a = api.cca_prefill(Q, K, V, w.g, w.w)
+    b = api.cca_prefill(Q, K, V, w.g, w.w)
+    torch.cuda.synchronize()
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
+def test_scale_argument():
+    w = wl(1, 2, 2, 512, 128, 16, 64)
+    Q, K, V = make_qkv(w, "cuda")
+    O, LSE, Kc, Vc = api.cca_prefill(Q, K, V, w.g, w.w, scale=0.05)
+    torch.cuda.synchronize()
+    Or, Lr, Kr, Vr = oracle.prefill(Q, K, V, w.g, w.w, scale=0.05)
+    check_out(O, LSE, Or, Lr, Q.dtype, "scale=0.05")
+
+
+def test_streams_and_preallocated_outputs():
+    w = wl(1, 4, 4, 768, 128, 16, 128)
+    Q, K, V = make_qkv(w, "cuda")
+    s = torch.cuda.Stream()
+    out = (torch.full_like(Q, float("nan")), torch.full((1, 4, 768), float("nan"), device="cuda"),
+           torch.empty(1, 4, 48, 128, dtype=Q.dtype, device="cuda"),
+           torch.empty(1, 4, 48, 128, dtype=Q.dtype, device="cuda"))
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        api.cca_prefill(Q, K, V, w.g, w.w, out=out, stream=s)
+    s.synchronize()
+    Or, Lr, _, _ = oracle.prefill(Q, K, V, w.g, w.w)
+    check_out(out[0], out[1], Or, Lr, Q.dtype, "side stream")
+
+
+def test_dev_status_stays_zero():
+    w = wl(1, 2, 2, 512, 128, 16, 64)
+    Q, K, V = make_qkv(w, "cuda")
+    Kc, Vc = api.cca_pool(Q, K, V, w.g)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    api.cca_attn_fwd(Q, K, V, Kc, Vc, w.g, w.w, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
