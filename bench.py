@@ -139,6 +139,21 @@ def recorded_traffic(kernel_file: str, workload_key: str):
     return None
 
 
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The slowest rank's elapsed time (the job's time); identity at world == 1."""
+    if world <= 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(total_ms: float, steps: int, tokens_per_rank_step: int, world: int):
+    """(ms per step, whole-job tokens/s): every rank processes its own batch each step."""
+    ms_per_step = total_ms / steps
+    return ms_per_step, tokens_per_rank_step * world / (ms_per_step / 1e3)
+
+
 def time_steps(fn, steps, stream):
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
@@ -207,13 +222,8 @@ def run_cca(args, rank, world, local):
     sampler.start()
     total_ms, pool_ms, attn_ms = measure(wl, args.steps, args.warmup)
     clocks = sampler.stop()
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
-    ms_per_step = total_ms / args.steps
-    tokens_per_step = wl.B * wl.N * world
-    value = tokens_per_step / (ms_per_step / 1e3)
+    total_ms = max_over_ranks(total_ms, world, dev)
+    ms_per_step, value = job_throughput(total_ms, args.steps, wl.B * wl.N, world)
     flops = W.attn_flops(wl)
     pbytes = W.pool_bytes(wl)
     attn_tflops = flops / (attn_ms / 1e3) / 1e12

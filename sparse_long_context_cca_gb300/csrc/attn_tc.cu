@@ -3,25 +3,33 @@
 // Method section, fusion equation
 //     Att_i = softmax(Q_i [K^G_{T_i}; K^L_{U_i}]^T / sqrt(d)) [V^G_{T_i}; V^L_{U_i}]).
 //
-// One CTA owns one tile of 128 query rows of one (batch, query head).  The
-// keys it visits form one sequence of 128-key tiles: first the core tokens
-// Kc/Vc [0, n_core(last row)), then the raw tokens K/V of the band
-// [lo(first row), last row].  A single online-softmax state (row max m, row
-// sum l, output accumulator O in tensor memory) runs over the whole sequence,
-// so the core and local segments share one normalisation.  Only tiles that
-// straddle a visibility edge are masked:
+// Persistent kernel, one CTA per SM.  A work item is 256 query rows of one
+// (batch, query head), split in two 128-row halves A and B that share every
+// K/V tile the CTA loads.  The keys form one sequence of 128-key tiles: the
+// core tokens Kc/Vc [0, n_core(last row)), then the raw tokens K/V of the band
+// [lo(first row), last row].  Each half visits only the tiles it can see (a
+// half skips a tile that lies wholly outside its own band or staircase), and
+// keeps one online-softmax state (row max m, row sum l, O in tensor memory)
+// over its whole sequence, so core and local segments share one normalisation.
+// Only tiles that straddle a visibility edge are masked:
 //   core tile:  column c (core y0+c) is visible to row i iff y0 + c < lo(i)/g;
 //   local tile: column c (token y0+c) is visible to row i iff lo(i) <= y0+c <= i.
 //
-// Roles (192 threads):
-//   warp 0      TMA producer: Q tile once, then K/V tiles into a ring of NS
-//               32 KB shared-memory slots (128-byte swizzle, two 64-column
-//               halves per tile);
-//   warp 1      MMA issuer (one thread): S = Q K^T into TMEM (fp32), then
-//               O += P V with P read from TMEM (bf16);
-//   warps 2..5  softmax + epilogue: thread t owns TMEM lane / query row t.
-// Tensor memory (512 columns): S0 | S1 | O | P0 | P1, S and P double-buffered
-// so that the QK^T of tile j+1 and the PV of tile j-1 overlap the softmax of j.
+// Roles (320 threads):
+//   warp 0       TMA producer: the two Q tiles of an item, then K(t), V(t) for
+//                every tile t into a ring of NS 32 KB slots (128-byte swizzle);
+//   warp 1       MMA issuer (one thread): S_h = Q_h K^T (both operands in shared
+//                memory) and O_h += P_h V (P_h in tensor memory, V MN-major);
+//   warps 2..5   softmax + epilogue of half A, warps 6..9 the same for half B.
+//                A warp may only touch TMEM lanes 32*(warp%4) .. +31, so each
+//                group of four consecutive warps covers the 128 lanes once;
+//                thread t of the group owns TMEM lane / query row t.
+// Tensor memory (512 columns): S_A | S_B | O_A | O_B.  P_h (bf16) overwrites
+// the first 64 columns of S_h after the softmax has read S_h.  The issuer
+// writes S_h for the next tile only after the PV that read P_h (issue order),
+// and a completed S_h therefore also means that every earlier PV of the half
+// has completed, which is what lets the softmax rescale O_h in place.
+// Work items are ordered heaviest first and dealt round-robin to the CTAs.
 // Every mbarrier wait is bounded in time; on a time-out the CTA stops, drains
 // what it has in flight, frees its tensor memory and reports CCA_ERR_TIMEOUT.
 #include <cuda.h>
@@ -37,41 +45,43 @@
 namespace cca {
 namespace {
 
-constexpr int BM = 128;                       // query rows per CTA
+constexpr int BM = 128;                       // query rows per half
 constexpr int BN = 128;                       // keys per tile
 constexpr int HD = 128;                       // head dimension
 constexpr int NS = 5;                         // ring slots
 constexpr uint32_t TILE_BYTES = BN * HD * 2;  // one bf16 128x128 tile
 constexpr uint32_t HALF_BYTES = TILE_BYTES / 2;
-constexpr int NUM_THREADS = 192;
+constexpr int NUM_THREADS = 320;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TM_S0 = 0, TM_O = 256, TM_P0 = 384;  // S1 = 128, P1 = 448
-constexpr float LAZY_RESCALE_LOG2 = 8.0f;     // keep a stale max while it is within 2^8
+constexpr uint32_t TM_S = 0;    // S_h at h * 128
+constexpr uint32_t TM_O = 256;  // O_h at 256 + h * 128
+constexpr float LAZY_RESCALE_LOG2 = 8.0f;  // keep a stale max while it is within 2^8
 
 constexpr uint32_t IDESC_QK = ptx::idesc_bf16_f32(BM, BN, 0, 0);  // Q, K both K-major
 constexpr uint32_t IDESC_PV = ptx::idesc_bf16_f32(BM, HD, 0, 1);  // P (TMEM), V MN-major
 
 // shared-memory layout (offsets from a 1024-byte aligned base)
-constexpr uint32_t OFF_Q = 0;
-constexpr uint32_t OFF_RING = TILE_BYTES;
+constexpr uint32_t OFF_Q = 0;  // Q_A, Q_B
+constexpr uint32_t OFF_RING = 2 * TILE_BYTES;
 constexpr uint32_t OFF_BAR = OFF_RING + NS * TILE_BYTES;
-// barrier indices
 constexpr int B_QFULL = 0;
-constexpr int B_FULL = 1;              // NS
-constexpr int B_EMPTY = B_FULL + NS;   // NS
-constexpr int B_SFULL = B_EMPTY + NS;  // 2
-constexpr int B_SFREE = B_SFULL + 2;   // 2
-constexpr int B_PFULL = B_SFREE + 2;   // 2
-constexpr int B_PVDONE = B_PFULL + 2;  // 2
-constexpr int B_DRAIN = B_PVDONE + 2;
+constexpr int B_QFREE = 1;
+constexpr int B_FULL = 2;               // NS
+constexpr int B_EMPTY = B_FULL + NS;    // NS
+constexpr int B_SFULL = B_EMPTY + NS;   // 2 (per half)
+constexpr int B_PFULL = B_SFULL + 2;    // 2
+constexpr int B_PVDONE = B_PFULL + 2;   // 2
+constexpr int B_OFREE = B_PVDONE + 2;   // 2
+constexpr int B_DRAIN = B_OFREE + 2;
 constexpr int NUM_BARS = B_DRAIN + 1;
 constexpr uint32_t OFF_TMEMPTR = OFF_BAR + NUM_BARS * 8;
 constexpr uint32_t OFF_ABORT = OFF_TMEMPTR + 4;
 constexpr uint32_t SMEM_USED = OFF_ABORT + 4;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack for manual alignment
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 struct Params {
-    int B, Hq, Hkv, N, g, w, n_qtiles;
+    int B, Hq, Hkv, N, g, w, n_pairs, n_items;
     float scale_log2;
     __nv_bfloat16 *O;
     float *LSE;
@@ -80,42 +90,65 @@ struct Params {
     int skip_q_load;  // test hook: never load Q, so the pipeline waits run out
 };
 
-struct TileRange {
-    int Tc, T, lo0, i0, i1, nc_min, lo1;
-};
-
 __device__ __forceinline__ int lo_of(int i, int w) { return i - w + 1 > 0 ? i - w + 1 : 0; }
 
-__device__ __forceinline__ TileRange tile_range(const Params &p, int qt) {
-    TileRange r;
-    r.i0 = qt * BM;
-    r.i1 = min(r.i0 + BM - 1, p.N - 1);
-    r.lo0 = lo_of(r.i0, p.w);
-    r.lo1 = lo_of(r.i1, p.w);
-    const int nc_max = r.lo1 / p.g;
-    r.nc_min = r.lo0 / p.g;
-    r.Tc = (nc_max + BN - 1) / BN;
-    const int Tl = (r.i1 - r.lo0 + 1 + BN - 1) / BN;
-    r.T = r.Tc + Tl;
-    return r;
-}
+// The tile sequence of one work item and which half uses which tile.
+struct Item {
+    int bh, kvz;
+    int a[2], b[2];     // first / last valid row of each half
+    bool valid[2];
+    int tc[2];          // core tiles used by each half: [0, tc[h])
+    int Tc;             // core tiles loaded (max of tc)
+    int lo0;            // first key of local tile 0
+    int kl[2], kh[2];   // local tiles used by each half: [kl, kh)
+    int T;              // tiles loaded
 
-// Load order shared by the producer and the MMA issuer:
-// K0, K1, V0, K2, V1, ..., K(T-1), V(T-2), V(T-1).
-__device__ __forceinline__ void decode_load(int u, int T, bool &is_v, int &t) {
-    if (u == 0) {
-        is_v = false;
-        t = 0;
-    } else if (u == 2 * T - 1) {
-        is_v = true;
-        t = T - 1;
-    } else if (u & 1) {
-        is_v = false;
-        t = (u + 1) >> 1;
-    } else {
-        is_v = true;
-        t = (u >> 1) - 1;
+    __device__ __forceinline__ bool uses(int h, int t) const {
+        if (!valid[h]) return false;
+        if (t < Tc) return t < tc[h];
+        const int k = t - Tc;
+        return k >= kl[h] && k < kh[h];
     }
+    __device__ __forceinline__ int first(int h) const { return tc[h] > 0 ? 0 : Tc + kl[h]; }
+    // next used tile after t, or -1
+    __device__ __forceinline__ int next(int h, int t) const {
+        if (t < Tc) return (t + 1 < tc[h]) ? t + 1 : Tc + kl[h];
+        return (t + 1 < Tc + kh[h]) ? t + 1 : -1;
+    }
+    __device__ __forceinline__ int count(int h) const { return valid[h] ? tc[h] + kh[h] - kl[h] : 0; }
+};
+
+__device__ __forceinline__ Item make_item(const Params &p, int k) {
+    Item it;
+    const int BH = p.B * p.Hq;
+    const int pair = p.n_pairs - 1 - k / BH;  // heaviest pairs first
+    it.bh = k % BH;
+    const int b = it.bh / p.Hq, h = it.bh % p.Hq;
+    it.kvz = b * p.Hkv + h / (p.Hq / p.Hkv);
+    const int i0 = pair * 2 * BM;
+    for (int hh = 0; hh < 2; ++hh) {
+        it.a[hh] = i0 + hh * BM;
+        it.valid[hh] = it.a[hh] < p.N;
+        it.b[hh] = min(it.a[hh] + BM - 1, p.N - 1);
+    }
+    it.lo0 = lo_of(it.a[0], p.w);
+    const int last = it.valid[1] ? it.b[1] : it.b[0];
+    const int Tl = (last - it.lo0) / BN + 1;
+    it.Tc = 0;
+    for (int hh = 0; hh < 2; ++hh) {
+        if (!it.valid[hh]) {
+            it.tc[hh] = 0;
+            it.kl[hh] = it.kh[hh] = 0;
+            continue;
+        }
+        const int nc = lo_of(it.b[hh], p.w) / p.g;
+        it.tc[hh] = (nc + BN - 1) / BN;
+        it.Tc = max(it.Tc, it.tc[hh]);
+        it.kl[hh] = (lo_of(it.a[hh], p.w) - it.lo0) / BN;
+        it.kh[hh] = (it.b[hh] - it.lo0) / BN + 1;
+    }
+    it.T = it.Tc + Tl;
+    return it;
 }
 
 __device__ __forceinline__ void report_timeout(const Params &p) {
@@ -137,26 +170,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // Heaviest query tiles first: block x -> (tile rank, batch*head).
-    const int BH = p.B * p.Hq;
-    const int qt = p.n_qtiles - 1 - static_cast<int>(blockIdx.x / BH);
-    const int bh = static_cast<int>(blockIdx.x % BH);
-    const int b = bh / p.Hq, h = bh % p.Hq;
-    const int kvz = b * p.Hkv + h / (p.Hq / p.Hkv);
-    const TileRange tr = tile_range(p, qt);
-    const int T = tr.T;
-
     if (threadIdx.x == 0) {
         ptx::mbar_init(bar(B_QFULL), 1);
+        ptx::mbar_init(bar(B_QFREE), 1);
         for (int s = 0; s < NS; ++s) {
             ptx::mbar_init(bar(B_FULL + s), 1);
             ptx::mbar_init(bar(B_EMPTY + s), 1);
         }
-        for (int s = 0; s < 2; ++s) {
-            ptx::mbar_init(bar(B_SFULL + s), 1);
-            ptx::mbar_init(bar(B_SFREE + s), 128);
-            ptx::mbar_init(bar(B_PFULL + s), 128);
-            ptx::mbar_init(bar(B_PVDONE + s), 1);
+        for (int h = 0; h < 2; ++h) {
+            ptx::mbar_init(bar(B_SFULL + h), 1);
+            ptx::mbar_init(bar(B_PFULL + h), 128);
+            ptx::mbar_init(bar(B_PVDONE + h), 1);
+            ptx::mbar_init(bar(B_OFREE + h), 128);
         }
         ptx::mbar_init(bar(B_DRAIN), 1);
         *abort_flag = 0;
@@ -170,232 +195,307 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_ptr_smem;
+    const uint64_t lim = p.wait_limit_ns;
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
-        if (lane == 0) {
+    if (warp < 2) {
+        if (warp == 0 && lane == 0) {
+            // ------------------------------------------------------------ producer
             ptx::prefetch_tmap(&tmQ);
             ptx::prefetch_tmap(&tmK);
             ptx::prefetch_tmap(&tmV);
             ptx::prefetch_tmap(&tmKc);
             ptx::prefetch_tmap(&tmVc);
-            if (!p.skip_q_load) {
-                ptx::mbar_arrive_expect_tx(bar(B_QFULL), TILE_BYTES);
-                ptx::tma_load_3d(&tmQ, bar(B_QFULL), base + OFF_Q, 0, tr.i0, bh);
-                ptx::tma_load_3d(&tmQ, bar(B_QFULL), base + OFF_Q + HALF_BYTES, 64, tr.i0, bh);
-            }
-            int issued = 0;
-            for (int u = 0; u < 2 * T; ++u) {
-                const int slot = u % NS;
-                if (!ptx::wait_bounded(bar(B_EMPTY + slot), ((u / NS) & 1) ^ 1, abort_flag, p.wait_limit_ns))
-                    break;
-                bool is_v;
-                int t;
-                decode_load(u, T, is_v, t);
-                const bool core = t < tr.Tc;
-                const void *map = core ? (is_v ? (const void *)&tmVc : (const void *)&tmKc)
-                                       : (is_v ? (const void *)&tmV : (const void *)&tmK);
-                const int y = core ? t * BN : tr.lo0 + (t - tr.Tc) * BN;
-                const uint32_t dst = base + OFF_RING + slot * TILE_BYTES;
-                ptx::mbar_arrive_expect_tx(bar(B_FULL + slot), TILE_BYTES);
-                ptx::tma_load_3d(map, bar(B_FULL + slot), dst, 0, y, kvz);
-                ptx::tma_load_3d(map, bar(B_FULL + slot), dst + HALF_BYTES, 64, y, kvz);
-                issued = u + 1;
+            uint32_t u = 0;  // ring loads issued so far
+            int n_iter = 0;
+            bool ok = true;
+            for (int k = blockIdx.x; ok && k < p.n_items; k += gridDim.x, ++n_iter) {
+                const Item it = make_item(p, k);
+                if (!ptx::wait_bounded(bar(B_QFREE), (n_iter & 1) ^ 1, abort_flag, lim)) break;
+                if (!p.skip_q_load) {
+                    ptx::mbar_arrive_expect_tx(bar(B_QFULL), 2 * TILE_BYTES);
+                    for (int h = 0; h < 2; ++h) {
+                        const uint32_t dst = base + OFF_Q + h * TILE_BYTES;
+                        ptx::tma_load_3d(&tmQ, bar(B_QFULL), dst, 0, it.a[h], it.bh);
+                        ptx::tma_load_3d(&tmQ, bar(B_QFULL), dst + HALF_BYTES, 64, it.a[h], it.bh);
+                    }
+                }
+                for (int t = 0; ok && t < it.T; ++t) {
+                    const bool core = t < it.Tc;
+                    const int y = core ? t * BN : it.lo0 + (t - it.Tc) * BN;
+                    for (int kv = 0; kv < 2; ++kv, ++u) {
+                        const int slot = u % NS;
+                        if (!ptx::wait_bounded(bar(B_EMPTY + slot), ((u / NS) & 1) ^ 1, abort_flag, lim)) {
+                            ok = false;
+                            break;
+                        }
+                        const void *map = core ? (kv ? (const void *)&tmVc : (const void *)&tmKc)
+                                               : (kv ? (const void *)&tmV : (const void *)&tmK);
+                        const uint32_t dst = base + OFF_RING + slot * TILE_BYTES;
+                        ptx::mbar_arrive_expect_tx(bar(B_FULL + slot), TILE_BYTES);
+                        ptx::tma_load_3d(map, bar(B_FULL + slot), dst, 0, y, it.kvz);
+                        ptx::tma_load_3d(map, bar(B_FULL + slot), dst + HALF_BYTES, 64, y, it.kvz);
+                    }
+                }
             }
             if (*abort_flag) {
                 // Let the copies already issued land before the CTA exits.
-                for (int u = issued - NS > 0 ? issued - NS : 0; u < issued; ++u) {
-                    volatile int never = 0;
-                    ptx::wait_bounded(bar(B_FULL + u % NS), (u / NS) & 1, &never, p.wait_limit_ns);
-                }
-                if (!p.skip_q_load) {
-                    volatile int never = 0;
-                    ptx::wait_bounded(bar(B_QFULL), 0, &never, p.wait_limit_ns);
-                }
+                volatile int never = 0;
+                for (uint32_t v = u > NS ? u - NS : 0; v < u; ++v)
+                    ptx::wait_bounded(bar(B_FULL + v % NS), (v / NS) & 1, &never, lim);
+                if (!p.skip_q_load && n_iter > 0)
+                    ptx::wait_bounded(bar(B_QFULL), (n_iter - 1) & 1, &never, lim);
             }
-        }
-        __syncwarp();
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            bool ok = ptx::wait_bounded(bar(B_QFULL), 0, abort_flag, p.wait_limit_ns);
-            for (int u = 0; ok && u < 2 * T; ++u) {
-                const int slot = u % NS;
-                if (!ptx::wait_bounded(bar(B_FULL + slot), (u / NS) & 1, abort_flag, p.wait_limit_ns)) break;
-                bool is_v;
-                int t;
-                decode_load(u, T, is_v, t);
-                const int sb = t & 1;
-                const uint32_t tile = base + OFF_RING + slot * TILE_BYTES;
-                if (!is_v) {
-                    if (!ptx::wait_bounded(bar(B_SFREE + sb), ((t >> 1) & 1) ^ 1, abort_flag, p.wait_limit_ns))
-                        break;
+        } else if (warp == 1 && lane == 0) {
+            // ------------------------------------------------------------ MMA issuer
+            uint32_t ubase = 0;
+            int n_iter = 0;
+            int kpend[NS];
+            for (int s = 0; s < NS; ++s) kpend[s] = 0;
+            uint32_t pf_cnt[2] = {0, 0};
+            int n_half[2] = {0, 0};  // items each half has processed
+            bool ok = true;
+            for (int k = blockIdx.x; ok && k < p.n_items; k += gridDim.x, ++n_iter) {
+                const Item it = make_item(p, k);
+                if (!ptx::wait_bounded(bar(B_QFULL), n_iter & 1, abort_flag, lim)) break;
+                int s_left = it.count(0) + it.count(1);
+                // S_h = Q_h K(t)^T into S_h.  The first user of a ring slot waits for the copy.
+                auto issue_s = [&](int h, int t) -> bool {
+                    const uint32_t uk = ubase + 2 * t;
+                    const int slot = uk % NS;
+                    if (kpend[slot] == 0) {
+                        if (!ptx::wait_bounded(bar(B_FULL + slot), (uk / NS) & 1, abort_flag, lim)) return false;
+                        kpend[slot] = (it.uses(0, t) ? 1 : 0) + (it.uses(1, t) ? 1 : 0);
+                    }
                     ptx::tc_fence_after();
+                    const uint32_t tile = base + OFF_RING + slot * TILE_BYTES;
+                    const uint32_t q = base + OFF_Q + h * TILE_BYTES;
 #pragma unroll
                     for (int kk = 0; kk < HD / 16; ++kk) {
                         const uint32_t koff = (kk >> 2) * HALF_BYTES + (kk & 3) * 32;
-                        const uint64_t ad = ptx::smem_desc_sw128(base + OFF_Q + koff, 16, 1024);
-                        const uint64_t bd = ptx::smem_desc_sw128(tile + koff, 16, 1024);
-                        ptx::mma_ss(tmem + TM_S0 + sb * BN, ad, bd, IDESC_QK, kk > 0 ? 1u : 0u);
+                        ptx::mma_ss(tmem + TM_S + h * BN, ptx::smem_desc_sw128(q + koff, 16, 1024),
+                                    ptx::smem_desc_sw128(tile + koff, 16, 1024), IDESC_QK, kk > 0 ? 1u : 0u);
                     }
-                    ptx::tc_commit(bar(B_SFULL + sb));
-                } else {
-                    if (!ptx::wait_bounded(bar(B_PFULL + sb), (t >> 1) & 1, abort_flag, p.wait_limit_ns)) break;
-                    ptx::tc_fence_after();
-#pragma unroll
-                    for (int kk = 0; kk < BN / 16; ++kk) {
-                        const uint64_t bd = ptx::smem_desc_sw128(tile + kk * 2048, HALF_BYTES, 1024);
-                        ptx::mma_ts(tmem + TM_O, tmem + TM_P0 + sb * 64 + kk * 8, bd, IDESC_PV,
-                                    (t > 0 || kk > 0) ? 1u : 0u);
+                    ptx::tc_commit(bar(B_SFULL + h));
+                    if (--kpend[slot] == 0) ptx::tc_commit(bar(B_EMPTY + slot));
+                    if (--s_left == 0) ptx::tc_commit(bar(B_QFREE));
+                    return true;
+                };
+                // Prologue: first S of each half, earliest tile first, so that the issuer
+                // never waits on a copy that sits behind one it has not consumed yet.
+                {
+                    const bool b_first = it.valid[1] && it.first(1) < it.first(0);
+                    for (int q = 0; ok && q < 2; ++q) {
+                        const int h = b_first ? 1 - q : q;
+                        if (it.valid[h]) ok = issue_s(h, it.first(h));
                     }
-                    ptx::tc_commit(bar(B_PVDONE + sb));
                 }
-                ptx::tc_commit(bar(B_EMPTY + slot));
+                bool first_pv[2] = {true, true};
+                for (int t = 0; ok && t < it.T; ++t) {
+                    const uint32_t uv = ubase + 2 * t + 1;
+                    const int vslot = uv % NS;
+                    if (!ptx::wait_bounded(bar(B_FULL + vslot), (uv / NS) & 1, abort_flag, lim)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t vtile = base + OFF_RING + vslot * TILE_BYTES;
+                    for (int h = 0; h < 2; ++h) {
+                        if (!it.uses(h, t)) continue;
+                        if (!ptx::wait_bounded(bar(B_PFULL + h), pf_cnt[h] & 1, abort_flag, lim)) {
+                            ok = false;
+                            break;
+                        }
+                        ++pf_cnt[h];
+                        if (first_pv[h]) {
+                            // the epilogue of this half's previous item must have read O_h
+                            if (!ptx::wait_bounded(bar(B_OFREE + h), (n_half[h] & 1) ^ 1, abort_flag, lim)) {
+                                ok = false;
+                                break;
+                            }
+                        }
+                        ptx::tc_fence_after();
+#pragma unroll
+                        for (int kk = 0; kk < BN / 16; ++kk) {
+                            ptx::mma_ts(tmem + TM_O + h * HD, tmem + TM_S + h * BN + kk * 8,
+                                        ptx::smem_desc_sw128(vtile + kk * 2048, HALF_BYTES, 1024), IDESC_PV,
+                                        (!first_pv[h] || kk > 0) ? 1u : 0u);
+                        }
+                        first_pv[h] = false;
+                        const int tn = it.next(h, t);
+                        if (tn >= 0) {
+                            if (!issue_s(h, tn)) {
+                                ok = false;
+                                break;
+                            }
+                        } else {
+                            ptx::tc_commit(bar(B_PVDONE + h));
+                        }
+                    }
+                    if (!ok) break;
+                    ptx::tc_commit(bar(B_EMPTY + vslot));
+                }
+                ubase += 2 * it.T;
+                for (int h = 0; h < 2; ++h) n_half[h] += it.valid[h] ? 1 : 0;
             }
             // Whatever was issued must complete before tensor memory is freed.
             ptx::tc_commit(bar(B_DRAIN));
             volatile int never = 0;
-            ptx::wait_bounded(bar(B_DRAIN), 0, &never, p.wait_limit_ns);
+            ptx::wait_bounded(bar(B_DRAIN), 0, &never, lim);
         }
         __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax + epilogue
-        const int quarter = warp & 3;  // TMEM lane quarter this warp may access
+        const int h = (warp - 2) >> 2;  // half
+        const int quarter = warp & 3;   // TMEM lane quarter this warp may access
         const int row = quarter * 32 + lane;
-        const int i = tr.i0 + row;
         const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-        const int lo_i = lo_of(i, p.w);
-        const int nc_i = lo_i / p.g;
-        float m = -INFINITY;  // running max of the log2-scaled logits
-        float l = 0.f;
+        const uint32_t tS = tmem + lane_addr + TM_S + h * BN;
+        const uint32_t tO = tmem + lane_addr + TM_O + h * HD;
+        uint32_t sf_cnt = 0;
+        int n_done = 0;  // items of this half finished
         bool ok = true;
-        for (int t = 0; t < T && ok; ++t) {
-            const int sb = t & 1;
-            // Waits are made warp-uniform: the tcgen05.ld/st that follow are warp-collective.
-            if (!__all_sync(0xffffffffu, ptx::wait_bounded(bar(B_SFULL + sb), (t >> 1) & 1, abort_flag,
-                                                            p.wait_limit_ns))) {
-                ok = false;
-                break;
-            }
-            ptx::tc_fence_after();
-            uint32_t s[4][32];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tmem + lane_addr + TM_S0 + sb * BN + c * 32, s[c]);
-            ptx::tmem_wait_ld(s[0]);
-            ptx::reg_touch(s[1]);
-            ptx::reg_touch(s[2]);
-            ptx::reg_touch(s[3]);
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(bar(B_SFREE + sb));
-
-            // visibility window of this row within the tile: columns [c_lo, c_hi]
-            const bool core = t < tr.Tc;
-            int c_lo = 0, c_hi = BN - 1;
-            bool masked;
-            if (core) {
-                const int y0 = t * BN;
-                masked = y0 + BN > tr.nc_min;
-                c_hi = min(nc_i - y0, BN) - 1;
-            } else {
-                const int y0 = tr.lo0 + (t - tr.Tc) * BN;
-                masked = (y0 < tr.lo1) || (y0 + BN - 1 > tr.i0);
-                c_lo = max(lo_i - y0, 0);
-                c_hi = min(i - y0, BN - 1);
-            }
-            float mx = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-#pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    const int col = c * 32 + k;
-                    float x = __uint_as_float(s[c][k]);
-                    if (masked && (col < c_lo || col > c_hi)) x = -INFINITY;
-                    s[c][k] = __float_as_uint(x);
-                    mx = fmaxf(mx, x);
-                }
-            }
-            const float m_tile = mx * p.scale_log2;  // -inf stays -inf
-            const float m_new = fmaxf(m, m_tile);
-            bool rescale = false;
-            if (m == -INFINITY) {
-                m = m_new;  // nothing accumulated yet for this row
-            } else if (m_new > m + LAZY_RESCALE_LOG2) {
-                rescale = true;
-            }
-            if (__any_sync(0xffffffffu, rescale)) {
-                // O holds the sum up to tile t-1: wait for that PV, then rescale in place.
-                if (!__all_sync(0xffffffffu, ptx::wait_bounded(bar(B_PVDONE + ((t - 1) & 1)), ((t - 1) >> 1) & 1,
-                                                                abort_flag, p.wait_limit_ns))) {
+        for (int k = blockIdx.x; ok && k < p.n_items; k += gridDim.x) {
+            const Item it = make_item(p, k);
+            if (!it.valid[h]) continue;
+            const int i = it.a[h] + row;
+            const int lo_i = lo_of(i, p.w);
+            const int nc_i = lo_i / p.g;
+            const int nc_first = lo_of(it.a[h], p.w) / p.g;
+            const int lo_last = lo_of(it.b[h], p.w);
+            float m = -INFINITY;  // running max of the log2-scaled logits
+            float l = 0.f;
+            for (int t = it.first(h); t >= 0; t = it.next(h, t)) {
+                if (!__all_sync(0xffffffffu, ptx::wait_bounded(bar(B_SFULL + h), sf_cnt & 1, abort_flag, lim))) {
                     ok = false;
                     break;
                 }
+                ++sf_cnt;
                 ptx::tc_fence_after();
-                const float f = rescale ? ptx::ex2(m - m_new) : 1.f;
+                uint32_t s[4][32];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tS + c * 32, s[c]);
+                ptx::tmem_wait_ld(s[0]);
+                ptx::reg_touch(s[1]);
+                ptx::reg_touch(s[2]);
+                ptx::reg_touch(s[3]);
+
+                // visibility window of this row within the tile: columns [c_lo, c_hi]
+                int c_lo = 0, c_hi = BN - 1;
+                bool masked;
+                if (t < it.Tc) {
+                    const int y0 = t * BN;
+                    masked = y0 + BN > nc_first;
+                    c_hi = min(nc_i - y0, BN) - 1;
+                } else {
+                    const int y0 = it.lo0 + (t - it.Tc) * BN;
+                    masked = (y0 < lo_last) || (y0 + BN - 1 > it.a[h]);
+                    c_lo = max(lo_i - y0, 0);
+                    c_hi = min(i - y0, BN - 1);
+                }
+                // row max with eight independent partial maxima (short dependency chains)
+                float mp[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) mp[q] = -INFINITY;
+                if (masked) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+#pragma unroll
+                        for (int kk = 0; kk < 32; ++kk) {
+                            const int col = c * 32 + kk;
+                            float x = __uint_as_float(s[c][kk]);
+                            x = (col < c_lo || col > c_hi) ? -INFINITY : x;
+                            s[c][kk] = __float_as_uint(x);
+                            mp[kk & 7] = fmaxf(mp[kk & 7], x);
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+#pragma unroll
+                        for (int kk = 0; kk < 32; ++kk) mp[kk & 7] = fmaxf(mp[kk & 7], __uint_as_float(s[c][kk]));
+                    }
+                }
+                const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                                       fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+                const float m_tile = mx * p.scale_log2;  // -inf stays -inf
+                const float m_new = fmaxf(m, m_tile);
+                bool rescale = false;
+                if (m == -INFINITY) {
+                    m = m_new;  // nothing accumulated yet for this row
+                } else if (m_new > m + LAZY_RESCALE_LOG2) {
+                    rescale = true;
+                }
+                if (__any_sync(0xffffffffu, rescale)) {
+                    // S_h complete => every earlier PV of this half is complete: O_h is stable.
+                    const float f = rescale ? ptx::ex2(m - m_new) : 1.f;
+#pragma unroll 1
+                    for (int c = 0; c < 8; ++c) {
+                        uint32_t o[16];
+                        ptx::tmem_ld16(tO + c * 16, o);
+                        ptx::tmem_wait_ld16(o);
+#pragma unroll
+                        for (int kk = 0; kk < 16; ++kk) o[kk] = __float_as_uint(__uint_as_float(o[kk]) * f);
+                        ptx::tmem_st16(tO + c * 16, o);
+                    }
+                    if (rescale) {
+                        l *= f;
+                        m = m_new;
+                    }
+                }
+                const float mu = (m == -INFINITY) ? 0.f : m;
+                float lp[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) lp[q] = 0.f;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    uint32_t o[32];
-                    ptx::tmem_ld32(tmem + lane_addr + TM_O + c * 32, o);
-                    ptx::tmem_wait_ld(o);
+                    uint32_t pk[16];
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * f);
-                    ptx::tmem_st32(tmem + lane_addr + TM_O + c * 32, o);
+                    for (int kk = 0; kk < 16; ++kk) {
+                        const float p0 = ptx::ex2(fmaf(__uint_as_float(s[c][2 * kk]), p.scale_log2, -mu));
+                        const float p1 = ptx::ex2(fmaf(__uint_as_float(s[c][2 * kk + 1]), p.scale_log2, -mu));
+                        lp[(2 * kk) & 7] += p0;
+                        lp[(2 * kk + 1) & 7] += p1;
+                        pk[kk] = ptx::pack_bf16x2(p0, p1);
+                    }
+                    ptx::tmem_st16(tS + c * 16, pk);  // P_h over the consumed columns of S_h
                 }
+                l += ((lp[0] + lp[1]) + (lp[2] + lp[3])) + ((lp[4] + lp[5]) + (lp[6] + lp[7]));
                 ptx::tmem_wait_st();
-                if (rescale) {
-                    l *= f;
-                    m = m_new;
-                }
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(bar(B_PFULL + h));
             }
-            const float mu = (m == -INFINITY) ? 0.f : m;
-            // P buffer sb was last read by the PV of tile t-2.
-            if (t >= 2 && !__all_sync(0xffffffffu, ptx::wait_bounded(bar(B_PVDONE + sb), ((t - 2) >> 1) & 1,
-                                                                      abort_flag, p.wait_limit_ns))) {
+            if (!ok) break;
+            // ---- epilogue: O_h / l -> bf16, LSE
+            if (!__all_sync(0xffffffffu, ptx::wait_bounded(bar(B_PVDONE + h), n_done & 1, abort_flag, lim))) {
                 ok = false;
                 break;
             }
             ptx::tc_fence_after();
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const float p0 = ptx::ex2(fmaf(__uint_as_float(s[c][2 * k]), p.scale_log2, -mu));
-                    const float p1 = ptx::ex2(fmaf(__uint_as_float(s[c][2 * k + 1]), p.scale_log2, -mu));
-                    l += p0 + p1;
-                    pk[k] = ptx::pack_bf16x2(p0, p1);
-                }
-                ptx::tmem_st16(tmem + lane_addr + TM_P0 + sb * 64 + c * 16, pk);
-            }
-            ptx::tmem_wait_st();
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(bar(B_PFULL + sb));
-        }
-        if (ok && __all_sync(0xffffffffu, ptx::wait_bounded(bar(B_PVDONE + ((T - 1) & 1)), ((T - 1) >> 1) & 1,
-                                                             abort_flag, p.wait_limit_ns))) {
-            ptx::tc_fence_after();
             const bool valid = i < p.N;
             const float inv = 1.f / l;
-            __nv_bfloat16 *orow = p.O + (static_cast<int64_t>(bh) * p.N + i) * HD;
+            __nv_bfloat16 *orow = p.O + (static_cast<int64_t>(it.bh) * p.N + i) * HD;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t o[32];
-                ptx::tmem_ld32(tmem + lane_addr + TM_O + c * 32, o);
+                ptx::tmem_ld32(tO + c * 32, o);
                 ptx::tmem_wait_ld(o);
                 uint4 v[4];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    v[k].x = ptx::pack_bf16x2(__uint_as_float(o[8 * k + 0]) * inv, __uint_as_float(o[8 * k + 1]) * inv);
-                    v[k].y = ptx::pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv, __uint_as_float(o[8 * k + 3]) * inv);
-                    v[k].z = ptx::pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv, __uint_as_float(o[8 * k + 5]) * inv);
-                    v[k].w = ptx::pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv, __uint_as_float(o[8 * k + 7]) * inv);
+                for (int q = 0; q < 4; ++q) {
+                    v[q].x = ptx::pack_bf16x2(__uint_as_float(o[8 * q + 0]) * inv, __uint_as_float(o[8 * q + 1]) * inv);
+                    v[q].y = ptx::pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
+                    v[q].z = ptx::pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv);
+                    v[q].w = ptx::pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
                 }
                 if (valid) {
                     uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) dst[k] = v[k];
+                    for (int q = 0; q < 4; ++q) dst[q] = v[q];
                 }
             }
-            if (valid) p.LSE[static_cast<int64_t>(bh) * p.N + i] = (m + __log2f(l)) * 0.6931471805599453f;
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar(B_OFREE + h));
+            if (valid) p.LSE[static_cast<int64_t>(it.bh) * p.N + i] = (m + __log2f(l)) * 0.6931471805599453f;
+            ++n_done;
         }
     }
 
@@ -439,6 +539,26 @@ bool encode_3d(EncodeTiledFn enc, CUtensorMap *map, const void *ptr, uint64_t ro
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+struct DeviceInfo {
+    bool ready = false;
+    int sms = 0;
+    cudaError_t attr_err = cudaSuccess;
+};
+
+DeviceInfo &device_info(int dev) {
+    static DeviceInfo info[64];
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lock(mu);
+    DeviceInfo &d = info[dev & 63];
+    if (!d.ready) {
+        cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+        d.attr_err = cudaFuncSetAttribute(attn_bf16_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          static_cast<int>(SMEM_BYTES));
+        d.ready = true;
+    }
+    return d;
+}
+
 }  // namespace
 
 // Test hooks (see cca_test_* in cca_api.cu).
@@ -449,20 +569,17 @@ cudaError_t launch_attn_bf16_tc(const void *Q, const void *K, const void *V, con
                                 void *O, float *LSE, const Shape &s, int32_t *dev_status, cudaStream_t stream) {
     EncodeTiledFn enc = get_encoder();
     if (enc == nullptr) return cudaErrorNotSupported;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const DeviceInfo &di = device_info(dev);
+    if (di.attr_err != cudaSuccess) return di.attr_err;
     const uint64_t G = static_cast<uint64_t>(s.N / s.g);
     CUtensorMap mQ, mK, mV, mKc, mVc;
     const uint64_t qh = static_cast<uint64_t>(s.B) * s.Hq, kh = static_cast<uint64_t>(s.B) * s.Hkv;
     if (!encode_3d(enc, &mQ, Q, s.N, qh) || !encode_3d(enc, &mK, K, s.N, kh) || !encode_3d(enc, &mV, V, s.N, kh) ||
         !encode_3d(enc, &mKc, Kc, G, kh) || !encode_3d(enc, &mVc, Vc, G, kh))
         return cudaErrorInvalidValue;
-
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(attn_bf16_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        static_cast<int>(SMEM_BYTES));
-    });
-    if (attr_err != cudaSuccess) return attr_err;
 
     Params p;
     p.B = s.B;
@@ -471,14 +588,15 @@ cudaError_t launch_attn_bf16_tc(const void *Q, const void *K, const void *V, con
     p.N = s.N;
     p.g = s.g;
     p.w = s.w;
-    p.n_qtiles = (s.N + BM - 1) / BM;
+    p.n_pairs = (s.N + 2 * BM - 1) / (2 * BM);
+    p.n_items = p.n_pairs * s.B * s.Hq;
     p.scale_log2 = s.scale * 1.4426950408889634f;
     p.O = static_cast<__nv_bfloat16 *>(O);
     p.LSE = LSE;
     p.status = dev_status;
     p.wait_limit_ns = g_wait_limit_ns;
     p.skip_q_load = g_skip_q_load;
-    const unsigned grid = static_cast<unsigned>(static_cast<uint64_t>(p.n_qtiles) * s.B * s.Hq);
+    const unsigned grid = static_cast<unsigned>(p.n_items < di.sms ? p.n_items : di.sms);
     attn_bf16_tc_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(mQ, mK, mV, mKc, mVc, p);
     return cudaGetLastError();
 }

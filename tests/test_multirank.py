@@ -1,0 +1,54 @@
+"""Host logic of the multi-rank benchmark path on CPU (gloo, world size 2):
+ranks are independent replicas, the job time is the slowest rank's, and the
+job throughput counts every rank's tokens."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    ms = [120.0, 180.0][rank]
+    job_ms = bench.max_over_ranks(ms, world, torch.device("cpu"))
+    per_step, value = bench.job_throughput(job_ms, 10, 32768, world)
+    q.put((rank, job_ms, per_step, value, bench.dist_env()))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_two_rank_timing_and_throughput():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, job_ms, per_step, value, env in res:
+        assert job_ms == 180.0
+        assert per_step == pytest.approx(18.0)
+        assert value == pytest.approx(2 * 32768 / 0.018)
+        assert env == (rank, 2, 0)
+
+
+def test_single_rank_is_identity():
+    assert bench.max_over_ranks(12.5, 1, torch.device("cpu")) == 12.5
+    assert bench.job_throughput(100.0, 10, 1000, 1) == (10.0, pytest.approx(1000 / 0.01))
