@@ -92,31 +92,55 @@ struct Params {
 
 __device__ __forceinline__ int lo_of(int i, int w) { return i - w + 1 > 0 ? i - w + 1 : 0; }
 
-// The tile sequence of one work item and which half uses which tile.
+// The tile sequence of one work item and which half uses which tile.  Per-half
+// fields are scalars chosen with selects (no runtime-indexed arrays, which
+// would live in local memory).
+struct Half {
+    int a, b;     // first / last valid row
+    bool valid;
+    int tc;       // core tiles used: [0, tc)
+    int kl, kh;   // local tiles used: [kl, kh)
+};
+
 struct Item {
     int bh, kvz;
-    int a[2], b[2];     // first / last valid row of each half
-    bool valid[2];
-    int tc[2];          // core tiles used by each half: [0, tc[h])
-    int Tc;             // core tiles loaded (max of tc)
-    int lo0;            // first key of local tile 0
-    int kl[2], kh[2];   // local tiles used by each half: [kl, kh)
-    int T;              // tiles loaded
+    Half hA, hB;
+    int Tc;   // core tiles loaded (max of the halves' tc)
+    int lo0;  // first key of local tile 0
+    int T;    // tiles loaded
 
-    __device__ __forceinline__ bool uses(int h, int t) const {
-        if (!valid[h]) return false;
-        if (t < Tc) return t < tc[h];
-        const int k = t - Tc;
-        return k >= kl[h] && k < kh[h];
-    }
-    __device__ __forceinline__ int first(int h) const { return tc[h] > 0 ? 0 : Tc + kl[h]; }
-    // next used tile after t, or -1
-    __device__ __forceinline__ int next(int h, int t) const {
-        if (t < Tc) return (t + 1 < tc[h]) ? t + 1 : Tc + kl[h];
-        return (t + 1 < Tc + kh[h]) ? t + 1 : -1;
-    }
-    __device__ __forceinline__ int count(int h) const { return valid[h] ? tc[h] + kh[h] - kl[h] : 0; }
+    __device__ __forceinline__ const Half &half(int h) const { return h ? hB : hA; }
 };
+
+__device__ __forceinline__ bool half_uses(const Half &x, int Tc, int t) {
+    if (!x.valid) return false;
+    if (t < Tc) return t < x.tc;
+    const int k = t - Tc;
+    return k >= x.kl && k < x.kh;
+}
+__device__ __forceinline__ int half_first(const Half &x, int Tc) { return x.tc > 0 ? 0 : Tc + x.kl; }
+// next used tile after t, or -1
+__device__ __forceinline__ int half_next(const Half &x, int Tc, int t) {
+    if (t < Tc) return (t + 1 < x.tc) ? t + 1 : Tc + x.kl;
+    return (t + 1 < Tc + x.kh) ? t + 1 : -1;
+}
+__device__ __forceinline__ int half_count(const Half &x) { return x.valid ? x.tc + x.kh - x.kl : 0; }
+
+__device__ __forceinline__ Half make_half(const Params &p, int a, int lo0) {
+    Half x;
+    x.a = a;
+    x.valid = a < p.N;
+    x.b = min(a + BM - 1, p.N - 1);
+    if (!x.valid) {
+        x.tc = x.kl = x.kh = 0;
+        return x;
+    }
+    const int nc = lo_of(x.b, p.w) / p.g;
+    x.tc = (nc + BN - 1) / BN;
+    x.kl = (lo_of(a, p.w) - lo0) / BN;
+    x.kh = (x.b - lo0) / BN + 1;
+    return x;
+}
 
 __device__ __forceinline__ Item make_item(const Params &p, int k) {
     Item it;
@@ -126,28 +150,12 @@ __device__ __forceinline__ Item make_item(const Params &p, int k) {
     const int b = it.bh / p.Hq, h = it.bh % p.Hq;
     it.kvz = b * p.Hkv + h / (p.Hq / p.Hkv);
     const int i0 = pair * 2 * BM;
-    for (int hh = 0; hh < 2; ++hh) {
-        it.a[hh] = i0 + hh * BM;
-        it.valid[hh] = it.a[hh] < p.N;
-        it.b[hh] = min(it.a[hh] + BM - 1, p.N - 1);
-    }
-    it.lo0 = lo_of(it.a[0], p.w);
-    const int last = it.valid[1] ? it.b[1] : it.b[0];
-    const int Tl = (last - it.lo0) / BN + 1;
-    it.Tc = 0;
-    for (int hh = 0; hh < 2; ++hh) {
-        if (!it.valid[hh]) {
-            it.tc[hh] = 0;
-            it.kl[hh] = it.kh[hh] = 0;
-            continue;
-        }
-        const int nc = lo_of(it.b[hh], p.w) / p.g;
-        it.tc[hh] = (nc + BN - 1) / BN;
-        it.Tc = max(it.Tc, it.tc[hh]);
-        it.kl[hh] = (lo_of(it.a[hh], p.w) - it.lo0) / BN;
-        it.kh[hh] = (it.b[hh] - it.lo0) / BN + 1;
-    }
-    it.T = it.Tc + Tl;
+    it.lo0 = lo_of(i0, p.w);
+    it.hA = make_half(p, i0, it.lo0);
+    it.hB = make_half(p, i0 + BM, it.lo0);
+    const int last = it.hB.valid ? it.hB.b : it.hA.b;
+    it.Tc = max(it.hA.tc, it.hB.tc);
+    it.T = it.Tc + (last - it.lo0) / BN + 1;
     return it;
 }
 
@@ -215,8 +223,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     ptx::mbar_arrive_expect_tx(bar(B_QFULL), 2 * TILE_BYTES);
                     for (int h = 0; h < 2; ++h) {
                         const uint32_t dst = base + OFF_Q + h * TILE_BYTES;
-                        ptx::tma_load_3d(&tmQ, bar(B_QFULL), dst, 0, it.a[h], it.bh);
-                        ptx::tma_load_3d(&tmQ, bar(B_QFULL), dst + HALF_BYTES, 64, it.a[h], it.bh);
+                        const int row0 = h ? it.hB.a : it.hA.a;
+                        ptx::tma_load_3d(&tmQ, bar(B_QFULL), dst, 0, row0, it.bh);
+                        ptx::tma_load_3d(&tmQ, bar(B_QFULL), dst + HALF_BYTES, 64, row0, it.bh);
                     }
                 }
                 for (int t = 0; ok && t < it.T; ++t) {
@@ -257,14 +266,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int k = blockIdx.x; ok && k < p.n_items; k += gridDim.x, ++n_iter) {
                 const Item it = make_item(p, k);
                 if (!ptx::wait_bounded(bar(B_QFULL), n_iter & 1, abort_flag, lim)) break;
-                int s_left = it.count(0) + it.count(1);
+                int s_left = half_count(it.hA) + half_count(it.hB);
                 // S_h = Q_h K(t)^T into S_h.  The first user of a ring slot waits for the copy.
                 auto issue_s = [&](int h, int t) -> bool {
                     const uint32_t uk = ubase + 2 * t;
                     const int slot = uk % NS;
                     if (kpend[slot] == 0) {
                         if (!ptx::wait_bounded(bar(B_FULL + slot), (uk / NS) & 1, abort_flag, lim)) return false;
-                        kpend[slot] = (it.uses(0, t) ? 1 : 0) + (it.uses(1, t) ? 1 : 0);
+                        kpend[slot] = (half_uses(it.hA, it.Tc, t) ? 1 : 0) + (half_uses(it.hB, it.Tc, t) ? 1 : 0);
                     }
                     ptx::tc_fence_after();
                     const uint32_t tile = base + OFF_RING + slot * TILE_BYTES;
@@ -283,10 +292,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 // Prologue: first S of each half, earliest tile first, so that the issuer
                 // never waits on a copy that sits behind one it has not consumed yet.
                 {
-                    const bool b_first = it.valid[1] && it.first(1) < it.first(0);
+                    const bool b_first = it.hB.valid && half_first(it.hB, it.Tc) < half_first(it.hA, it.Tc);
                     for (int q = 0; ok && q < 2; ++q) {
                         const int h = b_first ? 1 - q : q;
-                        if (it.valid[h]) ok = issue_s(h, it.first(h));
+                        const Half &x = it.half(h);
+                        if (x.valid) ok = issue_s(h, half_first(x, it.Tc));
                     }
                 }
                 bool first_pv[2] = {true, true};
@@ -299,7 +309,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                     const uint32_t vtile = base + OFF_RING + vslot * TILE_BYTES;
                     for (int h = 0; h < 2; ++h) {
-                        if (!it.uses(h, t)) continue;
+                        const Half &x = it.half(h);
+                        if (!half_uses(x, it.Tc, t)) continue;
                         if (!ptx::wait_bounded(bar(B_PFULL + h), pf_cnt[h] & 1, abort_flag, lim)) {
                             ok = false;
                             break;
@@ -320,7 +331,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                         (!first_pv[h] || kk > 0) ? 1u : 0u);
                         }
                         first_pv[h] = false;
-                        const int tn = it.next(h, t);
+                        const int tn = half_next(x, it.Tc, t);
                         if (tn >= 0) {
                             if (!issue_s(h, tn)) {
                                 ok = false;
@@ -334,7 +345,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     ptx::tc_commit(bar(B_EMPTY + vslot));
                 }
                 ubase += 2 * it.T;
-                for (int h = 0; h < 2; ++h) n_half[h] += it.valid[h] ? 1 : 0;
+                n_half[0] += it.hA.valid ? 1 : 0;
+                n_half[1] += it.hB.valid ? 1 : 0;
             }
             // Whatever was issued must complete before tensor memory is freed.
             ptx::tc_commit(bar(B_DRAIN));
@@ -355,15 +367,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         bool ok = true;
         for (int k = blockIdx.x; ok && k < p.n_items; k += gridDim.x) {
             const Item it = make_item(p, k);
-            if (!it.valid[h]) continue;
-            const int i = it.a[h] + row;
+            const Half x = h ? it.hB : it.hA;
+            if (!x.valid) continue;
+            const int i = x.a + row;
             const int lo_i = lo_of(i, p.w);
             const int nc_i = lo_i / p.g;
-            const int nc_first = lo_of(it.a[h], p.w) / p.g;
-            const int lo_last = lo_of(it.b[h], p.w);
+            const int nc_first = lo_of(x.a, p.w) / p.g;
+            const int lo_last = lo_of(x.b, p.w);
             float m = -INFINITY;  // running max of the log2-scaled logits
             float l = 0.f;
-            for (int t = it.first(h); t >= 0; t = it.next(h, t)) {
+            for (int t = half_first(x, it.Tc); t >= 0; t = half_next(x, it.Tc, t)) {
                 if (!__all_sync(0xffffffffu, ptx::wait_bounded(bar(B_SFULL + h), sf_cnt & 1, abort_flag, lim))) {
                     ok = false;
                     break;
@@ -387,35 +400,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     c_hi = min(nc_i - y0, BN) - 1;
                 } else {
                     const int y0 = it.lo0 + (t - it.Tc) * BN;
-                    masked = (y0 < lo_last) || (y0 + BN - 1 > it.a[h]);
+                    masked = (y0 < lo_last) || (y0 + BN - 1 > x.a);
                     c_lo = max(lo_i - y0, 0);
                     c_hi = min(i - y0, BN - 1);
                 }
-                // row max with eight independent partial maxima (short dependency chains)
+                // row max: 3-input max over eight independent partial maxima
                 float mp[8];
-#pragma unroll
-                for (int q = 0; q < 8; ++q) mp[q] = -INFINITY;
                 if (masked) {
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
 #pragma unroll
                         for (int kk = 0; kk < 32; ++kk) {
                             const int col = c * 32 + kk;
-                            float x = __uint_as_float(s[c][kk]);
-                            x = (col < c_lo || col > c_hi) ? -INFINITY : x;
-                            s[c][kk] = __float_as_uint(x);
-                            mp[kk & 7] = fmaxf(mp[kk & 7], x);
+                            const float x = __uint_as_float(s[c][kk]);
+                            s[c][kk] = __float_as_uint((col < c_lo || col > c_hi) ? -INFINITY : x);
                         }
                     }
-                } else {
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-#pragma unroll
-                        for (int kk = 0; kk < 32; ++kk) mp[kk & 7] = fmaxf(mp[kk & 7], __uint_as_float(s[c][kk]));
-                    }
                 }
-                const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
-                                       fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    mp[q] = fmaxf(__uint_as_float(s[q >> 1][(q & 1) * 16]), __uint_as_float(s[q >> 1][(q & 1) * 16 + 1]));
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+#pragma unroll
+                    for (int kk = 2; kk < 16; kk += 2)
+                        mp[q] = ptx::max3(mp[q], __uint_as_float(s[q >> 1][(q & 1) * 16 + kk]),
+                                          __uint_as_float(s[q >> 1][(q & 1) * 16 + kk + 1]));
+                }
+                const float mx = ptx::max3(ptx::max3(mp[0], mp[1], mp[2]), ptx::max3(mp[3], mp[4], mp[5]),
+                                           fmaxf(mp[6], mp[7]));
                 const float m_tile = mx * p.scale_log2;  // -inf stays -inf
                 const float m_new = fmaxf(m, m_tile);
                 bool rescale = false;
@@ -442,23 +455,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 }
                 const float mu = (m == -INFINITY) ? 0.f : m;
-                float lp[8];
+                // p = 2^(s*scale - mu), two columns per packed FMA; row sum in four packed partials
+                const uint64_t sc2 = ptx::f2(p.scale_log2, p.scale_log2);
+                const uint64_t nm2 = ptx::f2(-mu, -mu);
+                uint64_t lp[2] = {0, 0};
 #pragma unroll
-                for (int q = 0; q < 8; ++q) lp[q] = 0.f;
+                for (int c = 0; c < 8; ++c) {
+                    uint32_t pk[8];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int kk = 0; kk < 16; ++kk) {
-                        const float p0 = ptx::ex2(fmaf(__uint_as_float(s[c][2 * kk]), p.scale_log2, -mu));
-                        const float p1 = ptx::ex2(fmaf(__uint_as_float(s[c][2 * kk + 1]), p.scale_log2, -mu));
-                        lp[(2 * kk) & 7] += p0;
-                        lp[(2 * kk + 1) & 7] += p1;
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const int col = (c & 1) * 16 + 2 * kk;
+                        const uint64_t x2 = ptx::fma2(
+                            ptx::f2(__uint_as_float(s[c >> 1][col]), __uint_as_float(s[c >> 1][col + 1])), sc2, nm2);
+                        float x0, x1;
+                        ptx::f2_split(x2, x0, x1);
+                        const float p0 = ptx::ex2(x0);
+                        const float p1 = ptx::ex2(x1);
+                        lp[kk & 1] = ptx::add2(lp[kk & 1], ptx::f2(p0, p1));
                         pk[kk] = ptx::pack_bf16x2(p0, p1);
                     }
-                    ptx::tmem_st16(tS + c * 16, pk);  // P_h over the consumed columns of S_h
+                    ptx::tmem_st8(tS + c * 8, pk);  // P_h over the consumed columns of S_h
                 }
-                l += ((lp[0] + lp[1]) + (lp[2] + lp[3])) + ((lp[4] + lp[5]) + (lp[6] + lp[7]));
+                {
+                    float a0, a1, b0, b1;
+                    ptx::f2_split(lp[0], a0, a1);
+                    ptx::f2_split(lp[1], b0, b1);
+                    l += (a0 + a1) + (b0 + b1);
+                }
                 ptx::tmem_wait_st();
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(bar(B_PFULL + h));

@@ -74,8 +74,10 @@ int cca_pool(const void *Q, const void *K, const void *V, void *Kc, void *Vc, co
     const void *ptrs[5] = {Q, K, V, Kc, Vc};
     for (const void *q : ptrs)
         if (q == nullptr || !aligned16(q)) return CCA_ERR_INVALID_ARG;
+    if (params->dev_status != nullptr && (reinterpret_cast<uintptr_t>(params->dev_status) & 3u) != 0)
+        return CCA_ERR_INVALID_ARG;
     if ((st = check_device()) != CCA_OK) return st;
-    return from_cuda(cca::launch_pool(params->dtype, Q, K, V, Kc, Vc, to_shape(params),
+    return from_cuda(cca::launch_pool(params->dtype, Q, K, V, Kc, Vc, to_shape(params), params->dev_status,
                                       static_cast<cudaStream_t>(stream)));
 }
 

@@ -12,9 +12,10 @@ struct Shape {
     float scale;  // resolved softmax scale (> 0)
 };
 
-// Global-aware pooling. dtype: 0 = bf16, 1 = f32.
+// Global-aware pooling. dtype: 0 = bf16, 1 = f32.  `status` (optional device
+// int32) receives CCA_ERR_TIMEOUT if a copy wait runs out.
 cudaError_t launch_pool(int dtype, const void *Q, const void *K, const void *V, void *Kc, void *Vc,
-                        const Shape &s, cudaStream_t stream);
+                        const Shape &s, int32_t *status, cudaStream_t stream);
 
 // fp32 fused attention on CUDA cores (any supported d).
 cudaError_t launch_attn_f32(const float *Q, const float *K, const float *V, const float *Kc,

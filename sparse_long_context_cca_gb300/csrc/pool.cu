@@ -5,14 +5,21 @@
 // q_last is the query of the group's last token (for grouped-query attention,
 // the mean of the logits of the query heads sharing the KV head).
 //
-// Memory-bound: 6*g*d flops per 4*g*d bytes.  One warp owns one group.  Each
-// lane holds one 16-byte vector of a row (d=128 bf16: 16 lanes per row, two
-// rows per warp-wide load), issues every load of a chunk of rows before any
-// arithmetic, reduces the dot products with shuffles, and keeps a running
-// (max, sum) so that any g streams through registers in chunks.
+// Memory-bound (6*g*d flops per 4*g*d bytes), so the design is about bytes in
+// flight.  A persistent grid of one CTA per SM; every warp owns a strided list of
+// groups and streams them as "chunks" of up to RS rows (RS*d*e = 4 KB of K and
+// 4 KB of V, plus the r group-last query rows with a group's first chunk).
+// Each warp feeds its own ring of S shared-memory stages with cp.async.bulk
+// copies (one elected lane issues them), so several chunks per warp are in
+// flight without holding registers, and the arithmetic on chunk c overlaps the
+// copies of chunks c+1 .. c+S-1.  Within a chunk a lane holds one 16-byte
+// vector of a row; logits are reduced with shuffles and a running (max, sum)
+// carries a group across chunks, so any g works.  Outputs are 16-byte stores.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <mutex>
 
 #include "internal.h"
 #include "sm100_ptx.cuh"
@@ -21,14 +28,11 @@ namespace cca {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
-
-__device__ __forceinline__ uint4 ld_nc16(const void *p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
+constexpr int NW_MAX = 12;                 // warps per CTA (each feeds and consumes its own ring)
+constexpr int S_MAX = 4;                   // ring stages per warp
+constexpr uint32_t CHUNK_BYTES = 4096;     // bytes of K (and of V) per chunk
+constexpr uint32_t SMEM_BUDGET = 224 * 1024;
+constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;
 
 template <typename T>
 struct VecTraits;
@@ -69,68 +73,124 @@ struct VecTraits<float> {
     }
 };
 
-// ITERS warp-wide row loads are in flight per chunk (RPI rows each).
-template <typename T, int D, int ITERS>
-__global__ void __launch_bounds__(256) pool_kernel(const T *__restrict__ Q, const T *__restrict__ K,
-                                                   const T *__restrict__ V, T *__restrict__ Kc,
-                                                   T *__restrict__ Vc, int Hq, int Hkv, int N, int g,
-                                                   float logit_scale, int64_t n_groups_total) {
-    using VT = VecTraits<T>;
-    constexpr int E = VT::E;        // elements per 16-byte vector
-    constexpr int LPR = D / E;      // lanes per row
-    constexpr int RPI = 32 / LPR;   // rows per warp-wide load
-    static_assert(LPR >= 1 && LPR <= 32 && 32 % LPR == 0, "unsupported head dim");
+struct PoolArgs {
+    int Hq, Hkv, N, g, r;
+    int S;                 // ring stages per warp
+    uint32_t stage_bytes;  // K chunk + V chunk + r query rows
+    float logit_scale;     // tau * log2(e) / r
+    int64_t n_groups;      // B * Hkv * (N / g)
+    int32_t *status;
+};
 
+__device__ __forceinline__ uint4 lds16(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(NW_MAX * 32) pool_kernel(const T *__restrict__ Q, const T *__restrict__ K,
+                                                       const T *__restrict__ V, T *__restrict__ Kc,
+                                                       T *__restrict__ Vc, const PoolArgs a) {
+    using VT = VecTraits<T>;
+    constexpr int E = VT::E;                 // elements per 16-byte vector
+    constexpr int LPR = D / E;               // lanes per row
+    constexpr int RPI = 32 / LPR;            // rows per warp-wide pass
+    constexpr uint32_t ROW_BYTES = D * sizeof(T);
+    constexpr int RS = CHUNK_BYTES / ROW_BYTES;  // rows per chunk
+    static_assert(LPR >= 1 && LPR <= 32 && 32 % LPR == 0 && RS % RPI == 0, "unsupported head dim");
+
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    __shared__ uint64_t bars[NW_MAX][S_MAX];
+    __shared__ int abort_flag;
     const int lane = threadIdx.x & 31;
+    const int wib = threadIdx.x >> 5;
     const int sub = lane / LPR;
     const int cl = lane % LPR;
-    const int64_t gw = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (gw >= n_groups_total) return;  // warp-uniform
+    if (threadIdx.x == 0) abort_flag = 0;
+    if (lane == 0)
+        for (int s = 0; s < a.S; ++s) ptx::mbar_init(ptx::smem_addr(&bars[wib][s]), 1);
+    ptx::fence_mbar_init();
+    __syncthreads();
 
-    const int G = N / g;
-    const int64_t j = gw % G;
-    const int64_t bk = gw / G;  // b * Hkv + kv
-    const int64_t b = bk / Hkv;
-    const int64_t kv = bk % Hkv;
-    const int r = Hq / Hkv;
+    const uint32_t ring = ptx::smem_addr(smem_raw) + wib * a.S * a.stage_bytes;
+    const int G = a.N / a.g;
+    const int nch = (a.g + RS - 1) / RS;  // chunks per group
+    const int nw = blockDim.x >> 5;
+    const int64_t tw = static_cast<int64_t>(gridDim.x) * nw;
+    const int64_t gw = static_cast<int64_t>(blockIdx.x) * nw + wib;
+    const int64_t my_groups = gw < a.n_groups ? (a.n_groups - 1 - gw) / tw + 1 : 0;
+    const int64_t n_chunks = my_groups * nch;
 
-    // Sum of the group-last queries of the r query heads; 1/r is in logit_scale.
-    float q[E];
-#pragma unroll
-    for (int e = 0; e < E; ++e) q[e] = 0.f;
-    const int64_t last = (j + 1) * g - 1;
-    for (int hh = 0; hh < r; ++hh) {
-        const T *qp = Q + ((b * Hq + kv * r + hh) * static_cast<int64_t>(N) + last) * D + cl * E;
-        float f[E];
-        VT::unpack(ld_nc16(qp), f);
-#pragma unroll
-        for (int e = 0; e < E; ++e) q[e] += f[e];
-    }
+    // lane 0: bring chunk c of this warp's stream into stage c % S
+    auto issue = [&](int64_t c) {
+        const int64_t gid = gw + (c / nch) * tw;
+        const int ch = static_cast<int>(c % nch);
+        const int64_t j = gid % G;
+        const int64_t bk = gid / G;
+        const int t0 = ch * RS;
+        const int rows = min(RS, a.g - t0);
+        const uint32_t stage = ring + static_cast<uint32_t>(c % a.S) * a.stage_bytes;
+        const uint32_t bar = ptx::smem_addr(&bars[wib][c % a.S]);
+        const uint32_t kv_bytes = rows * ROW_BYTES;
+        ptx::mbar_arrive_expect_tx(bar, 2 * kv_bytes + (ch == 0 ? a.r * ROW_BYTES : 0));
+        const int64_t row0 = bk * a.N + j * a.g + t0;
+        ptx::bulk_load(stage, K + row0 * D, kv_bytes, bar);
+        ptx::bulk_load(stage + CHUNK_BYTES, V + row0 * D, kv_bytes, bar);
+        if (ch == 0) {
+            const int64_t b = bk / a.Hkv, kv = bk % a.Hkv;
+            const int64_t last = (j + 1) * a.g - 1;
+            for (int hh = 0; hh < a.r; ++hh)
+                ptx::bulk_load(stage + 2 * CHUNK_BYTES + hh * ROW_BYTES,
+                               Q + ((b * a.Hq + kv * a.r + hh) * static_cast<int64_t>(a.N) + last) * D, ROW_BYTES,
+                               bar);
+        }
+    };
+    if (lane == 0)
+        for (int64_t c = 0; c < n_chunks && c < a.S; ++c) issue(c);
+    __syncwarp();
 
-    const T *Kg = K + (bk * N + j * g) * static_cast<int64_t>(D) + cl * E;
-    const T *Vg = V + (bk * N + j * g) * static_cast<int64_t>(D) + cl * E;
-
+    float q[E], ak[E], av[E];
     float m = -INFINITY, l = 0.f;
-    float ak[E], av[E];
+    int64_t c = 0;
+    for (; c < n_chunks; ++c) {
+        const int st = static_cast<int>(c % a.S);
+        const uint32_t stage = ring + st * a.stage_bytes;
+        volatile int *af = &abort_flag;
+        if (!__all_sync(kFull, ptx::wait_bounded(ptx::smem_addr(&bars[wib][st]), (c / a.S) & 1, af,
+                                                  WAIT_LIMIT_NS)))
+            break;
+        const int ch = static_cast<int>(c % nch);
+        const int t0 = ch * RS;
+        const int rows = min(RS, a.g - t0);
+        if (ch == 0) {
+            // new group: sum of the r group-last queries (1/r is in logit_scale)
 #pragma unroll
-    for (int e = 0; e < E; ++e) ak[e] = av[e] = 0.f;
-
-    for (int t0 = 0; t0 < g; t0 += RPI * ITERS) {
-        uint4 kr[ITERS], vr[ITERS];
+            for (int e = 0; e < E; ++e) q[e] = ak[e] = av[e] = 0.f;
+            m = -INFINITY;
+            l = 0.f;
+            for (int hh = 0; hh < a.r; ++hh) {
+                float f[E];
+                VT::unpack(lds16(stage + 2 * CHUNK_BYTES + hh * ROW_BYTES + cl * 16), f);
 #pragma unroll
-        for (int it = 0; it < ITERS; ++it) {
-            const int t = t0 + it * RPI + sub;
-            if (t < g) {
-                kr[it] = ld_nc16(Kg + static_cast<int64_t>(t) * D);
-                vr[it] = ld_nc16(Vg + static_cast<int64_t>(t) * D);
-            } else {
-                kr[it] = make_uint4(0, 0, 0, 0);
-                vr[it] = make_uint4(0, 0, 0, 0);
+                for (int e = 0; e < E; ++e) q[e] += f[e];
             }
         }
-        float s[ITERS];
+        constexpr int PASSES = RS / RPI;
+        uint4 kr[PASSES], vr[PASSES];
+        float s[PASSES];
 #pragma unroll
-        for (int it = 0; it < ITERS; ++it) {
+        for (int it = 0; it < PASSES; ++it) {
+            const int t = it * RPI + sub;
+            if (t < rows) {
+                kr[it] = lds16(stage + t * ROW_BYTES + cl * 16);
+                vr[it] = lds16(stage + CHUNK_BYTES + t * ROW_BYTES + cl * 16);
+            } else {
+                kr[it] = vr[it] = make_uint4(0, 0, 0, 0);
+            }
+        }
+#pragma unroll
+        for (int it = 0; it < PASSES; ++it) {
             float f[E];
             VT::unpack(kr[it], f);
             float p = 0.f;
@@ -138,12 +198,11 @@ __global__ void __launch_bounds__(256) pool_kernel(const T *__restrict__ Q, cons
             for (int e = 0; e < E; ++e) p = fmaf(q[e], f[e], p);
 #pragma unroll
             for (int o = LPR / 2; o > 0; o >>= 1) p += __shfl_xor_sync(kFull, p, o);
-            const int t = t0 + it * RPI + sub;
-            s[it] = (t < g) ? p * logit_scale : -INFINITY;  // log2 domain
+            s[it] = (it * RPI + sub < rows) ? p * a.logit_scale : -INFINITY;  // log2 domain
         }
         float cm = s[0];
 #pragma unroll
-        for (int it = 1; it < ITERS; ++it) cm = fmaxf(cm, s[it]);
+        for (int it = 1; it < PASSES; ++it) cm = fmaxf(cm, s[it]);
 #pragma unroll
         for (int o = LPR; o < 32; o <<= 1) cm = fmaxf(cm, __shfl_xor_sync(kFull, cm, o));
         const float mn = fmaxf(m, cm);  // finite: row t0 of the chunk is valid
@@ -155,7 +214,7 @@ __global__ void __launch_bounds__(256) pool_kernel(const T *__restrict__ Q, cons
             av[e] *= corr;
         }
 #pragma unroll
-        for (int it = 0; it < ITERS; ++it) {
+        for (int it = 0; it < PASSES; ++it) {
             const float p = ptx::ex2(s[it] - mn);
             l += p;
             float fk[E], fv[E];
@@ -168,60 +227,125 @@ __global__ void __launch_bounds__(256) pool_kernel(const T *__restrict__ Q, cons
             }
         }
         m = mn;
-    }
-    // Combine the RPI row-subgroups of the warp.
+        // every lane has read the stage: refill it with chunk c + S
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && c + a.S < n_chunks) issue(c + a.S);
+
+        if (ch == nch - 1) {
+            // group done: combine the RPI row-subgroups, normalise, store
+            float lt = l, kt[E], vt[E];
 #pragma unroll
-    for (int o = LPR; o < 32; o <<= 1) {
-        l += __shfl_xor_sync(kFull, l, o);
+            for (int e = 0; e < E; ++e) {
+                kt[e] = ak[e];
+                vt[e] = av[e];
+            }
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-            ak[e] += __shfl_xor_sync(kFull, ak[e], o);
-            av[e] += __shfl_xor_sync(kFull, av[e], o);
+            for (int o = LPR; o < 32; o <<= 1) {
+                lt += __shfl_xor_sync(kFull, lt, o);
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    kt[e] += __shfl_xor_sync(kFull, kt[e], o);
+                    vt[e] += __shfl_xor_sync(kFull, vt[e], o);
+                }
+            }
+            const float inv = 1.f / lt;
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                kt[e] *= inv;
+                vt[e] *= inv;
+            }
+            const int64_t gid = gw + (c / nch) * tw;
+            const int64_t orow = gid * static_cast<int64_t>(D) + cl * E;  // gid = (b*Hkv + kv)*G + j
+            if (RPI >= 2) {
+                if (sub == 0) *reinterpret_cast<uint4 *>(Kc + orow) = VT::pack(kt);
+                if (sub == 1) *reinterpret_cast<uint4 *>(Vc + orow) = VT::pack(vt);
+            } else {
+                *reinterpret_cast<uint4 *>(Kc + orow) = VT::pack(kt);
+                *reinterpret_cast<uint4 *>(Vc + orow) = VT::pack(vt);
+            }
         }
     }
-    const float inv = 1.f / l;
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-        ak[e] *= inv;
-        av[e] *= inv;
+    if (c < n_chunks) {
+        // gave up: let this warp's copies in flight land before the CTA exits
+        volatile int never = 0;
+        if (lane == 0) {
+            const int64_t end = (c + a.S < n_chunks) ? c + a.S : n_chunks;
+            for (int64_t x = c; x < end; ++x)
+                ptx::wait_bounded(ptx::smem_addr(&bars[wib][x % a.S]), (x / a.S) & 1, &never, WAIT_LIMIT_NS);
+            if (a.status != nullptr) atomicCAS(a.status, 0, static_cast<int32_t>(-4));
+        }
+        __syncwarp();
     }
-    const int64_t orow = (bk * G + j) * static_cast<int64_t>(D) + cl * E;
-    if (RPI >= 2) {
-        if (sub == 0) *reinterpret_cast<uint4 *>(Kc + orow) = VT::pack(ak);
-        if (sub == 1) *reinterpret_cast<uint4 *>(Vc + orow) = VT::pack(av);
-    } else {
-        *reinterpret_cast<uint4 *>(Kc + orow) = VT::pack(ak);
-        *reinterpret_cast<uint4 *>(Vc + orow) = VT::pack(av);
+}
+
+struct DevInfo {
+    bool ready = false;
+    int sms = 0;
+};
+
+int sm_count() {
+    static DevInfo info[64];
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    DevInfo &d = info[dev & 63];
+    if (!d.ready) {
+        cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+        d.ready = true;
     }
+    return d.sms;
 }
 
 template <typename T, int D>
 cudaError_t launch_typed(const void *Q, const void *K, const void *V, void *Kc, void *Vc, const Shape &s,
-                         cudaStream_t stream) {
-    constexpr int E = VecTraits<T>::E;
-    constexpr int RPI = 32 / (D / E);
-    constexpr int ITERS = RPI >= 4 ? 4 : 8;  // 16 rows per chunk (8 when one row per load)
-    const int64_t total = static_cast<int64_t>(s.B) * s.Hkv * (s.N / s.g);
-    const int warps_per_block = 8;
-    const int64_t blocks = (total + warps_per_block - 1) / warps_per_block;
-    const float log2e = 1.4426950408889634f;
-    const float logit_scale = s.scale * log2e / static_cast<float>(s.Hq / s.Hkv);
-    pool_kernel<T, D, ITERS><<<static_cast<unsigned>(blocks), warps_per_block * 32, 0, stream>>>(
-        static_cast<const T *>(Q), static_cast<const T *>(K), static_cast<const T *>(V),
-        static_cast<T *>(Kc), static_cast<T *>(Vc), s.Hq, s.Hkv, s.N, s.g, logit_scale, total);
+                         int32_t *status, cudaStream_t stream) {
+    constexpr uint32_t ROW = D * sizeof(T);
+    PoolArgs a;
+    a.Hq = s.Hq;
+    a.Hkv = s.Hkv;
+    a.N = s.N;
+    a.g = s.g;
+    a.r = s.Hq / s.Hkv;
+    a.stage_bytes = 2 * CHUNK_BYTES + static_cast<uint32_t>(a.r) * ROW;
+    // two stages per warp and as many warps as fit (up to NW_MAX): more warps hide the
+    // latency of the per-chunk arithmetic, two stages keep a copy in flight per warp
+    a.S = 2;
+    int nw = static_cast<int>(SMEM_BUDGET / (a.S * a.stage_bytes));
+    if (nw > NW_MAX) nw = NW_MAX;
+    if (nw < 1) return cudaErrorNotSupported;  // a stage would not fit (hundreds of query heads per KV head)
+    a.logit_scale = s.scale * 1.4426950408889634f / static_cast<float>(a.r);
+    a.n_groups = static_cast<int64_t>(s.B) * s.Hkv * (s.N / s.g);
+    a.status = status;
+    const uint32_t smem = nw * a.S * a.stage_bytes;
+    static std::once_flag once;
+    static cudaError_t attr = cudaSuccess;
+    std::call_once(once, [] {
+        attr = cudaFuncSetAttribute(pool_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(SMEM_BUDGET));
+    });
+    if (attr != cudaSuccess) return attr;
+    const int sms = sm_count();
+    if (sms <= 0) return cudaErrorInvalidDevice;
+    const int64_t want = (a.n_groups + nw - 1) / nw;
+    const unsigned grid = static_cast<unsigned>(want < sms ? want : sms);
+    pool_kernel<T, D><<<grid, nw * 32, smem, stream>>>(static_cast<const T *>(Q), static_cast<const T *>(K),
+                                                       static_cast<const T *>(V), static_cast<T *>(Kc),
+                                                       static_cast<T *>(Vc), a);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_pool(int dtype, const void *Q, const void *K, const void *V, void *Kc, void *Vc,
-                        const Shape &s, cudaStream_t stream) {
+                        const Shape &s, int32_t *status, cudaStream_t stream) {
     if (dtype == 0) {
-        if (s.d == 128) return launch_typed<__nv_bfloat16, 128>(Q, K, V, Kc, Vc, s, stream);
-        if (s.d == 64) return launch_typed<__nv_bfloat16, 64>(Q, K, V, Kc, Vc, s, stream);
+        if (s.d == 128) return launch_typed<__nv_bfloat16, 128>(Q, K, V, Kc, Vc, s, status, stream);
+        if (s.d == 64) return launch_typed<__nv_bfloat16, 64>(Q, K, V, Kc, Vc, s, status, stream);
     } else {
-        if (s.d == 128) return launch_typed<float, 128>(Q, K, V, Kc, Vc, s, stream);
-        if (s.d == 64) return launch_typed<float, 64>(Q, K, V, Kc, Vc, s, stream);
+        if (s.d == 128) return launch_typed<float, 128>(Q, K, V, Kc, Vc, s, status, stream);
+        if (s.d == 64) return launch_typed<float, 64>(Q, K, V, Kc, Vc, s, status, stream);
     }
     return cudaErrorNotSupported;
 }
