@@ -258,10 +258,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // ------------------------------------------------------------ MMA issuer
             uint32_t ubase = 0;
             int n_iter = 0;
-            int kpend[NS];
-            for (int s = 0; s < NS; ++s) kpend[s] = 0;
+            uint32_t kpend = 0;  // pending S issues per ring slot, 2 bits per slot
             uint32_t pf_cnt[2] = {0, 0};
             int n_half[2] = {0, 0};  // items each half has processed
+            // Descriptors of step 0 for Q_A, Q_B and for ring slot 0; a slot adds TILE_BYTES/16.
+            const uint64_t dq0 = ptx::smem_desc_sw128(base + OFF_Q, 16, 1024);
+            const uint64_t dq1 = ptx::smem_desc_sw128(base + OFF_Q + TILE_BYTES, 16, 1024);
+            const uint64_t dk0 = ptx::smem_desc_sw128(base + OFF_RING, 16, 1024);
+            const uint64_t dv0 = ptx::smem_desc_sw128(base + OFF_RING, HALF_BYTES, 1024);
             bool ok = true;
             for (int k = blockIdx.x; ok && k < p.n_items; k += gridDim.x, ++n_iter) {
                 const Item it = make_item(p, k);
@@ -271,21 +275,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 auto issue_s = [&](int h, int t) -> bool {
                     const uint32_t uk = ubase + 2 * t;
                     const int slot = uk % NS;
-                    if (kpend[slot] == 0) {
+                    uint32_t pend = (kpend >> (2 * slot)) & 3u;
+                    if (pend == 0) {
                         if (!ptx::wait_bounded(bar(B_FULL + slot), (uk / NS) & 1, abort_flag, lim)) return false;
-                        kpend[slot] = (half_uses(it.hA, it.Tc, t) ? 1 : 0) + (half_uses(it.hB, it.Tc, t) ? 1 : 0);
+                        pend = (half_uses(it.hA, it.Tc, t) ? 1u : 0u) + (half_uses(it.hB, it.Tc, t) ? 1u : 0u);
                     }
                     ptx::tc_fence_after();
-                    const uint32_t tile = base + OFF_RING + slot * TILE_BYTES;
-                    const uint32_t q = base + OFF_Q + h * TILE_BYTES;
-#pragma unroll
-                    for (int kk = 0; kk < HD / 16; ++kk) {
-                        const uint32_t koff = (kk >> 2) * HALF_BYTES + (kk & 3) * 32;
-                        ptx::mma_ss(tmem + TM_S + h * BN, ptx::smem_desc_sw128(q + koff, 16, 1024),
-                                    ptx::smem_desc_sw128(tile + koff, 16, 1024), IDESC_QK, kk > 0 ? 1u : 0u);
-                    }
+                    ptx::mma_ss_k128(tmem + TM_S + h * BN, h ? dq1 : dq0, dk0 + static_cast<uint64_t>(slot) * (TILE_BYTES >> 4),
+                                     IDESC_QK, 0u);
                     ptx::tc_commit(bar(B_SFULL + h));
-                    if (--kpend[slot] == 0) ptx::tc_commit(bar(B_EMPTY + slot));
+                    --pend;
+                    kpend = (kpend & ~(3u << (2 * slot))) | (pend << (2 * slot));
+                    if (pend == 0) ptx::tc_commit(bar(B_EMPTY + slot));
                     if (--s_left == 0) ptx::tc_commit(bar(B_QFREE));
                     return true;
                 };
@@ -307,7 +308,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         ok = false;
                         break;
                     }
-                    const uint32_t vtile = base + OFF_RING + vslot * TILE_BYTES;
                     for (int h = 0; h < 2; ++h) {
                         const Half &x = it.half(h);
                         if (!half_uses(x, it.Tc, t)) continue;
@@ -324,12 +324,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             }
                         }
                         ptx::tc_fence_after();
-#pragma unroll
-                        for (int kk = 0; kk < BN / 16; ++kk) {
-                            ptx::mma_ts(tmem + TM_O + h * HD, tmem + TM_S + h * BN + kk * 8,
-                                        ptx::smem_desc_sw128(vtile + kk * 2048, HALF_BYTES, 1024), IDESC_PV,
-                                        (!first_pv[h] || kk > 0) ? 1u : 0u);
-                        }
+                        ptx::mma_ts_k128(tmem + TM_O + h * HD, tmem + TM_S + h * BN,
+                                         dv0 + static_cast<uint64_t>(vslot) * (TILE_BYTES >> 4), IDESC_PV,
+                                         first_pv[h] ? 0u : 1u);
                         first_pv[h] = false;
                         const int tn = half_next(x, it.Tc, t);
                         if (tn >= 0) {
