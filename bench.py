@@ -266,11 +266,43 @@ def run_cca(args, rank, world, local):
                           "pool_gbs": W.pool_bytes(wl2) / (pm / 1e3) / 1e9,
                           "pool_frac": W.pool_bytes(wl2) / (pm / 1e3) / 1e9 / peaks["hbm_gbs"]}
         out["gpu_launches"] += 2 * max(3, args.steps // 4)
+    if args.comparator:
+        out["full_attention_comparator"] = comparator(wl, dev, stream, max(3, args.steps // 4), ms_per_step)
+        out["gpu_launches"] += max(3, args.steps // 4)
     if not args.no_e2e:
         out["e2e"] = e2e(wl, dev, stream, max(3, args.steps // 2), world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
     return out
+
+
+def comparator(wl, dev, stream, steps, cca_ms_per_step):
+    """Dense causal softmax attention over the same Q, K, V with the same kernel (g = 1,
+    w = N), timed like the CCA step: the attention-level counterpart of the pages'
+    CCA-versus-full-attention prefill comparison."""
+    from sparse_long_context_cca_gb300 import api
+    from sparse_long_context_cca_gb300.inputs import make_qkv
+    Q, K, V = make_qkv(wl, dev)
+    O = torch.empty_like(Q)
+    LSE = torch.empty((wl.B, wl.Hq, wl.N), dtype=torch.float32, device=dev)
+    for _ in range(2):
+        api.causal_attention(Q, K, V, O=O, LSE=LSE, stream=stream)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        api.causal_attention(Q, K, V, O=O, LSE=LSE, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    flops = 4.0 * wl.d * wl.N * (wl.N + 1) / 2 * wl.B * wl.Hq
+    del Q, K, V, O, LSE
+    torch.cuda.empty_cache()
+    return {"what": "causal softmax attention over all N keys, same kernel (g=1, w=N)",
+            "attn_ms": ms, "eff_tflops": flops / (ms / 1e3) / 1e12,
+            "cca_speedup": ms / cca_ms_per_step,
+            "note": "CCA step = pooling + fused attention; speed-up = full attention time / CCA step time"}
 
 
 def e2e(wl, dev, stream, steps, world):
@@ -378,6 +410,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-128k", dest="also_128k", action="store_false")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-comparator", dest="comparator", action="store_false")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -178,3 +178,12 @@ def cca_prefill(Q, K, V, g: int, w: int, scale: float = 0.0, out=None, stream=No
     Kc, Vc = cca_pool(Q, K, V, g, Kc, Vc, scale, stream)
     O, LSE = cca_attn_fwd(Q, K, V, Kc, Vc, g, w, O, LSE, scale, None, stream)
     return O, LSE, Kc, Vc
+
+
+def causal_attention(Q, K, V, scale: float = 0.0, O=None, LSE=None, stream=None):
+    """Full causal softmax attention through the same fused kernel: with g = 1 every
+    token is its own core and with w >= N no core is visible, so the visible set of
+    query i is exactly tokens [0, i] (the closed form the oracle is pinned to).
+    K and V serve as their own core tensors (shape [B, Hkv, N/1, d])."""
+    N = Q.shape[2]
+    return cca_attn_fwd(Q, K, V, K, V, 1, N, O, LSE, scale, None, stream)

@@ -117,3 +117,13 @@ def test_dev_status_stays_zero():
     api.cca_attn_fwd(Q, K, V, Kc, Vc, w.g, w.w, dev_status=st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
+
+
+def test_causal_attention_comparator():
+    """The full-attention comparator (same kernel, g = 1, w = N) is causal attention."""
+    w = wl(1, 4, 2, 1000, 128, 1, 1000)
+    Q, K, V = make_qkv(w, "cuda")
+    O, LSE = api.causal_attention(Q, K, V)
+    torch.cuda.synchronize()
+    Or, Lr, _, _ = oracle.prefill(Q, K, V, 1, w.N)
+    check_out(O, LSE, Or, Lr, Q.dtype, "causal comparator")
