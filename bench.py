@@ -266,6 +266,10 @@ def run_cca(args, rank, world, local):
                           "pool_gbs": W.pool_bytes(wl2) / (pm / 1e3) / 1e9,
                           "pool_frac": W.pool_bytes(wl2) / (pm / 1e3) / 1e9 / peaks["hbm_gbs"]}
         out["gpu_launches"] += 2 * max(3, args.steps // 4)
+    if args.decode:
+        out["decode"] = decode_bench(wl, dev, stream, 50, peaks)
+        if args.also_128k and wl is not W.MHA_128K:
+            out["decode_128k"] = decode_bench(W.MHA_128K, dev, stream, 50, peaks)
     if args.comparator:
         out["full_attention_comparator"] = comparator(wl, dev, stream, max(3, args.steps // 4), ms_per_step)
         out["gpu_launches"] += max(3, args.steps // 4)
@@ -274,6 +278,43 @@ def run_cca(args, rank, world, local):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
     return out
+
+
+def decode_bench(wl, dev, stream, iters, peaks):
+    """One decoding step at the last position of the workload (the token that sees the
+    most cores): cca_decode_fwd over the caches, timed with CUDA events."""
+    from sparse_long_context_cca_gb300 import api
+    from sparse_long_context_cca_gb300.inputs import make_qkv
+    Q, K, V = make_qkv(wl, dev)
+    Kc, Vc = api.cca_pool(Q, K, V, wl.g, stream=stream)
+    pos = wl.N - 1
+    q = Q[:, :, pos].contiguous()
+    del Q
+    O = torch.empty_like(q)
+    LSE = torch.empty((wl.B, wl.Hq), dtype=torch.float32, device=dev)
+    ws = torch.empty(api.decode_workspace_size(wl.B, wl.Hq, wl.Hkv, wl.N, wl.d, wl.g, wl.w, q.dtype),
+                     dtype=torch.uint8, device=dev)
+    for _ in range(5):
+        api.cca_decode_fwd(q, K, V, Kc, Vc, pos, wl.g, wl.w, O, LSE, ws, stream=stream)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(iters):
+        api.cca_decode_fwd(q, K, V, Kc, Vc, pos, wl.g, wl.w, O, LSE, ws, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) / iters * 1e3
+    lo = max(0, pos - wl.w + 1)
+    keys = lo // wl.g + (pos - lo + 1)
+    e = 2 if wl.dtype == "bf16" else 4
+    nbytes = wl.B * wl.Hkv * keys * 2 * wl.d * e + 2 * wl.B * wl.Hq * wl.d * e
+    del K, V, Kc, Vc
+    torch.cuda.empty_cache()
+    return {"what": f"one decode step at position {pos} ({keys} visible keys per head), split-KV + combine",
+            "us_per_step": us, "tokens_per_s": wl.B / (us * 1e-6),
+            "gbs": nbytes / (us * 1e-6) / 1e9, "hbm_frac": nbytes / (us * 1e-6) / 1e9 / peaks["hbm_gbs"],
+            "algorithmic_bytes": nbytes, "kernel_launches_per_step": 2}
 
 
 def comparator(wl, dev, stream, steps, cca_ms_per_step):
@@ -411,6 +452,7 @@ def main():
     ap.add_argument("--no-128k", dest="also_128k", action="store_false")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-comparator", dest="comparator", action="store_false")
+    ap.add_argument("--no-decode", dest="decode", action="store_false")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -108,6 +108,47 @@ int cca_pool(const void *Q, const void *K, const void *V, void *Kc, void *Vc,
 int cca_attn_fwd(const void *Q, const void *K, const void *V, const void *Kc, const void *Vc,
                  void *O, float *LSE, const cca_params_t *params, void *stream);
 
+/*
+ * Decoding (one new token per sequence).  The pages describe a decode step that
+ * keeps only the core tokens plus the local window in the KV cache and pools a
+ * group once it has filled (news write-up, efficiency and KV-cache paragraphs;
+ * OpenReview rebuttal, cache-size answer).  Here a decode step at position
+ * `pos` computes exactly row `pos` of cca_attn_fwd over the caches.
+ *
+ * cca_decode_fwd - for every (b, h): one softmax over the visible cores
+ * j < lo(pos)/g followed by the window tokens [lo(pos), pos], lo(pos) =
+ * max(0, pos - w + 1).
+ *   Q      [B, Hq, d]          query of the token at position pos
+ *   K, V   [B, Hkv, Ncap, d]   caches; rows [lo(pos), pos] must be valid
+ *   Kc, Vc [B, Hkv, Ncap/g, d] core caches; rows [0, lo(pos)/g) must be valid
+ *   O      [B, Hq, d]          output (dtype of Q);  LSE [B, Hq] fp32
+ *   params.N = Ncap (cache capacity, a multiple of g); 0 <= pos < Ncap.
+ *   workspace: caller-owned device buffer of at least
+ *   cca_decode_workspace_size(params) bytes (per-split partial results); it
+ *   needs no initialisation and is fully rewritten by every call.
+ * The keys are split across CTAs (flash-decoding) and the partial results are
+ * merged by a second kernel on the same stream.
+ * Supported: bf16 or f32, d in {64, 128}, Hq/Hkv <= 8.
+ */
+int cca_decode_fwd(const void *Q, const void *K, const void *V, const void *Kc, const void *Vc, void *O,
+                   float *LSE, int pos, const cca_params_t *params, void *workspace,
+                   uint64_t workspace_bytes, void *stream);
+
+/* Bytes of workspace cca_decode_fwd needs for these shapes (0 on bad params). */
+uint64_t cca_decode_workspace_size(const cca_params_t *params);
+
+/*
+ * cca_pool_group - pool one newly completed group j of the caches (the
+ * pooling equation for a single group): for every (b, kv),
+ *   Kc[b, kv, j] = sum_t a_t K[b, kv, j*g + t],  Vc likewise,
+ *   a = softmax_t(tau * mean_{h in kv} q[b, h] . K[b, kv, j*g + t]),
+ * where q [B, Hq, d] is the query of the group's last token (j+1)*g - 1, i.e.
+ * the token just decoded.  K, V [B, Hkv, Ncap, d]; Kc, Vc [B, Hkv, Ncap/g, d];
+ * params.N = Ncap; 0 <= j < Ncap/g.  Same support as cca_pool.
+ */
+int cca_pool_group(const void *q, const void *K, const void *V, void *Kc, void *Vc, int j,
+                   const cca_params_t *params, void *stream);
+
 /* Static English text for a status code (never NULL). */
 const char *cca_status_string(int status);
 

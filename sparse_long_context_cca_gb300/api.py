@@ -43,8 +43,8 @@ class CcaParams(ctypes.Structure):
 _lib = None
 _lock = threading.Lock()
 
-EXPORTED = ["cca_pool", "cca_attn_fwd", "cca_status_string", "cca_abi_version",
-            "cca_test_set_wait_limit_ns", "cca_test_skip_q_load"]
+EXPORTED = ["cca_pool", "cca_attn_fwd", "cca_decode_fwd", "cca_decode_workspace_size", "cca_pool_group",
+            "cca_status_string", "cca_abi_version", "cca_test_set_wait_limit_ns", "cca_test_skip_q_load"]
 
 
 def library_path() -> str:
@@ -68,6 +68,12 @@ def load_library():
         lib.cca_pool.restype = ctypes.c_int
         lib.cca_attn_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, pp, vp]
         lib.cca_attn_fwd.restype = ctypes.c_int
+        lib.cca_decode_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, ctypes.c_int, pp, vp, ctypes.c_uint64, vp]
+        lib.cca_decode_fwd.restype = ctypes.c_int
+        lib.cca_decode_workspace_size.argtypes = [pp]
+        lib.cca_decode_workspace_size.restype = ctypes.c_uint64
+        lib.cca_pool_group.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, pp, vp]
+        lib.cca_pool_group.restype = ctypes.c_int
         lib.cca_status_string.argtypes = [ctypes.c_int]
         lib.cca_status_string.restype = ctypes.c_char_p
         lib.cca_abi_version.argtypes = []
@@ -187,3 +193,66 @@ def causal_attention(Q, K, V, scale: float = 0.0, O=None, LSE=None, stream=None)
     K and V serve as their own core tensors (shape [B, Hkv, N/1, d])."""
     N = Q.shape[2]
     return cca_attn_fwd(Q, K, V, K, V, 1, N, O, LSE, scale, None, stream)
+
+
+def decode_workspace_size(B, Hq, Hkv, Ncap, d, g, w, dtype) -> int:
+    prm = make_params(B, Hq, Hkv, Ncap, d, g, w, _DTYPE[dtype])
+    return int(load_library().cca_decode_workspace_size(ctypes.byref(prm)))
+
+
+def cca_decode_fwd(q, K, V, Kc, Vc, pos: int, g: int, w: int, O=None, LSE=None, workspace=None,
+                   scale: float = 0.0, stream=None):
+    """One decoding step: row `pos` of the fused attention over the caches.
+    q [B, Hq, d]; K, V [B, Hkv, Ncap, d]; Kc, Vc [B, Hkv, Ncap/g, d].
+    Returns (O [B, Hq, d], LSE [B, Hq])."""
+    lib = load_library()
+    if q.dim() != 3 or K.dim() != 4:
+        raise ValueError("q must be [B, Hq, d] and K [B, Hkv, Ncap, d]")
+    B, Hq, d = q.shape
+    Hkv, Ncap = K.shape[1], K.shape[2]
+    if q.dtype not in _DTYPE:
+        raise ValueError(f"unsupported dtype {q.dtype}")
+    G = Ncap // g if g > 0 else 0
+    _check(q, "q", q.dtype, (B, Hq, d))
+    _check(K, "K", q.dtype, (B, Hkv, Ncap, d))
+    _check(V, "V", q.dtype, (B, Hkv, Ncap, d))
+    _check(Kc, "Kc", q.dtype, (B, Hkv, G, d))
+    _check(Vc, "Vc", q.dtype, (B, Hkv, G, d))
+    if O is None:
+        O = torch.empty_like(q)
+    if LSE is None:
+        LSE = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    _check(O, "O", q.dtype, (B, Hq, d))
+    _check(LSE, "LSE", torch.float32, (B, Hq))
+    prm = make_params(B, Hq, Hkv, Ncap, d, g, w, _DTYPE[q.dtype], scale)
+    need = int(lib.cca_decode_workspace_size(ctypes.byref(prm)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if not workspace.is_cuda or workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"workspace must be a CUDA buffer of at least {need} bytes")
+    st = lib.cca_decode_fwd(q.data_ptr(), K.data_ptr(), V.data_ptr(), Kc.data_ptr(), Vc.data_ptr(),
+                            O.data_ptr(), LSE.data_ptr(), int(pos), ctypes.byref(prm), workspace.data_ptr(),
+                            workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    if st != CCA_OK:
+        raise CcaError(st, "cca_decode_fwd")
+    return O, LSE
+
+
+def cca_pool_group(q, K, V, Kc, Vc, j: int, g: int, scale: float = 0.0, stream=None):
+    """Pool the newly completed group j of the caches in place (Kc[:, :, j], Vc[:, :, j]),
+    scored by q [B, Hq, d], the query of the group's last token."""
+    lib = load_library()
+    B, Hq, d = q.shape
+    Hkv, Ncap = K.shape[1], K.shape[2]
+    G = Ncap // g if g > 0 else 0
+    _check(q, "q", q.dtype, (B, Hq, d))
+    _check(K, "K", q.dtype, (B, Hkv, Ncap, d))
+    _check(V, "V", q.dtype, (B, Hkv, Ncap, d))
+    _check(Kc, "Kc", q.dtype, (B, Hkv, G, d))
+    _check(Vc, "Vc", q.dtype, (B, Hkv, G, d))
+    prm = make_params(B, Hq, Hkv, Ncap, d, g, 1, _DTYPE[q.dtype], scale)
+    st = lib.cca_pool_group(q.data_ptr(), K.data_ptr(), V.data_ptr(), Kc.data_ptr(), Vc.data_ptr(), int(j),
+                            ctypes.byref(prm), _stream_handle(stream))
+    if st != CCA_OK:
+        raise CcaError(st, "cca_pool_group")
+    return Kc, Vc

@@ -102,6 +102,41 @@ int cca_attn_fwd(const void *Q, const void *K, const void *V, const void *Kc, co
     return from_cuda(cca::launch_attn_bf16_tc(Q, K, V, Kc, Vc, O, LSE, s, params->dev_status, strm));
 }
 
+int cca_decode_fwd(const void *Q, const void *K, const void *V, const void *Kc, const void *Vc, void *O, float *LSE,
+                   int pos, const cca_params_t *params, void *workspace, uint64_t workspace_bytes, void *stream) {
+    int st = check_shape(params, true);
+    if (st != CCA_OK) return st;
+    const void *ptrs[8] = {Q, K, V, Kc, Vc, O, LSE, workspace};
+    for (const void *q : ptrs)
+        if (q == nullptr || !aligned16(q)) return CCA_ERR_INVALID_ARG;
+    if (pos < 0 || pos >= params->N) return CCA_ERR_INVALID_ARG;
+    const int r = params->Hq / params->Hkv;
+    if (r != 1 && r != 2 && r != 4 && r != 8) return CCA_ERR_UNSUPPORTED;
+    const cca::Shape s = to_shape(params);
+    if (workspace_bytes < cca::decode_workspace_bytes(s)) return CCA_ERR_INVALID_ARG;
+    if ((st = check_device()) != CCA_OK) return st;
+    return from_cuda(cca::launch_decode(params->dtype, Q, K, V, Kc, Vc, O, LSE, s, pos,
+                                        static_cast<float *>(workspace), static_cast<cudaStream_t>(stream)));
+}
+
+uint64_t cca_decode_workspace_size(const cca_params_t *params) {
+    if (check_shape(params, true) != CCA_OK) return 0;
+    return cca::decode_workspace_bytes(to_shape(params));
+}
+
+int cca_pool_group(const void *q, const void *K, const void *V, void *Kc, void *Vc, int j, const cca_params_t *params,
+                   void *stream) {
+    int st = check_shape(params, false);
+    if (st != CCA_OK) return st;
+    const void *ptrs[5] = {q, K, V, Kc, Vc};
+    for (const void *x : ptrs)
+        if (x == nullptr || !aligned16(x)) return CCA_ERR_INVALID_ARG;
+    if (j < 0 || j >= params->N / params->g) return CCA_ERR_INVALID_ARG;
+    if ((st = check_device()) != CCA_OK) return st;
+    return from_cuda(cca::launch_pool_group(params->dtype, q, K, V, Kc, Vc, to_shape(params), j,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
 const char *cca_status_string(int status) {
     switch (status) {
         case CCA_OK: return "ok";

@@ -1,0 +1,407 @@
+// Decoding step of CCA attention: the new token at position `pos` attends, with
+// one softmax, to the visible core tokens j < lo(pos)/g and to the raw tokens of
+// its window [lo(pos), pos] ("Core Context Aware Transformers for Long Context
+// Language Modeling", Method section, fusion equation, evaluated for one query
+// row; the write-up's decoding paragraph keeps only cores + window in the KV
+// cache).  Plus pooling of a single newly completed group (pooling equation).
+//
+// Memory-bound: every visible key and value row is read once per KV head and
+// used by the r query heads that share it.  The visible list is split across
+// CTAs (flash-decoding); each CTA keeps an online-softmax state per query head
+// over its slice, and a second kernel merges the slices' (max, sum, output)
+// partials, which live in a caller-provided workspace.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "internal.h"
+#include "sm100_ptx.cuh"
+
+namespace cca {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int DEC_WARPS = 4;
+constexpr int MIN_KEYS_PER_SPLIT = 256;
+constexpr int MAX_SPLITS = 64;
+
+template <typename T>
+struct Vec;
+template <>
+struct Vec<__nv_bfloat16> {
+    static constexpr int E = 8;
+    __device__ static void unpack(const uint4 &v, float (&f)[8]) {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            f[2 * i] = __uint_as_float(w[i] << 16);
+            f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    }
+    __device__ static uint4 pack(const float (&f)[8]) {
+        return make_uint4(ptx::pack_bf16x2(f[0], f[1]), ptx::pack_bf16x2(f[2], f[3]), ptx::pack_bf16x2(f[4], f[5]),
+                          ptx::pack_bf16x2(f[6], f[7]));
+    }
+};
+template <>
+struct Vec<float> {
+    static constexpr int E = 4;
+    __device__ static void unpack(const uint4 &v, float (&f)[4]) {
+        f[0] = __uint_as_float(v.x);
+        f[1] = __uint_as_float(v.y);
+        f[2] = __uint_as_float(v.z);
+        f[3] = __uint_as_float(v.w);
+    }
+    __device__ static uint4 pack(const float (&f)[4]) {
+        return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]), __float_as_uint(f[3]));
+    }
+};
+
+__device__ __forceinline__ uint4 ldg16(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
+struct DecodeArgs {
+    int Hq, Hkv, Ncap, g, pos;
+    int n_core, lo, L;  // visible cores, first window token, visible keys
+    int splits;         // CTAs per (b, kv)
+    float scale_log2;
+};
+
+// Partials: ws[((b*Hq + h) * MAX_SPLITS + s) * (D + 2) + {0..D-1: o, D: m, D+1: l}]
+template <typename T, int D, int R>
+__global__ void __launch_bounds__(DEC_WARPS * 32) decode_split_kernel(const T *__restrict__ Q, const T *__restrict__ K,
+                                                                      const T *__restrict__ V,
+                                                                      const T *__restrict__ Kc,
+                                                                      const T *__restrict__ Vc, float *__restrict__ ws,
+                                                                      const DecodeArgs a) {
+    using VT = Vec<T>;
+    constexpr int E = VT::E;
+    constexpr int LPR = D / E;     // lanes per key row
+    constexpr int RPI = 32 / LPR;  // keys per warp-wide pass
+    constexpr int UNROLL = 4;
+    __shared__ float sm_m[DEC_WARPS][R], sm_l[DEC_WARPS][R];
+    __shared__ float sm_o[DEC_WARPS][R][D];
+
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int sub = lane / LPR, cl = lane % LPR;
+    const int s = blockIdx.x;
+    const int bk = blockIdx.y;  // b * Hkv + kv
+    const int b = bk / a.Hkv, kv = bk % a.Hkv;
+    // this CTA's slice of the visible list, then this warp's part of it
+    const int x0 = static_cast<int>(static_cast<int64_t>(a.L) * s / a.splits);
+    const int x1 = static_cast<int>(static_cast<int64_t>(a.L) * (s + 1) / a.splits);
+    const int wx0 = x0 + (x1 - x0) * warp / DEC_WARPS;
+    const int wx1 = x0 + (x1 - x0) * (warp + 1) / DEC_WARPS;
+
+    float q[R][E], o[R][E], m[R], l[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        float f[E];
+        VT::unpack(ldg16(Q + (static_cast<int64_t>(b) * a.Hq + kv * R + r) * D + cl * E), f);
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            q[r][e] = f[e];
+            o[r][e] = 0.f;
+        }
+        m[r] = -INFINITY;
+        l[r] = 0.f;
+    }
+    // list index x < n_core is core x; otherwise window token lo + (x - n_core)
+    const T *kc = Kc + static_cast<int64_t>(bk) * (a.Ncap / a.g) * D + cl * E;
+    const T *vc = Vc + static_cast<int64_t>(bk) * (a.Ncap / a.g) * D + cl * E;
+    const T *kr = K + static_cast<int64_t>(bk) * a.Ncap * D + cl * E;
+    const T *vr = V + static_cast<int64_t>(bk) * a.Ncap * D + cl * E;
+
+    for (int xb = wx0; xb < wx1; xb += RPI * UNROLL) {
+        uint4 kk[UNROLL], vv[UNROLL];
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            const int x = xb + u * RPI + sub;
+            if (x < wx1) {
+                const bool core = x < a.n_core;
+                const int64_t row = core ? x : a.lo + (x - a.n_core);
+                kk[u] = ldg16((core ? kc : kr) + row * D);
+                vv[u] = ldg16((core ? vc : vr) + row * D);
+            } else {
+                kk[u] = vv[u] = make_uint4(0, 0, 0, 0);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            const bool valid = xb + u * RPI + sub < wx1;
+            float kf[E], vf[E];
+            VT::unpack(kk[u], kf);
+            VT::unpack(vv[u], vf);
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                float dot = 0.f;
+#pragma unroll
+                for (int e = 0; e < E; ++e) dot = fmaf(q[r][e], kf[e], dot);
+#pragma unroll
+                for (int off = LPR / 2; off > 0; off >>= 1) dot += __shfl_xor_sync(kFull, dot, off);
+                if (valid) {
+                    const float xl = dot * a.scale_log2;
+                    const float mn = fmaxf(m[r], xl);
+                    const float corr = ptx::ex2(m[r] - mn);
+                    const float p = ptx::ex2(xl - mn);
+                    l[r] = l[r] * corr + p;
+#pragma unroll
+                    for (int e = 0; e < E; ++e) o[r][e] = fmaf(p, vf[e], o[r][e] * corr);
+                    m[r] = mn;
+                }
+            }
+        }
+    }
+    // merge the RPI key subgroups of the warp (lanes with the same column chunk)
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+#pragma unroll
+        for (int off = LPR; off < 32; off <<= 1) {
+            const float mo = __shfl_xor_sync(kFull, m[r], off);
+            const float lo_ = __shfl_xor_sync(kFull, l[r], off);
+            const float mn = fmaxf(m[r], mo);
+            const float ca = (m[r] == -INFINITY) ? 0.f : ptx::ex2(m[r] - mn);
+            const float cb = (mo == -INFINITY) ? 0.f : ptx::ex2(mo - mn);
+            l[r] = l[r] * ca + lo_ * cb;
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                const float oo = __shfl_xor_sync(kFull, o[r][e], off);
+                o[r][e] = o[r][e] * ca + oo * cb;
+            }
+            m[r] = mn;
+        }
+        if (sub == 0) {
+#pragma unroll
+            for (int e = 0; e < E; ++e) sm_o[warp][r][cl * E + e] = o[r][e];
+            if (cl == 0) {
+                sm_m[warp][r] = m[r];
+                sm_l[warp][r] = l[r];
+            }
+        }
+    }
+    __syncthreads();
+    // merge the warps and write this split's partial for each query head
+    for (int idx = threadIdx.x; idx < R * D; idx += blockDim.x) {
+        const int r = idx / D, c = idx % D;
+        float mx = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < DEC_WARPS; ++w) mx = fmaxf(mx, sm_m[w][r]);
+        float acc = 0.f, lsum = 0.f;
+#pragma unroll
+        for (int w = 0; w < DEC_WARPS; ++w) {
+            const float f = (sm_m[w][r] == -INFINITY) ? 0.f : ptx::ex2(sm_m[w][r] - mx);
+            acc += sm_o[w][r][c] * f;
+            lsum += sm_l[w][r] * f;
+        }
+        float *dst = ws + ((static_cast<int64_t>(b) * a.Hq + kv * R + r) * MAX_SPLITS + s) * (D + 2);
+        dst[c] = acc;
+        if (c == 0) {
+            dst[D] = mx;
+            dst[D + 1] = lsum;
+        }
+    }
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(D) decode_combine_kernel(const float *__restrict__ ws, T *__restrict__ O,
+                                                           float *__restrict__ LSE, int splits) {
+    const int bh = blockIdx.x;
+    const int c = threadIdx.x;
+    const float *base = ws + static_cast<int64_t>(bh) * MAX_SPLITS * (D + 2);
+    float mx = -INFINITY;
+    for (int s = 0; s < splits; ++s) mx = fmaxf(mx, base[s * (D + 2) + D]);
+    float acc = 0.f, lsum = 0.f;
+    for (int s = 0; s < splits; ++s) {
+        const float ms = base[s * (D + 2) + D];
+        const float f = (ms == -INFINITY) ? 0.f : ptx::ex2(ms - mx);
+        acc += base[s * (D + 2) + c] * f;
+        lsum += base[s * (D + 2) + D + 1] * f;
+    }
+    const float val = acc / lsum;
+    if constexpr (sizeof(T) == 2) {
+        O[static_cast<int64_t>(bh) * D + c] = __float2bfloat16_rn(val);
+    } else {
+        O[static_cast<int64_t>(bh) * D + c] = val;
+    }
+    if (c == 0) LSE[bh] = (mx + __log2f(lsum)) * 0.6931471805599453f;
+}
+
+// One warp per (b, kv): pools group j with the supplied group-last queries q[B, Hq, D].
+template <typename T, int D>
+__global__ void __launch_bounds__(128) pool_group_kernel(const T *__restrict__ q, const T *__restrict__ K,
+                                                         const T *__restrict__ V, T *__restrict__ Kc,
+                                                         T *__restrict__ Vc, int Hq, int Hkv, int Ncap, int g, int j,
+                                                         float logit_scale, int n_bk) {
+    using VT = Vec<T>;
+    constexpr int E = VT::E;
+    constexpr int LPR = D / E;
+    constexpr int RPI = 32 / LPR;
+    const int lane = threadIdx.x & 31;
+    const int bk = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (bk >= n_bk) return;
+    const int sub = lane / LPR, cl = lane % LPR;
+    const int b = bk / Hkv, kv = bk % Hkv, r = Hq / Hkv;
+    float qs[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) qs[e] = 0.f;
+    for (int hh = 0; hh < r; ++hh) {
+        float f[E];
+        VT::unpack(ldg16(q + (static_cast<int64_t>(b) * Hq + kv * r + hh) * D + cl * E), f);
+#pragma unroll
+        for (int e = 0; e < E; ++e) qs[e] += f[e];
+    }
+    const T *kg = K + (static_cast<int64_t>(bk) * Ncap + static_cast<int64_t>(j) * g) * D + cl * E;
+    const T *vg = V + (static_cast<int64_t>(bk) * Ncap + static_cast<int64_t>(j) * g) * D + cl * E;
+    float m = -INFINITY, l = 0.f, ak[E], av[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) ak[e] = av[e] = 0.f;
+    for (int t0 = 0; t0 < g; t0 += RPI) {
+        const int t = t0 + sub;
+        float kf[E], vf[E];
+        VT::unpack(t < g ? ldg16(kg + static_cast<int64_t>(t) * D) : make_uint4(0, 0, 0, 0), kf);
+        VT::unpack(t < g ? ldg16(vg + static_cast<int64_t>(t) * D) : make_uint4(0, 0, 0, 0), vf);
+        float dot = 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) dot = fmaf(qs[e], kf[e], dot);
+#pragma unroll
+        for (int off = LPR / 2; off > 0; off >>= 1) dot += __shfl_xor_sync(kFull, dot, off);
+        if (t < g) {
+            const float xl = dot * logit_scale;
+            const float mn = fmaxf(m, xl);
+            const float corr = ptx::ex2(m - mn);
+            const float p = ptx::ex2(xl - mn);
+            l = l * corr + p;
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                ak[e] = fmaf(p, kf[e], ak[e] * corr);
+                av[e] = fmaf(p, vf[e], av[e] * corr);
+            }
+            m = mn;
+        }
+    }
+#pragma unroll
+    for (int off = LPR; off < 32; off <<= 1) {
+        const float mo = __shfl_xor_sync(kFull, m, off);
+        const float lo_ = __shfl_xor_sync(kFull, l, off);
+        const float mn = fmaxf(m, mo);
+        const float ca = (m == -INFINITY) ? 0.f : ptx::ex2(m - mn);
+        const float cb = (mo == -INFINITY) ? 0.f : ptx::ex2(mo - mn);
+        l = l * ca + lo_ * cb;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            ak[e] = ak[e] * ca + __shfl_xor_sync(kFull, ak[e], off) * cb;
+            av[e] = av[e] * ca + __shfl_xor_sync(kFull, av[e], off) * cb;
+        }
+        m = mn;
+    }
+    const float inv = 1.f / l;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+        ak[e] *= inv;
+        av[e] *= inv;
+    }
+    if (sub == 0) {
+        const int64_t orow = (static_cast<int64_t>(bk) * (Ncap / g) + j) * D + cl * E;
+        *reinterpret_cast<uint4 *>(Kc + orow) = VT::pack(ak);
+        *reinterpret_cast<uint4 *>(Vc + orow) = VT::pack(av);
+    }
+}
+
+int decode_splits(int L) {
+    const int sp = (L + MIN_KEYS_PER_SPLIT - 1) / MIN_KEYS_PER_SPLIT;
+    return sp < 1 ? 1 : (sp > MAX_SPLITS ? MAX_SPLITS : sp);
+}
+
+template <typename T, int D, int R>
+cudaError_t launch_decode_typed(const void *Q, const void *K, const void *V, const void *Kc, const void *Vc, void *O,
+                                float *LSE, const Shape &s, int pos, float *ws, cudaStream_t stream) {
+    DecodeArgs a;
+    a.Hq = s.Hq;
+    a.Hkv = s.Hkv;
+    a.Ncap = s.N;
+    a.g = s.g;
+    a.pos = pos;
+    a.lo = pos - s.w + 1 > 0 ? pos - s.w + 1 : 0;
+    a.n_core = a.lo / s.g;
+    a.L = a.n_core + (pos - a.lo + 1);
+    a.splits = decode_splits(a.L);
+    a.scale_log2 = s.scale * 1.4426950408889634f;
+    dim3 grid(a.splits, s.B * s.Hkv);
+    decode_split_kernel<T, D, R><<<grid, DEC_WARPS * 32, 0, stream>>>(
+        static_cast<const T *>(Q), static_cast<const T *>(K), static_cast<const T *>(V), static_cast<const T *>(Kc),
+        static_cast<const T *>(Vc), ws, a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    decode_combine_kernel<T, D><<<s.B * s.Hq, D, 0, stream>>>(ws, static_cast<T *>(O), LSE, a.splits);
+    return cudaGetLastError();
+}
+
+template <typename T, int D>
+cudaError_t dispatch_r(const void *Q, const void *K, const void *V, const void *Kc, const void *Vc, void *O,
+                       float *LSE, const Shape &s, int pos, float *ws, cudaStream_t stream) {
+    switch (s.Hq / s.Hkv) {
+        case 1: return launch_decode_typed<T, D, 1>(Q, K, V, Kc, Vc, O, LSE, s, pos, ws, stream);
+        case 2: return launch_decode_typed<T, D, 2>(Q, K, V, Kc, Vc, O, LSE, s, pos, ws, stream);
+        case 4: return launch_decode_typed<T, D, 4>(Q, K, V, Kc, Vc, O, LSE, s, pos, ws, stream);
+        case 8: return launch_decode_typed<T, D, 8>(Q, K, V, Kc, Vc, O, LSE, s, pos, ws, stream);
+        default: return cudaErrorNotSupported;
+    }
+}
+
+}  // namespace
+
+uint64_t decode_workspace_bytes(const Shape &s) {
+    return static_cast<uint64_t>(s.B) * s.Hq * MAX_SPLITS * (s.d + 2) * sizeof(float);
+}
+
+cudaError_t launch_decode(int dtype, const void *Q, const void *K, const void *V, const void *Kc, const void *Vc,
+                          void *O, float *LSE, const Shape &s, int pos, float *ws, cudaStream_t stream) {
+    if (dtype == 0) {
+        if (s.d == 128) return dispatch_r<__nv_bfloat16, 128>(Q, K, V, Kc, Vc, O, LSE, s, pos, ws, stream);
+        if (s.d == 64) return dispatch_r<__nv_bfloat16, 64>(Q, K, V, Kc, Vc, O, LSE, s, pos, ws, stream);
+    } else {
+        if (s.d == 128) return dispatch_r<float, 128>(Q, K, V, Kc, Vc, O, LSE, s, pos, ws, stream);
+        if (s.d == 64) return dispatch_r<float, 64>(Q, K, V, Kc, Vc, O, LSE, s, pos, ws, stream);
+    }
+    return cudaErrorNotSupported;
+}
+
+cudaError_t launch_pool_group(int dtype, const void *q, const void *K, const void *V, void *Kc, void *Vc,
+                              const Shape &s, int j, cudaStream_t stream) {
+    const int n_bk = s.B * s.Hkv;
+    const unsigned blocks = static_cast<unsigned>((n_bk + 3) / 4);
+    const float ls = s.scale * 1.4426950408889634f / static_cast<float>(s.Hq / s.Hkv);
+    if (dtype == 0) {
+        if (s.d == 128)
+            pool_group_kernel<__nv_bfloat16, 128><<<blocks, 128, 0, stream>>>(
+                static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(K),
+                static_cast<const __nv_bfloat16 *>(V), static_cast<__nv_bfloat16 *>(Kc),
+                static_cast<__nv_bfloat16 *>(Vc), s.Hq, s.Hkv, s.N, s.g, j, ls, n_bk);
+        else if (s.d == 64)
+            pool_group_kernel<__nv_bfloat16, 64><<<blocks, 128, 0, stream>>>(
+                static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(K),
+                static_cast<const __nv_bfloat16 *>(V), static_cast<__nv_bfloat16 *>(Kc),
+                static_cast<__nv_bfloat16 *>(Vc), s.Hq, s.Hkv, s.N, s.g, j, ls, n_bk);
+        else
+            return cudaErrorNotSupported;
+    } else {
+        if (s.d == 128)
+            pool_group_kernel<float, 128><<<blocks, 128, 0, stream>>>(
+                static_cast<const float *>(q), static_cast<const float *>(K), static_cast<const float *>(V),
+                static_cast<float *>(Kc), static_cast<float *>(Vc), s.Hq, s.Hkv, s.N, s.g, j, ls, n_bk);
+        else if (s.d == 64)
+            pool_group_kernel<float, 64><<<blocks, 128, 0, stream>>>(
+                static_cast<const float *>(q), static_cast<const float *>(K), static_cast<const float *>(V),
+                static_cast<float *>(Kc), static_cast<float *>(Vc), s.Hq, s.Hkv, s.N, s.g, j, ls, n_bk);
+        else
+            return cudaErrorNotSupported;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace cca

@@ -28,4 +28,11 @@ cudaError_t launch_attn_bf16_tc(const void *Q, const void *K, const void *V, con
                                 const void *Vc, void *O, float *LSE, const Shape &s,
                                 int32_t *dev_status, cudaStream_t stream);
 
+// Decode step (row `pos` of the fused attention over the caches) and single-group pooling.
+uint64_t decode_workspace_bytes(const Shape &s);
+cudaError_t launch_decode(int dtype, const void *Q, const void *K, const void *V, const void *Kc, const void *Vc,
+                          void *O, float *LSE, const Shape &s, int pos, float *ws, cudaStream_t stream);
+cudaError_t launch_pool_group(int dtype, const void *q, const void *K, const void *V, void *Kc, void *Vc,
+                              const Shape &s, int j, cudaStream_t stream);
+
 }  // namespace cca

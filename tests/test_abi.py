@@ -99,3 +99,24 @@ def test_python_binding_requires_cuda_tensors(lib):
     x = torch.zeros(1, 2, 16, 128, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         api.cca_pool(x, x, x, 4)
+
+
+def test_decode_rejects_bad_arguments(lib):
+    prm = api.make_params(1, 4, 4, 1024, 128, 16, 256, api.CCA_BF16)
+    need = lib.cca_decode_workspace_size(ctypes.byref(prm))
+    assert need > 0
+    args = P[:7]
+    assert lib.cca_decode_fwd(*args, -1, ctypes.byref(prm), P[0], need, None) == api.CCA_ERR_INVALID_ARG
+    assert lib.cca_decode_fwd(*args, 1024, ctypes.byref(prm), P[0], need, None) == api.CCA_ERR_INVALID_ARG
+    assert lib.cca_decode_fwd(*args, 5, ctypes.byref(prm), P[0], need - 16, None) == api.CCA_ERR_INVALID_ARG
+    assert lib.cca_decode_fwd(*args, 5, ctypes.byref(prm), 0, need, None) == api.CCA_ERR_INVALID_ARG
+    prm3 = api.make_params(1, 6, 2, 1024, 128, 16, 256, api.CCA_BF16)   # 3 query heads per KV head
+    assert lib.cca_decode_fwd(*args, 5, ctypes.byref(prm3), P[0], 1 << 30, None) == api.CCA_ERR_UNSUPPORTED
+    bad = api.make_params(1, 4, 4, 1000, 128, 16, 256, api.CCA_BF16)    # N % g != 0
+    assert lib.cca_decode_workspace_size(ctypes.byref(bad)) == 0
+
+
+def test_pool_group_rejects_bad_group(lib):
+    prm = api.make_params(1, 4, 4, 1024, 128, 16, 1, api.CCA_BF16)
+    assert lib.cca_pool_group(*P[:5], -1, ctypes.byref(prm), None) == api.CCA_ERR_INVALID_ARG
+    assert lib.cca_pool_group(*P[:5], 64, ctypes.byref(prm), None) == api.CCA_ERR_INVALID_ARG

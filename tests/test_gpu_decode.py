@@ -1,0 +1,100 @@
+"""Decode step on the GPU: one new token per sequence attends to the visible
+core tokens and its window, i.e. row `pos` of the fused attention; groups are
+pooled as they complete.  Checked against the fp64 oracle's rows and against
+the prefill kernels."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity import check_cores, check_out
+from sparse_long_context_cca_gb300 import api
+from sparse_long_context_cca_gb300.inputs import make_qkv
+from sparse_long_context_cca_gb300.workloads import Workload
+
+pytestmark = pytest.mark.gpu
+
+
+def wl(B, Hq, Hkv, N, d, g, w, dtype="bf16", seed=11):
+    return Workload(f"decode B{B} Hq{Hq} Hkv{Hkv} N{N} d{d} g{g} w{w} {dtype}", B, Hq, Hkv, N, d, g, w, dtype,
+                    seed, 0.01)
+
+
+CASES = [wl(1, 4, 4, 4096, 128, 16, 1024), wl(2, 8, 2, 2048, 128, 16, 256), wl(1, 4, 1, 3000, 128, 8, 500),
+         wl(1, 2, 2, 1024, 64, 4, 100), wl(1, 4, 2, 1024, 128, 16, 200, "f32"), wl(1, 2, 2, 512, 64, 32, 64, "f32")]
+
+
+@pytest.mark.parametrize("w", CASES, ids=lambda w: w.name)
+def test_decode_rows_match_oracle(w):
+    Q, K, V = make_qkv(w, "cuda")
+    Kc, Vc = api.cca_pool(Q, K, V, w.g)
+    Kr, Vr = oracle.pool(Q, K, V, w.g)
+    rng = np.random.default_rng(w.seed)
+    positions = sorted({0, 1, w.w - 2, w.w - 1, w.w, w.w + w.g - 1, w.w + w.g, w.N // 2, w.N - 1}
+                       | set(rng.integers(0, w.N, 6).tolist()))
+    ws = torch.empty(api.decode_workspace_size(w.B, w.Hq, w.Hkv, w.N, w.d, w.g, w.w, Q.dtype),
+                     dtype=torch.uint8, device="cuda")
+    for pos in positions:
+        if not 0 <= pos < w.N:
+            continue
+        q = Q[:, :, pos].contiguous()
+        O, LSE = api.cca_decode_fwd(q, K, V, Kc, Vc, pos, w.g, w.w, workspace=ws)
+        torch.cuda.synchronize()
+        rows = [(b, h, pos) for b in range(w.B) for h in range(w.Hq)]
+        Oa, La = oracle.attn_rows(Q, K, V, Kc, Vc, w.g, w.w, rows)   # the GPU's own core tokens
+        check_out(O.reshape(-1, w.d), LSE.reshape(-1), Oa, La, Q.dtype, f"{w.name} pos {pos} attention")
+        Oe, Le = oracle.attn_rows(Q, K, V, Kr, Vr, w.g, w.w, rows)   # fp64 core tokens
+        check_out(O.reshape(-1, w.d), LSE.reshape(-1), Oe, Le, Q.dtype, f"{w.name} pos {pos} end-to-end")
+
+
+def test_decode_matches_prefill_row():
+    w = wl(1, 8, 8, 2048, 128, 16, 512)
+    Q, K, V = make_qkv(w, "cuda")
+    O, LSE, Kc, Vc = api.cca_prefill(Q, K, V, w.g, w.w)
+    for pos in (0, 700, 1500, 2047):
+        Od, Ld = api.cca_decode_fwd(Q[:, :, pos].contiguous(), K, V, Kc, Vc, pos, w.g, w.w)
+        torch.cuda.synchronize()
+        a, b = Od.float(), O[:, :, pos].float()
+        assert (a - b).abs().max().item() <= 2e-2 * b.abs().max().item()
+        assert (Ld - LSE[:, :, pos]).abs().max().item() <= 5e-3
+
+
+@pytest.mark.parametrize("w", [wl(2, 8, 2, 1024, 128, 16, 128), wl(1, 2, 2, 640, 64, 5, 50, "f32"),
+                               wl(1, 4, 4, 512, 128, 1, 16)], ids=lambda w: w.name)
+def test_pool_group_matches_full_pooling(w):
+    Q, K, V = make_qkv(w, "cuda")
+    Kc, Vc = api.cca_pool(Q, K, V, w.g)
+    Kg = torch.zeros_like(Kc)
+    Vg = torch.zeros_like(Vc)
+    for j in (0, 1, w.N // w.g // 2, w.N // w.g - 1):
+        api.cca_pool_group(Q[:, :, (j + 1) * w.g - 1].contiguous(), K, V, Kg, Vg, j, w.g)
+    torch.cuda.synchronize()
+    Kr, Vr = oracle.pool(Q, K, V, w.g)
+    for j in (0, 1, w.N // w.g // 2, w.N // w.g - 1):
+        check_cores(Kg[:, :, j], Vg[:, :, j], Kr[:, :, j], Vr[:, :, j], Q.dtype, f"{w.name} group {j}")
+
+
+def test_incremental_decode_loop():
+    """Prefill the first P tokens, then decode one token at a time, pooling each group
+    as soon as its last token is decoded; every step equals the oracle's row."""
+    w = wl(1, 4, 2, 1536, 128, 16, 256)
+    Q, K, V = make_qkv(w, "cuda")
+    P = 1000
+    G = w.N // w.g
+    Kc = torch.zeros((w.B, w.Hkv, G, w.d), dtype=Q.dtype, device="cuda")
+    Vc = torch.zeros_like(Kc)
+    # cores of the groups complete inside the prefix
+    for j in range(P // w.g):
+        api.cca_pool_group(Q[:, :, (j + 1) * w.g - 1].contiguous(), K, V, Kc, Vc, j, w.g)
+    Kr, Vr = oracle.pool(Q, K, V, w.g)
+    ws = torch.empty(api.decode_workspace_size(w.B, w.Hq, w.Hkv, w.N, w.d, w.g, w.w, Q.dtype),
+                     dtype=torch.uint8, device="cuda")
+    for pos in range(P, P + 70):
+        q = Q[:, :, pos].contiguous()
+        O, LSE = api.cca_decode_fwd(q, K, V, Kc, Vc, pos, w.g, w.w, workspace=ws)
+        if (pos + 1) % w.g == 0:
+            api.cca_pool_group(q, K, V, Kc, Vc, (pos + 1) // w.g - 1, w.g)
+        torch.cuda.synchronize()
+        rows = [(0, h, pos) for h in range(w.Hq)]
+        Oe, Le = oracle.attn_rows(Q, K, V, Kr, Vr, w.g, w.w, rows)
+        check_out(O.reshape(-1, w.d), LSE.reshape(-1), Oe, Le, Q.dtype, f"step {pos}")
