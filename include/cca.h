@@ -65,7 +65,8 @@ enum cca_status {
     CCA_ERR_INVALID_ARG = -1, /* null/misaligned pointer, bad size, N % g != 0, Hq % Hkv != 0 */
     CCA_ERR_UNSUPPORTED = -2, /* dtype/d combination not built, or the device is not sm_103 */
     CCA_ERR_CUDA = -3,        /* a CUDA runtime/driver call or the launch failed */
-    CCA_ERR_TIMEOUT = -4      /* written to dev_status by a kernel that gave up waiting */
+    CCA_ERR_TIMEOUT = -4,     /* written to dev_status by a kernel that gave up waiting */
+    CCA_ERR_SCRATCH_LIMIT = -5 /* cca_decode_fwd_noalloc: shapes exceed its fixed scratch */
 };
 
 enum cca_dtype {
@@ -136,6 +137,35 @@ int cca_decode_fwd(const void *Q, const void *K, const void *V, const void *Kc, 
 
 /* Bytes of workspace cca_decode_fwd needs for these shapes (0 on bad params). */
 uint64_t cca_decode_workspace_size(const cca_params_t *params);
+
+/*
+ * cca_decode_fwd_noalloc - cca_decode_fwd for callers that cannot allocate
+ * device memory.  The pages have no counterpart: this entry point exists for
+ * deployments in which this library may not obtain memory of its own, e.g. a
+ * plug-in inside a host framework that owns every device allocation through
+ * its own pool, a serving loop whose memory budget is fixed at start-up, or a
+ * caller that must avoid cudaMalloc's implicit device-wide synchronisation in
+ * its decode loop.  Such a caller can still pass its inputs and outputs, but
+ * not a workspace.
+ *
+ * Same arguments, semantics and support as cca_decode_fwd, minus the
+ * workspace: the per-split partial results live in one fixed array of
+ * CCA_DECODE_NOALLOC_MAX_BYTES inside the library's device code, which every
+ * GPU that loads the library holds until the process exits.  Shapes whose
+ * cca_decode_workspace_size() exceeds that maximum are rejected with
+ * CCA_ERR_SCRATCH_LIMIT before anything is launched.  The function calls no
+ * cudaMalloc/cudaFree and no allocating library routine.
+ *
+ * The first call on a device (with that device current) looks up the array's
+ * device address with cudaGetSymbolAddress; make that first call before any
+ * stream capture.  All calls share the one array: calls whose kernels may
+ * overlap on a GPU (different streams without ordering) race on it and give
+ * undefined results.  Nothing in it needs to start at zero: every call
+ * rewrites each partial it later reads.
+ */
+#define CCA_DECODE_NOALLOC_MAX_BYTES (4ull << 20)
+int cca_decode_fwd_noalloc(const void *Q, const void *K, const void *V, const void *Kc, const void *Vc,
+                           void *O, float *LSE, int pos, const cca_params_t *params, void *stream);
 
 /*
  * cca_pool_group - pool one newly completed group j of the caches (the

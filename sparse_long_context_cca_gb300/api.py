@@ -20,6 +20,7 @@ CCA_ERR_INVALID_ARG = -1
 CCA_ERR_UNSUPPORTED = -2
 CCA_ERR_CUDA = -3
 CCA_ERR_TIMEOUT = -4
+CCA_ERR_SCRATCH_LIMIT = -5
 CCA_BF16 = 0
 CCA_F32 = 1
 
@@ -44,6 +45,7 @@ _lib = None
 _lock = threading.Lock()
 
 EXPORTED = ["cca_pool", "cca_attn_fwd", "cca_decode_fwd", "cca_decode_workspace_size", "cca_pool_group",
+            "cca_decode_fwd_noalloc",
             "cca_status_string", "cca_abi_version", "cca_test_set_wait_limit_ns", "cca_test_skip_q_load"]
 
 
@@ -70,6 +72,8 @@ def load_library():
         lib.cca_attn_fwd.restype = ctypes.c_int
         lib.cca_decode_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, ctypes.c_int, pp, vp, ctypes.c_uint64, vp]
         lib.cca_decode_fwd.restype = ctypes.c_int
+        lib.cca_decode_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, ctypes.c_int, pp, vp]
+        lib.cca_decode_fwd_noalloc.restype = ctypes.c_int
         lib.cca_decode_workspace_size.argtypes = [pp]
         lib.cca_decode_workspace_size.restype = ctypes.c_uint64
         lib.cca_pool_group.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, pp, vp]

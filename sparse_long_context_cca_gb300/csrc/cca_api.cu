@@ -13,6 +13,8 @@ extern unsigned long long g_wait_limit_ns;
 extern int g_skip_q_load;
 }  // namespace cca
 
+static_assert(cca::DECODE_NOALLOC_MAX_BYTES == CCA_DECODE_NOALLOC_MAX_BYTES, "scratch size mismatch");
+
 namespace {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -119,6 +121,26 @@ int cca_decode_fwd(const void *Q, const void *K, const void *V, const void *Kc, 
                                         static_cast<float *>(workspace), static_cast<cudaStream_t>(stream)));
 }
 
+int cca_decode_fwd_noalloc(const void *Q, const void *K, const void *V, const void *Kc, const void *Vc, void *O,
+                           float *LSE, int pos, const cca_params_t *params, void *stream) {
+    int st = check_shape(params, true);
+    if (st != CCA_OK) return st;
+    const void *ptrs[7] = {Q, K, V, Kc, Vc, O, LSE};
+    for (const void *q : ptrs)
+        if (q == nullptr || !aligned16(q)) return CCA_ERR_INVALID_ARG;
+    if (pos < 0 || pos >= params->N) return CCA_ERR_INVALID_ARG;
+    const int r = params->Hq / params->Hkv;
+    if (r != 1 && r != 2 && r != 4 && r != 8) return CCA_ERR_UNSUPPORTED;
+    const cca::Shape s = to_shape(params);
+    if (cca::decode_workspace_bytes(s) > cca::DECODE_NOALLOC_MAX_BYTES) return CCA_ERR_SCRATCH_LIMIT;
+    if ((st = check_device()) != CCA_OK) return st;
+    float *scratch = nullptr;
+    cudaError_t e = cca::decode_noalloc_scratch(&scratch);
+    if (e != cudaSuccess) return CCA_ERR_CUDA;
+    return from_cuda(cca::launch_decode(params->dtype, Q, K, V, Kc, Vc, O, LSE, s, pos, scratch,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
 uint64_t cca_decode_workspace_size(const cca_params_t *params) {
     if (check_shape(params, true) != CCA_OK) return 0;
     return cca::decode_workspace_bytes(to_shape(params));
@@ -144,6 +166,7 @@ const char *cca_status_string(int status) {
         case CCA_ERR_UNSUPPORTED: return "unsupported dtype/head-dim combination or device";
         case CCA_ERR_CUDA: return "CUDA error";
         case CCA_ERR_TIMEOUT: return "device pipeline wait timed out";
+        case CCA_ERR_SCRATCH_LIMIT: return "shapes need more scratch than the no-allocation entry point holds";
         default: return "unknown status";
     }
 }

@@ -355,6 +355,30 @@ cudaError_t dispatch_r(const void *Q, const void *K, const void *V, const void *
 
 }  // namespace
 
+// Scratch of cca_decode_fwd_noalloc: a fixed array in the library's device image.
+// Every GPU that loads the library holds it until the process exits.  Host code may
+// not use its name as an address (on the host it is only a stand-in); the device
+// address is looked up once per device with cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_decode_scratch[DECODE_NOALLOC_MAX_BYTES];
+
+cudaError_t decode_noalloc_scratch(float **out) {
+    static std::mutex mu;
+    static void *ptrs[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (ptrs[dev] == nullptr) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_decode_scratch);  // with `dev` current
+        if (e != cudaSuccess) return e;
+        ptrs[dev] = p;
+    }
+    *out = static_cast<float *>(ptrs[dev]);
+    return cudaSuccess;
+}
+
 uint64_t decode_workspace_bytes(const Shape &s) {
     return static_cast<uint64_t>(s.B) * s.Hq * MAX_SPLITS * (s.d + 2) * sizeof(float);
 }

@@ -32,6 +32,10 @@ cudaError_t launch_attn_bf16_tc(const void *Q, const void *K, const void *V, con
 uint64_t decode_workspace_bytes(const Shape &s);
 cudaError_t launch_decode(int dtype, const void *Q, const void *K, const void *V, const void *Kc, const void *Vc,
                           void *O, float *LSE, const Shape &s, int pos, float *ws, cudaStream_t stream);
+// Fixed scratch of the no-allocation decode entry point (bytes) and its device address
+// on the current device (looked up on first use per device).
+constexpr uint64_t DECODE_NOALLOC_MAX_BYTES = 4ull << 20;
+cudaError_t decode_noalloc_scratch(float **out);
 cudaError_t launch_pool_group(int dtype, const void *q, const void *K, const void *V, void *Kc, void *Vc,
                               const Shape &s, int j, cudaStream_t stream);
 
