@@ -64,6 +64,13 @@ def _bind(lib):
     lib.cca_oracle_attn_rows.argtypes = [dp, dp, dp, dp, dp, ip, ctypes.c_int64, dp, dp,
                                          i, i, i, i, i, i, i, ctypes.c_double]
     lib.cca_oracle_attn_rows.restype = None
+    lib.cca_oracle_pool_mode.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i, i, ctypes.c_double, i]
+    lib.cca_oracle_pool_mode.restype = None
+    lib.cca_oracle_attn_mode.argtypes = [dp, dp, dp, dp, dp, dp, dp, i, i, i, i, i, i, i, ctypes.c_double, i]
+    lib.cca_oracle_attn_mode.restype = None
+    lib.cca_oracle_attn_rows_mode.argtypes = [dp, dp, dp, dp, dp, ip, ctypes.c_int64, dp, dp,
+                                              i, i, i, i, i, i, i, ctypes.c_double, i]
+    lib.cca_oracle_attn_rows_mode.restype = None
     lib.cca_oracle_threads.argtypes = []
     lib.cca_oracle_threads.restype = ctypes.c_int
     lib.cca_oracle_set_threads.argtypes = [ctypes.c_int]
@@ -104,8 +111,9 @@ def _shapes(Q, K):
     return B, Hq, Hkv, N, d
 
 
-def pool(Q, K, V, g: int, scale: float | None = None, lib=None):
-    """Global-aware pooling -> (Kc, Vc), each [B, Hkv, N/g, d] fp64."""
+def pool(Q, K, V, g: int, scale: float | None = None, lib=None, pool_mode: int = 0):
+    """Global-aware pooling -> (Kc, Vc), each [B, Hkv, N/g, d] fp64.
+    pool_mode 0: softmax weights of the group-last query (the method); 1: mean; 2: max."""
     lib = lib or load()
     Q, K, V = widen(Q), widen(K), widen(V)
     B, Hq, Hkv, N, d = _shapes(Q, K)
@@ -113,12 +121,14 @@ def pool(Q, K, V, g: int, scale: float | None = None, lib=None):
     scale = float(d) ** -0.5 if scale is None else float(scale)
     Kc = np.zeros((B, Hkv, N // g, d))
     Vc = np.zeros((B, Hkv, N // g, d))
-    lib.cca_oracle_pool(_ptr(Q), _ptr(K), _ptr(V), _ptr(Kc), _ptr(Vc), B, Hq, Hkv, N, d, g, scale)
+    lib.cca_oracle_pool_mode(_ptr(Q), _ptr(K), _ptr(V), _ptr(Kc), _ptr(Vc), B, Hq, Hkv, N, d, g, scale,
+                             int(pool_mode))
     return Kc, Vc
 
 
-def attn(Q, K, V, Kc, Vc, g: int, w: int, scale: float | None = None, lib=None):
-    """Fused core/local attention -> (O [B,Hq,N,d], LSE [B,Hq,N]) in fp64."""
+def attn(Q, K, V, Kc, Vc, g: int, w: int, scale: float | None = None, lib=None, window_mode: int = 0):
+    """Fused core/local attention -> (O [B,Hq,N,d], LSE [B,Hq,N]) in fp64.
+    window_mode 1: raw window starts at the group boundary g*(lo(i)//g) (no gap)."""
     lib = lib or load()
     Q, K, V, Kc, Vc = (widen(t) for t in (Q, K, V, Kc, Vc))
     B, Hq, Hkv, N, d = _shapes(Q, K)
@@ -126,12 +136,13 @@ def attn(Q, K, V, Kc, Vc, g: int, w: int, scale: float | None = None, lib=None):
     scale = float(d) ** -0.5 if scale is None else float(scale)
     O = np.zeros((B, Hq, N, d))
     LSE = np.zeros((B, Hq, N))
-    lib.cca_oracle_attn(_ptr(Q), _ptr(K), _ptr(V), _ptr(Kc), _ptr(Vc), _ptr(O), _ptr(LSE),
-                        B, Hq, Hkv, N, d, g, w, scale)
+    lib.cca_oracle_attn_mode(_ptr(Q), _ptr(K), _ptr(V), _ptr(Kc), _ptr(Vc), _ptr(O), _ptr(LSE),
+                             B, Hq, Hkv, N, d, g, w, scale, int(window_mode))
     return O, LSE
 
 
-def attn_rows(Q, K, V, Kc, Vc, g: int, w: int, rows, scale: float | None = None, lib=None):
+def attn_rows(Q, K, V, Kc, Vc, g: int, w: int, rows, scale: float | None = None, lib=None,
+              window_mode: int = 0):
     """Fused attention for selected (b, h, i) rows -> (O [n, d], LSE [n])."""
     lib = lib or load()
     Q, K, V, Kc, Vc = (widen(t) for t in (Q, K, V, Kc, Vc))
@@ -141,14 +152,15 @@ def attn_rows(Q, K, V, Kc, Vc, g: int, w: int, rows, scale: float | None = None,
     n = rows.shape[0]
     O = np.zeros((n, d))
     LSE = np.zeros((n,))
-    lib.cca_oracle_attn_rows(_ptr(Q), _ptr(K), _ptr(V), _ptr(Kc), _ptr(Vc),
-                             rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), n,
-                             _ptr(O), _ptr(LSE), B, Hq, Hkv, N, d, g, w, scale)
+    lib.cca_oracle_attn_rows_mode(_ptr(Q), _ptr(K), _ptr(V), _ptr(Kc), _ptr(Vc),
+                                  rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), n,
+                                  _ptr(O), _ptr(LSE), B, Hq, Hkv, N, d, g, w, scale, int(window_mode))
     return O, LSE
 
 
-def prefill(Q, K, V, g: int, w: int, scale: float | None = None, lib=None):
+def prefill(Q, K, V, g: int, w: int, scale: float | None = None, lib=None, pool_mode: int = 0,
+            window_mode: int = 0):
     """End-to-end: pooling in fp64 (core tokens are not rounded), then attention."""
-    Kc, Vc = pool(Q, K, V, g, scale, lib=lib)
-    O, LSE = attn(Q, K, V, Kc, Vc, g, w, scale, lib=lib)
+    Kc, Vc = pool(Q, K, V, g, scale, lib=lib, pool_mode=pool_mode)
+    O, LSE = attn(Q, K, V, Kc, Vc, g, w, scale, lib=lib, window_mode=window_mode)
     return O, LSE, Kc, Vc

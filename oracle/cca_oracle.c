@@ -26,6 +26,14 @@
  *    group softmax; query head h reads KV head h / r;
  *  - scale = 1/sqrt(d) unless the caller passes another; natural-log LSE.
  *
+ * Variants (the ablations the pages mention; mode 0 is the method itself):
+ *  - pool_mode 1, mean pooling: every token of the group weighs 1/g;
+ *  - pool_mode 2, max pooling: the element-wise maximum of the group's keys
+ *    and of its values (OpenReview rebuttal, pooling-ablation table);
+ *  - window_mode 1, the window reaches back to the start of the group that
+ *    holds lo(i): raw tokens [g*(lo(i)/g), i], so that together with the cores
+ *    every earlier token is covered ("at least w preceding raw tokens").
+ *
  * Layouts: Q [B, Hq, N, d], K and V [B, Hkv, N, d], Kc and Vc [B, Hkv, N/g, d],
  * O [B, Hq, N, d], LSE [B, Hq, N]; all contiguous row-major fp64.
  */
@@ -57,8 +65,8 @@ void cca_oracle_set_threads(int n) {
 
 /* Global-aware pooling (pooling equation): one core key and one core value per
  * (batch, KV head, group). */
-void cca_oracle_pool(const double *Q, const double *K, const double *V, double *Kc, double *Vc,
-                     int B, int Hq, int Hkv, int N, int d, int g, double scale) {
+void cca_oracle_pool_mode(const double *Q, const double *K, const double *V, double *Kc, double *Vc,
+                          int B, int Hq, int Hkv, int N, int d, int g, double scale, int pool_mode) {
     const int64_t r = Hq / Hkv;
     const int64_t n_groups = N / g;
     const int64_t total = (int64_t)B * Hkv * n_groups;
@@ -87,6 +95,24 @@ void cca_oracle_pool(const double *Q, const double *K, const double *V, double *
                 }
                 s[t] = scale * acc / (double)r;
             }
+            if (pool_mode == 1)
+                for (int64_t t = 0; t < g; ++t) s[t] = 0.0; /* mean pooling: equal weights */
+            if (pool_mode == 2) {
+                /* max pooling: element-wise maximum of the group's keys and values */
+                double *kc = Kc + (bk * n_groups + j) * d;
+                double *vc = Vc + (bk * n_groups + j) * d;
+                for (int64_t c = 0; c < d; ++c) {
+                    double km = Kh[(j * g) * d + c], vm = Vh[(j * g) * d + c];
+                    for (int64_t t = 1; t < g; ++t) {
+                        const double kv_ = Kh[(j * g + t) * d + c], vv_ = Vh[(j * g + t) * d + c];
+                        km = kv_ > km ? kv_ : km;
+                        vm = vv_ > vm ? vv_ : vm;
+                    }
+                    kc[c] = km;
+                    vc[c] = vm;
+                }
+                continue;
+            }
             /* softmax over the group */
             double mx = s[0];
             for (int64_t t = 1; t < g; ++t) mx = s[t] > mx ? s[t] : mx;
@@ -111,9 +137,9 @@ void cca_oracle_pool(const double *Q, const double *K, const double *V, double *
  * followed by the raw tokens of the local window. */
 static void attend_row(const double *q, const double *Kh, const double *Vh, const double *Kch,
                        const double *Vch, int64_t i, int64_t d, int64_t g, int64_t w, double scale,
-                       double *z, double *o, double *lse) {
-    const int64_t lo = window_lo(i, w);
-    const int64_t n_core = lo / g;
+                       int window_mode, double *z, double *o, double *lse) {
+    const int64_t n_core = window_lo(i, w) / g;
+    const int64_t lo = window_mode ? n_core * g : window_lo(i, w); /* first raw token */
     const int64_t n_loc = i - lo + 1;
     for (int64_t j = 0; j < n_core; ++j) {
         double dot = 0.0;
@@ -144,38 +170,38 @@ static void attend_row(const double *q, const double *Kh, const double *Vh, cons
 
 /* Selected rows only: rows[3*t .. 3*t+2] = (b, h, i); outputs O[n_rows, d],
  * LSE[n_rows]. */
-void cca_oracle_attn_rows(const double *Q, const double *K, const double *V, const double *Kc,
-                          const double *Vc, const int64_t *rows, int64_t n_rows, double *O,
-                          double *LSE, int B, int Hq, int Hkv, int N, int d, int g, int w,
-                          double scale) {
+void cca_oracle_attn_rows_mode(const double *Q, const double *K, const double *V, const double *Kc,
+                               const double *Vc, const int64_t *rows, int64_t n_rows, double *O,
+                               double *LSE, int B, int Hq, int Hkv, int N, int d, int g, int w,
+                               double scale, int window_mode) {
     (void)B;
     const int64_t r = Hq / Hkv;
     const int64_t n_groups = N / g;
 #pragma omp parallel
     {
-        double *z = (double *)malloc(sizeof(double) * (size_t)(n_groups + (w < N ? w : N) + 1));
+        double *z = (double *)malloc(sizeof(double) * (size_t)(n_groups + (w < N ? w : N) + g + 1));
 #pragma omp for schedule(dynamic, 16)
         for (int64_t t = 0; t < n_rows; ++t) {
             const int64_t b = rows[3 * t], h = rows[3 * t + 1], i = rows[3 * t + 2];
             const int64_t bk = b * Hkv + h / r;
             attend_row(Q + ((b * Hq + h) * (int64_t)N + i) * d, K + bk * (int64_t)N * d,
                        V + bk * (int64_t)N * d, Kc + bk * n_groups * d, Vc + bk * n_groups * d, i,
-                       d, g, w, scale, z, O + t * d, LSE + t);
+                       d, g, w, scale, window_mode, z, O + t * d, LSE + t);
         }
         free(z);
     }
 }
 
 /* Every row of every (batch, query head). */
-void cca_oracle_attn(const double *Q, const double *K, const double *V, const double *Kc,
-                     const double *Vc, double *O, double *LSE, int B, int Hq, int Hkv, int N, int d,
-                     int g, int w, double scale) {
+void cca_oracle_attn_mode(const double *Q, const double *K, const double *V, const double *Kc,
+                          const double *Vc, double *O, double *LSE, int B, int Hq, int Hkv, int N, int d,
+                          int g, int w, double scale, int window_mode) {
     const int64_t r = Hq / Hkv;
     const int64_t n_groups = N / g;
     const int64_t total = (int64_t)B * Hq * N;
 #pragma omp parallel
     {
-        double *z = (double *)malloc(sizeof(double) * (size_t)(n_groups + (w < N ? w : N) + 1));
+        double *z = (double *)malloc(sizeof(double) * (size_t)(n_groups + (w < N ? w : N) + g + 1));
 #pragma omp for schedule(dynamic, 64)
         for (int64_t u = 0; u < total; ++u) {
             const int64_t i = u % N;
@@ -183,9 +209,26 @@ void cca_oracle_attn(const double *Q, const double *K, const double *V, const do
             const int64_t b = bh / Hq, h = bh % Hq;
             const int64_t bk = b * Hkv + h / r;
             attend_row(Q + u * d, K + bk * (int64_t)N * d, V + bk * (int64_t)N * d,
-                       Kc + bk * n_groups * d, Vc + bk * n_groups * d, i, d, g, w, scale, z,
-                       O + u * d, LSE + u);
+                       Kc + bk * n_groups * d, Vc + bk * n_groups * d, i, d, g, w, scale, window_mode,
+                       z, O + u * d, LSE + u);
         }
         free(z);
     }
+}
+
+/* The method itself (pool_mode 0, window_mode 0). */
+void cca_oracle_pool(const double *Q, const double *K, const double *V, double *Kc, double *Vc,
+                     int B, int Hq, int Hkv, int N, int d, int g, double scale) {
+    cca_oracle_pool_mode(Q, K, V, Kc, Vc, B, Hq, Hkv, N, d, g, scale, 0);
+}
+void cca_oracle_attn(const double *Q, const double *K, const double *V, const double *Kc,
+                     const double *Vc, double *O, double *LSE, int B, int Hq, int Hkv, int N, int d,
+                     int g, int w, double scale) {
+    cca_oracle_attn_mode(Q, K, V, Kc, Vc, O, LSE, B, Hq, Hkv, N, d, g, w, scale, 0);
+}
+void cca_oracle_attn_rows(const double *Q, const double *K, const double *V, const double *Kc,
+                          const double *Vc, const int64_t *rows, int64_t n_rows, double *O,
+                          double *LSE, int B, int Hq, int Hkv, int N, int d, int g, int w,
+                          double scale) {
+    cca_oracle_attn_rows_mode(Q, K, V, Kc, Vc, rows, n_rows, O, LSE, B, Hq, Hkv, N, d, g, w, scale, 0);
 }

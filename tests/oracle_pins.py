@@ -254,7 +254,48 @@ def pin_dense_mask_formulation(lib):
         np.testing.assert_allclose(LSE, LSE2, rtol=0, atol=1e-12)
 
 
+def pin_group_aligned_window_counts(lib):
+    data = _golden("visibility_counts.json")["group_aligned_window"]
+    for case in data["cases"]:
+        N, g, w = case["N"], case["g"], case["w"]
+        Q = np.zeros((1, 1, N, 8))
+        K, V = _rand((1, 1, N, 8), 41), _rand((1, 1, N, 8), 42)
+        Kc, Vc = oracle.pool(Q, K, V, g, lib=lib)
+        rows = [(0, 0, i) for i, _, _ in case["rows"]]
+        _, LSE = oracle.attn_rows(Q, K, V, Kc, Vc, g, w, rows, lib=lib, window_mode=1)
+        want = np.array([nc + nl for _, nc, nl in case["rows"]], dtype=np.float64)
+        np.testing.assert_allclose(np.exp(LSE), want, rtol=1e-12, atol=0)
+
+
+def pin_group_aligned_window_no_gap(lib):
+    # With g = 1 both windows coincide; with w >= N both are plain causal attention.
+    N, d = 40, 8
+    Q, K, V = _rand((1, 2, N, d), 43), _rand((1, 2, N, d), 44), _rand((1, 2, N, d), 45)
+    for g, w in ((1, 6), (4, 64)):
+        O0, L0, _, _ = oracle.prefill(Q, K, V, g, w, lib=lib)
+        O1, L1, _, _ = oracle.prefill(Q, K, V, g, w, lib=lib, window_mode=1)
+        np.testing.assert_allclose(O1, O0, rtol=0, atol=1e-13)
+        np.testing.assert_allclose(L1, L0, rtol=0, atol=1e-13)
+
+
+def pin_mean_pooling(lib):
+    B, H, N, d, g = 1, 2, 40, 8, 5
+    Q, K, V = _rand((B, H, N, d), 46, 3.0), _rand((B, H, N, d), 47), _rand((B, H, N, d), 48)
+    Kc, Vc = oracle.pool(Q, K, V, g, lib=lib, pool_mode=1)
+    np.testing.assert_allclose(Kc, K.reshape(B, H, N // g, g, d).mean(axis=3), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(Vc, V.reshape(B, H, N // g, g, d).mean(axis=3), rtol=0, atol=1e-12)
+
+
+def pin_max_pooling(lib):
+    B, H, N, d, g = 1, 2, 40, 8, 5
+    Q, K, V = _rand((B, H, N, d), 49), _rand((B, H, N, d), 50), _rand((B, H, N, d), 51)
+    Kc, Vc = oracle.pool(Q, K, V, g, lib=lib, pool_mode=2)
+    np.testing.assert_array_equal(Kc, K.reshape(B, H, N // g, g, d).max(axis=3))
+    np.testing.assert_array_equal(Vc, V.reshape(B, H, N // g, g, d).max(axis=3))
+
+
 ALL_PINS = [pin_worked_example, pin_gqa_worked_example, pin_visibility_counts, pin_g1_is_causal,
             pin_wide_window_is_causal, pin_early_rows_are_sliding_window, pin_pool_equal_keys_mean,
             pin_pool_zero_query_mean, pin_pool_dominant_query_selects, pin_unit_values,
-            pin_constant_keys_lse, pin_causality, pin_dense_mask_formulation]
+            pin_constant_keys_lse, pin_causality, pin_dense_mask_formulation,
+            pin_group_aligned_window_counts, pin_group_aligned_window_no_gap, pin_mean_pooling, pin_max_pooling]

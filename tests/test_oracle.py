@@ -29,8 +29,15 @@ MUTANTS = {
     "pool_first_token_query": ("const int64_t last = (j + 1) * g - 1;", "const int64_t last = j * g;"),
     "pool_not_normalised": ("const double a = s[t] / den;", "const double a = s[t];"),
     "pool_values_weighted_by_keys": ("vc[c] += a * v[c];", "vc[c] += a * k[c];"),
-    "partial_group_visible": ("const int64_t n_core = lo / g;", "const int64_t n_core = (lo + g - 1) / g;"),
-    "one_core_too_few": ("const int64_t n_core = lo / g;", "const int64_t n_core = lo / g > 0 ? lo / g - 1 : 0;"),
+    "partial_group_visible": ("const int64_t n_core = window_lo(i, w) / g;",
+                              "const int64_t n_core = (window_lo(i, w) + g - 1) / g;"),
+    "one_core_too_few": ("const int64_t n_core = window_lo(i, w) / g;",
+                         "const int64_t n_core = window_lo(i, w) / g > 0 ? window_lo(i, w) / g - 1 : 0;"),
+    "aligned_window_not_aligned": ("const int64_t lo = window_mode ? n_core * g : window_lo(i, w);",
+                                   "const int64_t lo = window_lo(i, w);"),
+    "max_pool_takes_min": ("km = kv_ > km ? kv_ : km;", "km = kv_ < km ? kv_ : km;"),
+    "mean_pool_not_uniform": ("for (int64_t t = 0; t < g; ++t) s[t] = 0.0; /* mean pooling: equal weights */",
+                              "(void)0; /* mean pooling: equal weights */"),
     "window_too_wide": ("return i - w + 1 > 0 ? i - w + 1 : 0;", "return i - w > 0 ? i - w : 0;"),
     "window_too_narrow": ("return i - w + 1 > 0 ? i - w + 1 : 0;", "return i - w + 2 > 0 ? (i - w + 2 < i ? i - w + 2 : i) : 0;"),
     "core_scale_dropped": ("z[j] = scale * dot;", "z[j] = dot;"),
