@@ -58,7 +58,7 @@
 extern "C" {
 #endif
 
-#define CCA_ABI_VERSION 1
+#define CCA_ABI_VERSION 2
 
 enum cca_status {
     CCA_OK = 0,
@@ -85,6 +85,11 @@ typedef struct cca_params {
     int32_t dtype;      /* enum cca_dtype */
     float scale;        /* softmax scale; <= 0 selects 1/sqrt(d) */
     int32_t *dev_status;/* optional device int32, see "Errors" above */
+    int32_t window_mode;/* 0: raw window [lo(i), i] (the method as read here);
+                           1: raw window [g*(lo(i)/g), i], reaching back to the group boundary
+                              so that cores + window cover every earlier token */
+    int32_t pool_mode;  /* 0: softmax weights of the group-last query (the method);
+                           1: mean pooling; 2: element-wise max pooling (the pages' ablations) */
 } cca_params_t;
 
 /*

@@ -38,7 +38,8 @@ class CcaParams(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int32), ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32),
                 ("N", ctypes.c_int32), ("d", ctypes.c_int32), ("g", ctypes.c_int32),
                 ("w", ctypes.c_int32), ("dtype", ctypes.c_int32), ("scale", ctypes.c_float),
-                ("dev_status", ctypes.c_void_p)]
+                ("dev_status", ctypes.c_void_p), ("window_mode", ctypes.c_int32),
+                ("pool_mode", ctypes.c_int32)]
 
 
 _lib = None
@@ -94,9 +95,10 @@ def status_string(status: int) -> str:
     return load_library().cca_status_string(int(status)).decode()
 
 
-def make_params(B, Hq, Hkv, N, d, g, w, dtype, scale=0.0, dev_status=None) -> CcaParams:
+def make_params(B, Hq, Hkv, N, d, g, w, dtype, scale=0.0, dev_status=None, window_mode=0,
+                pool_mode=0) -> CcaParams:
     return CcaParams(int(B), int(Hq), int(Hkv), int(N), int(d), int(g), int(w), int(dtype),
-                     float(scale), dev_status)
+                     float(scale), dev_status, int(window_mode), int(pool_mode))
 
 
 def _stream_handle(stream) -> int:
@@ -124,8 +126,9 @@ def _dims(Q, K):
     return B, Hq, Hkv, N, d
 
 
-def cca_pool(Q, K, V, g: int, Kc=None, Vc=None, scale: float = 0.0, stream=None):
-    """Global-aware pooling: returns (Kc, Vc), each [B, Hkv, N/g, d]."""
+def cca_pool(Q, K, V, g: int, Kc=None, Vc=None, scale: float = 0.0, stream=None, pool_mode: int = 0):
+    """Global-aware pooling: returns (Kc, Vc), each [B, Hkv, N/g, d].
+    pool_mode 0: softmax weights of the group-last query; 1: mean; 2: element-wise max."""
     lib = load_library()
     B, Hq, Hkv, N, d = _dims(Q, K)
     if Q.dtype not in _DTYPE:
@@ -140,7 +143,7 @@ def cca_pool(Q, K, V, g: int, Kc=None, Vc=None, scale: float = 0.0, stream=None)
         Vc = torch.empty((B, Hkv, G, d), dtype=Q.dtype, device=Q.device)
     _check(Kc, "Kc", Q.dtype, (B, Hkv, G, d))
     _check(Vc, "Vc", Q.dtype, (B, Hkv, G, d))
-    prm = make_params(B, Hq, Hkv, N, d, g, 1, _DTYPE[Q.dtype], scale)
+    prm = make_params(B, Hq, Hkv, N, d, g, 1, _DTYPE[Q.dtype], scale, pool_mode=pool_mode)
     st = lib.cca_pool(Q.data_ptr(), K.data_ptr(), V.data_ptr(), Kc.data_ptr(), Vc.data_ptr(),
                       ctypes.byref(prm), _stream_handle(stream))
     if st != CCA_OK:
@@ -149,8 +152,9 @@ def cca_pool(Q, K, V, g: int, Kc=None, Vc=None, scale: float = 0.0, stream=None)
 
 
 def cca_attn_fwd(Q, K, V, Kc, Vc, g: int, w: int, O=None, LSE=None, scale: float = 0.0,
-                 dev_status=None, stream=None):
-    """Fused core/local attention: returns (O [B,Hq,N,d], LSE [B,Hq,N] fp32)."""
+                 dev_status=None, stream=None, window_mode: int = 0):
+    """Fused core/local attention: returns (O [B,Hq,N,d], LSE [B,Hq,N] fp32).
+    window_mode 1: the raw window starts at the group boundary g*(lo(i)//g)."""
     lib = load_library()
     B, Hq, Hkv, N, d = _dims(Q, K)
     if Q.dtype not in _DTYPE:
@@ -171,7 +175,7 @@ def cca_attn_fwd(Q, K, V, Kc, Vc, g: int, w: int, O=None, LSE=None, scale: float
     if dev_status is not None:
         _check(dev_status, "dev_status", torch.int32, (1,))
         status_ptr = dev_status.data_ptr()
-    prm = make_params(B, Hq, Hkv, N, d, g, w, _DTYPE[Q.dtype], scale, status_ptr)
+    prm = make_params(B, Hq, Hkv, N, d, g, w, _DTYPE[Q.dtype], scale, status_ptr, window_mode=window_mode)
     st = lib.cca_attn_fwd(Q.data_ptr(), K.data_ptr(), V.data_ptr(), Kc.data_ptr(), Vc.data_ptr(),
                           O.data_ptr(), LSE.data_ptr(), ctypes.byref(prm), _stream_handle(stream))
     if st != CCA_OK:
@@ -179,14 +183,15 @@ def cca_attn_fwd(Q, K, V, Kc, Vc, g: int, w: int, O=None, LSE=None, scale: float
     return O, LSE
 
 
-def cca_prefill(Q, K, V, g: int, w: int, scale: float = 0.0, out=None, stream=None):
+def cca_prefill(Q, K, V, g: int, w: int, scale: float = 0.0, out=None, stream=None, pool_mode: int = 0,
+                window_mode: int = 0):
     """Both steps of CCA prefill: pooling, then fused attention.
     Returns (O, LSE, Kc, Vc).  `out` may hold preallocated (O, LSE, Kc, Vc)."""
     O = LSE = Kc = Vc = None
     if out is not None:
         O, LSE, Kc, Vc = out
-    Kc, Vc = cca_pool(Q, K, V, g, Kc, Vc, scale, stream)
-    O, LSE = cca_attn_fwd(Q, K, V, Kc, Vc, g, w, O, LSE, scale, None, stream)
+    Kc, Vc = cca_pool(Q, K, V, g, Kc, Vc, scale, stream, pool_mode=pool_mode)
+    O, LSE = cca_attn_fwd(Q, K, V, Kc, Vc, g, w, O, LSE, scale, None, stream, window_mode=window_mode)
     return O, LSE, Kc, Vc
 
 
@@ -205,7 +210,7 @@ def decode_workspace_size(B, Hq, Hkv, Ncap, d, g, w, dtype) -> int:
 
 
 def cca_decode_fwd(q, K, V, Kc, Vc, pos: int, g: int, w: int, O=None, LSE=None, workspace=None,
-                   scale: float = 0.0, stream=None):
+                   scale: float = 0.0, stream=None, window_mode: int = 0):
     """One decoding step: row `pos` of the fused attention over the caches.
     q [B, Hq, d]; K, V [B, Hkv, Ncap, d]; Kc, Vc [B, Hkv, Ncap/g, d].
     Returns (O [B, Hq, d], LSE [B, Hq])."""
@@ -228,7 +233,7 @@ def cca_decode_fwd(q, K, V, Kc, Vc, pos: int, g: int, w: int, O=None, LSE=None, 
         LSE = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
     _check(O, "O", q.dtype, (B, Hq, d))
     _check(LSE, "LSE", torch.float32, (B, Hq))
-    prm = make_params(B, Hq, Hkv, Ncap, d, g, w, _DTYPE[q.dtype], scale)
+    prm = make_params(B, Hq, Hkv, Ncap, d, g, w, _DTYPE[q.dtype], scale, window_mode=window_mode)
     need = int(lib.cca_decode_workspace_size(ctypes.byref(prm)))
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
@@ -242,7 +247,7 @@ def cca_decode_fwd(q, K, V, Kc, Vc, pos: int, g: int, w: int, O=None, LSE=None, 
     return O, LSE
 
 
-def cca_pool_group(q, K, V, Kc, Vc, j: int, g: int, scale: float = 0.0, stream=None):
+def cca_pool_group(q, K, V, Kc, Vc, j: int, g: int, scale: float = 0.0, stream=None, pool_mode: int = 0):
     """Pool the newly completed group j of the caches in place (Kc[:, :, j], Vc[:, :, j]),
     scored by q [B, Hq, d], the query of the group's last token."""
     lib = load_library()
@@ -254,7 +259,7 @@ def cca_pool_group(q, K, V, Kc, Vc, j: int, g: int, scale: float = 0.0, stream=N
     _check(V, "V", q.dtype, (B, Hkv, Ncap, d))
     _check(Kc, "Kc", q.dtype, (B, Hkv, G, d))
     _check(Vc, "Vc", q.dtype, (B, Hkv, G, d))
-    prm = make_params(B, Hq, Hkv, Ncap, d, g, 1, _DTYPE[q.dtype], scale)
+    prm = make_params(B, Hq, Hkv, Ncap, d, g, 1, _DTYPE[q.dtype], scale, pool_mode=pool_mode)
     st = lib.cca_pool_group(q.data_ptr(), K.data_ptr(), V.data_ptr(), Kc.data_ptr(), Vc.data_ptr(), int(j),
                             ctypes.byref(prm), _stream_handle(stream))
     if st != CCA_OK:

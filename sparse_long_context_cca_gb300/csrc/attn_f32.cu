@@ -57,7 +57,8 @@ __global__ void __launch_bounds__(128) attn_f32_kernel(const float *__restrict__
                                                        const float *__restrict__ Kc,
                                                        const float *__restrict__ Vc, float *__restrict__ O,
                                                        float *__restrict__ LSE, int Hq, int Hkv, int N,
-                                                       int g, int w, float scale_log2, int64_t total_rows) {
+                                                       int g, int w, int window_mode, float scale_log2,
+                                                       int64_t total_rows) {
     constexpr int PL = D / 32;
     const int lane = threadIdx.x & 31;
     const int64_t u = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -74,8 +75,9 @@ __global__ void __launch_bounds__(128) attn_f32_kernel(const float *__restrict__
         st.q[e] = Q[u * D + lane * PL + e];
         st.o[e] = 0.f;
     }
-    const int64_t lo = i - w + 1 > 0 ? i - w + 1 : 0;
-    const int64_t n_core = lo / g;
+    const int64_t lo_w = i - w + 1 > 0 ? i - w + 1 : 0;
+    const int64_t n_core = lo_w / g;
+    const int64_t lo = window_mode ? n_core * g : lo_w;  // first raw token of the window
     const float *kc = Kc + bk * G * D;
     const float *vc = Vc + bk * G * D;
     for (int64_t j = 0; j < n_core; ++j) st.step(kc + j * D, vc + j * D, lane, scale_log2);
@@ -99,10 +101,10 @@ cudaError_t launch_attn_f32(const float *Q, const float *K, const float *V, cons
     const float scale_log2 = s.scale * 1.4426950408889634f;
     if (s.d == 64) {
         attn_f32_kernel<64><<<blocks, warps * 32, 0, stream>>>(Q, K, V, Kc, Vc, O, LSE, s.Hq, s.Hkv, s.N, s.g,
-                                                               s.w, scale_log2, rows);
+                                                               s.w, s.window_mode, scale_log2, rows);
     } else if (s.d == 128) {
         attn_f32_kernel<128><<<blocks, warps * 32, 0, stream>>>(Q, K, V, Kc, Vc, O, LSE, s.Hq, s.Hkv, s.N,
-                                                                s.g, s.w, scale_log2, rows);
+                                                                s.g, s.w, s.window_mode, scale_log2, rows);
     } else {
         return cudaErrorNotSupported;
     }

@@ -82,6 +82,7 @@ static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 struct Params {
     int B, Hq, Hkv, N, g, w, n_pairs, n_items;
+    int window_mode;  // 1: raw window starts at the group boundary g * (lo(i) / g)
     float scale_log2;
     __nv_bfloat16 *O;
     float *LSE;
@@ -91,6 +92,11 @@ struct Params {
 };
 
 __device__ __forceinline__ int lo_of(int i, int w) { return i - w + 1 > 0 ? i - w + 1 : 0; }
+// first raw token of row i's window (cores stay j < lo(i)/g in both modes)
+__device__ __forceinline__ int win_of(const Params &p, int i) {
+    const int lo = lo_of(i, p.w);
+    return p.window_mode ? (lo / p.g) * p.g : lo;
+}
 
 // The tile sequence of one work item and which half uses which tile.  Per-half
 // fields are scalars chosen with selects (no runtime-indexed arrays, which
@@ -137,7 +143,7 @@ __device__ __forceinline__ Half make_half(const Params &p, int a, int lo0) {
     }
     const int nc = lo_of(x.b, p.w) / p.g;
     x.tc = (nc + BN - 1) / BN;
-    x.kl = (lo_of(a, p.w) - lo0) / BN;
+    x.kl = (win_of(p, a) - lo0) / BN;
     x.kh = (x.b - lo0) / BN + 1;
     return x;
 }
@@ -150,7 +156,7 @@ __device__ __forceinline__ Item make_item(const Params &p, int k) {
     const int b = it.bh / p.Hq, h = it.bh % p.Hq;
     it.kvz = b * p.Hkv + h / (p.Hq / p.Hkv);
     const int i0 = pair * 2 * BM;
-    it.lo0 = lo_of(i0, p.w);
+    it.lo0 = win_of(p, i0);
     it.hA = make_half(p, i0, it.lo0);
     it.hB = make_half(p, i0 + BM, it.lo0);
     const int last = it.hB.valid ? it.hB.b : it.hA.b;
@@ -367,10 +373,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const Half x = h ? it.hB : it.hA;
             if (!x.valid) continue;
             const int i = x.a + row;
-            const int lo_i = lo_of(i, p.w);
-            const int nc_i = lo_i / p.g;
+            const int lo_i = win_of(p, i);           // first raw token of this row's window
+            const int nc_i = lo_of(i, p.w) / p.g;    // cores visible to this row
             const int nc_first = lo_of(x.a, p.w) / p.g;
-            const int lo_last = lo_of(x.b, p.w);
+            const int lo_last = win_of(p, x.b);
             float m = -INFINITY;  // running max of the log2-scaled logits
             float l = 0.f;
             for (int t = half_first(x, it.Tc); t >= 0; t = half_next(x, it.Tc, t)) {
@@ -608,6 +614,7 @@ cudaError_t launch_attn_bf16_tc(const void *Q, const void *K, const void *V, con
     p.N = s.N;
     p.g = s.g;
     p.w = s.w;
+    p.window_mode = s.window_mode;
     p.n_pairs = (s.N + 2 * BM - 1) / (2 * BM);
     p.n_items = p.n_pairs * s.B * s.Hq;
     p.scale_log2 = s.scale * 1.4426950408889634f;

@@ -26,6 +26,8 @@ int check_shape(const cca_params_t *p, bool need_w) {
     if (p->Hq % p->Hkv != 0 || p->N % p->g != 0) return CCA_ERR_INVALID_ARG;
     if (p->dtype != CCA_BF16 && p->dtype != CCA_F32) return CCA_ERR_INVALID_ARG;
     if (!(p->scale == p->scale) || isinf(p->scale)) return CCA_ERR_INVALID_ARG;
+    if (p->window_mode < 0 || p->window_mode > 1 || p->pool_mode < 0 || p->pool_mode > 2)
+        return CCA_ERR_INVALID_ARG;
     // Element counts of the largest tensor must fit the kernels' 64-bit indexing and
     // row counts the 32-bit tensor-map coordinates.
     const double elems = static_cast<double>(p->B) * p->Hq * p->N * p->d;
@@ -44,6 +46,8 @@ cca::Shape to_shape(const cca_params_t *p) {
     s.g = p->g;
     s.w = p->w;
     s.scale = p->scale > 0.f ? p->scale : 1.0f / sqrtf(static_cast<float>(p->d));
+    s.window_mode = p->window_mode;
+    s.pool_mode = p->pool_mode;
     return s;
 }
 

@@ -232,11 +232,13 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const float *__restri
 }
 
 // One warp per (b, kv): pools group j with the supplied group-last queries q[B, Hq, D].
+// pool_max: element-wise maximum of the group's rows instead of the weighted sums
+// (mean pooling arrives as logit_scale = 0, i.e. equal weights).
 template <typename T, int D>
 __global__ void __launch_bounds__(128) pool_group_kernel(const T *__restrict__ q, const T *__restrict__ K,
                                                          const T *__restrict__ V, T *__restrict__ Kc,
                                                          T *__restrict__ Vc, int Hq, int Hkv, int Ncap, int g, int j,
-                                                         float logit_scale, int n_bk) {
+                                                         float logit_scale, int pool_max, int n_bk) {
     using VT = Vec<T>;
     constexpr int E = VT::E;
     constexpr int LPR = D / E;
@@ -257,14 +259,25 @@ __global__ void __launch_bounds__(128) pool_group_kernel(const T *__restrict__ q
     }
     const T *kg = K + (static_cast<int64_t>(bk) * Ncap + static_cast<int64_t>(j) * g) * D + cl * E;
     const T *vg = V + (static_cast<int64_t>(bk) * Ncap + static_cast<int64_t>(j) * g) * D + cl * E;
+    const float init = pool_max ? -INFINITY : 0.f;
     float m = -INFINITY, l = 0.f, ak[E], av[E];
 #pragma unroll
-    for (int e = 0; e < E; ++e) ak[e] = av[e] = 0.f;
+    for (int e = 0; e < E; ++e) ak[e] = av[e] = init;
     for (int t0 = 0; t0 < g; t0 += RPI) {
         const int t = t0 + sub;
         float kf[E], vf[E];
         VT::unpack(t < g ? ldg16(kg + static_cast<int64_t>(t) * D) : make_uint4(0, 0, 0, 0), kf);
         VT::unpack(t < g ? ldg16(vg + static_cast<int64_t>(t) * D) : make_uint4(0, 0, 0, 0), vf);
+        if (pool_max) {
+            if (t < g) {
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    ak[e] = fmaxf(ak[e], kf[e]);
+                    av[e] = fmaxf(av[e], vf[e]);
+                }
+            }
+            continue;
+        }
         float dot = 0.f;
 #pragma unroll
         for (int e = 0; e < E; ++e) dot = fmaf(qs[e], kf[e], dot);
@@ -284,26 +297,37 @@ __global__ void __launch_bounds__(128) pool_group_kernel(const T *__restrict__ q
             m = mn;
         }
     }
+    if (pool_max) {
 #pragma unroll
-    for (int off = LPR; off < 32; off <<= 1) {
-        const float mo = __shfl_xor_sync(kFull, m, off);
-        const float lo_ = __shfl_xor_sync(kFull, l, off);
-        const float mn = fmaxf(m, mo);
-        const float ca = (m == -INFINITY) ? 0.f : ptx::ex2(m - mn);
-        const float cb = (mo == -INFINITY) ? 0.f : ptx::ex2(mo - mn);
-        l = l * ca + lo_ * cb;
+        for (int off = LPR; off < 32; off <<= 1) {
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                ak[e] = fmaxf(ak[e], __shfl_xor_sync(kFull, ak[e], off));
+                av[e] = fmaxf(av[e], __shfl_xor_sync(kFull, av[e], off));
+            }
+        }
+    } else {
+#pragma unroll
+        for (int off = LPR; off < 32; off <<= 1) {
+            const float mo = __shfl_xor_sync(kFull, m, off);
+            const float lo_ = __shfl_xor_sync(kFull, l, off);
+            const float mn = fmaxf(m, mo);
+            const float ca = (m == -INFINITY) ? 0.f : ptx::ex2(m - mn);
+            const float cb = (mo == -INFINITY) ? 0.f : ptx::ex2(mo - mn);
+            l = l * ca + lo_ * cb;
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                ak[e] = ak[e] * ca + __shfl_xor_sync(kFull, ak[e], off) * cb;
+                av[e] = av[e] * ca + __shfl_xor_sync(kFull, av[e], off) * cb;
+            }
+            m = mn;
+        }
+        const float inv = 1.f / l;
 #pragma unroll
         for (int e = 0; e < E; ++e) {
-            ak[e] = ak[e] * ca + __shfl_xor_sync(kFull, ak[e], off) * cb;
-            av[e] = av[e] * ca + __shfl_xor_sync(kFull, av[e], off) * cb;
+            ak[e] *= inv;
+            av[e] *= inv;
         }
-        m = mn;
-    }
-    const float inv = 1.f / l;
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-        ak[e] *= inv;
-        av[e] *= inv;
     }
     if (sub == 0) {
         const int64_t orow = (static_cast<int64_t>(bk) * (Ncap / g) + j) * D + cl * E;
@@ -326,8 +350,9 @@ cudaError_t launch_decode_typed(const void *Q, const void *K, const void *V, con
     a.Ncap = s.N;
     a.g = s.g;
     a.pos = pos;
-    a.lo = pos - s.w + 1 > 0 ? pos - s.w + 1 : 0;
-    a.n_core = a.lo / s.g;
+    const int lo = pos - s.w + 1 > 0 ? pos - s.w + 1 : 0;
+    a.n_core = lo / s.g;
+    a.lo = s.window_mode ? a.n_core * s.g : lo;  // first raw token of the window
     a.L = a.n_core + (pos - a.lo + 1);
     a.splits = decode_splits(a.L);
     a.scale_log2 = s.scale * 1.4426950408889634f;
@@ -399,29 +424,30 @@ cudaError_t launch_pool_group(int dtype, const void *q, const void *K, const voi
                               const Shape &s, int j, cudaStream_t stream) {
     const int n_bk = s.B * s.Hkv;
     const unsigned blocks = static_cast<unsigned>((n_bk + 3) / 4);
-    const float ls = s.scale * 1.4426950408889634f / static_cast<float>(s.Hq / s.Hkv);
+    const float ls = s.pool_mode == 1 ? 0.f : s.scale * 1.4426950408889634f / static_cast<float>(s.Hq / s.Hkv);
+    const int pmax = s.pool_mode == 2 ? 1 : 0;
     if (dtype == 0) {
         if (s.d == 128)
             pool_group_kernel<__nv_bfloat16, 128><<<blocks, 128, 0, stream>>>(
                 static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(K),
                 static_cast<const __nv_bfloat16 *>(V), static_cast<__nv_bfloat16 *>(Kc),
-                static_cast<__nv_bfloat16 *>(Vc), s.Hq, s.Hkv, s.N, s.g, j, ls, n_bk);
+                static_cast<__nv_bfloat16 *>(Vc), s.Hq, s.Hkv, s.N, s.g, j, ls, pmax, n_bk);
         else if (s.d == 64)
             pool_group_kernel<__nv_bfloat16, 64><<<blocks, 128, 0, stream>>>(
                 static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(K),
                 static_cast<const __nv_bfloat16 *>(V), static_cast<__nv_bfloat16 *>(Kc),
-                static_cast<__nv_bfloat16 *>(Vc), s.Hq, s.Hkv, s.N, s.g, j, ls, n_bk);
+                static_cast<__nv_bfloat16 *>(Vc), s.Hq, s.Hkv, s.N, s.g, j, ls, pmax, n_bk);
         else
             return cudaErrorNotSupported;
     } else {
         if (s.d == 128)
             pool_group_kernel<float, 128><<<blocks, 128, 0, stream>>>(
                 static_cast<const float *>(q), static_cast<const float *>(K), static_cast<const float *>(V),
-                static_cast<float *>(Kc), static_cast<float *>(Vc), s.Hq, s.Hkv, s.N, s.g, j, ls, n_bk);
+                static_cast<float *>(Kc), static_cast<float *>(Vc), s.Hq, s.Hkv, s.N, s.g, j, ls, pmax, n_bk);
         else if (s.d == 64)
             pool_group_kernel<float, 64><<<blocks, 128, 0, stream>>>(
                 static_cast<const float *>(q), static_cast<const float *>(K), static_cast<const float *>(V),
-                static_cast<float *>(Kc), static_cast<float *>(Vc), s.Hq, s.Hkv, s.N, s.g, j, ls, n_bk);
+                static_cast<float *>(Kc), static_cast<float *>(Vc), s.Hq, s.Hkv, s.N, s.g, j, ls, pmax, n_bk);
         else
             return cudaErrorNotSupported;
     }

@@ -10,6 +10,8 @@ namespace cca {
 struct Shape {
     int B, Hq, Hkv, N, d, g, w;
     float scale;  // resolved softmax scale (> 0)
+    int window_mode = 0;  // 1: raw window starts at the group boundary g*(lo/g)
+    int pool_mode = 0;    // 0 softmax, 1 mean, 2 max
 };
 
 // Global-aware pooling. dtype: 0 = bf16, 1 = f32.  `status` (optional device

@@ -77,7 +77,8 @@ struct PoolArgs {
     int Hq, Hkv, N, g, r;
     int S;                 // ring stages per warp
     uint32_t stage_bytes;  // K chunk + V chunk + r query rows
-    float logit_scale;     // tau * log2(e) / r
+    float logit_scale;     // tau * log2(e) / r (0 for mean pooling: equal weights)
+    int pool_max;          // element-wise max pooling instead of weighted sums
     int64_t n_groups;      // B * Hkv * (N / g)
     int32_t *status;
 };
@@ -165,8 +166,12 @@ __global__ void __launch_bounds__(NW_MAX * 32) pool_kernel(const T *__restrict__
         const int rows = min(RS, a.g - t0);
         if (ch == 0) {
             // new group: sum of the r group-last queries (1/r is in logit_scale)
+            const float init = a.pool_max ? -INFINITY : 0.f;
 #pragma unroll
-            for (int e = 0; e < E; ++e) q[e] = ak[e] = av[e] = 0.f;
+            for (int e = 0; e < E; ++e) {
+                q[e] = 0.f;
+                ak[e] = av[e] = init;
+            }
             m = -INFINITY;
             l = 0.f;
             for (int hh = 0; hh < a.r; ++hh) {
@@ -189,6 +194,22 @@ __global__ void __launch_bounds__(NW_MAX * 32) pool_kernel(const T *__restrict__
                 kr[it] = vr[it] = make_uint4(0, 0, 0, 0);
             }
         }
+        if (a.pool_max) {
+            // element-wise maximum of the group's keys and of its values
+#pragma unroll
+            for (int it = 0; it < PASSES; ++it) {
+                if (it * RPI + sub < rows) {
+                    float fk[E], fv[E];
+                    VT::unpack(kr[it], fk);
+                    VT::unpack(vr[it], fv);
+#pragma unroll
+                    for (int e = 0; e < E; ++e) {
+                        ak[e] = fmaxf(ak[e], fk[e]);
+                        av[e] = fmaxf(av[e], fv[e]);
+                    }
+                }
+            }
+        } else {
 #pragma unroll
         for (int it = 0; it < PASSES; ++it) {
             float f[E];
@@ -227,6 +248,7 @@ __global__ void __launch_bounds__(NW_MAX * 32) pool_kernel(const T *__restrict__
             }
         }
         m = mn;
+        }
         // every lane has read the stage: refill it with chunk c + S
         ptx::fence_proxy_async_smem();
         __syncwarp();
@@ -240,13 +262,25 @@ __global__ void __launch_bounds__(NW_MAX * 32) pool_kernel(const T *__restrict__
                 kt[e] = ak[e];
                 vt[e] = av[e];
             }
+            if (a.pool_max) {
 #pragma unroll
-            for (int o = LPR; o < 32; o <<= 1) {
-                lt += __shfl_xor_sync(kFull, lt, o);
+                for (int o = LPR; o < 32; o <<= 1) {
 #pragma unroll
-                for (int e = 0; e < E; ++e) {
-                    kt[e] += __shfl_xor_sync(kFull, kt[e], o);
-                    vt[e] += __shfl_xor_sync(kFull, vt[e], o);
+                    for (int e = 0; e < E; ++e) {
+                        kt[e] = fmaxf(kt[e], __shfl_xor_sync(kFull, kt[e], o));
+                        vt[e] = fmaxf(vt[e], __shfl_xor_sync(kFull, vt[e], o));
+                    }
+                }
+                lt = 1.f;
+            } else {
+#pragma unroll
+                for (int o = LPR; o < 32; o <<= 1) {
+                    lt += __shfl_xor_sync(kFull, lt, o);
+#pragma unroll
+                    for (int e = 0; e < E; ++e) {
+                        kt[e] += __shfl_xor_sync(kFull, kt[e], o);
+                        vt[e] += __shfl_xor_sync(kFull, vt[e], o);
+                    }
                 }
             }
             const float inv = 1.f / lt;
@@ -315,7 +349,8 @@ cudaError_t launch_typed(const void *Q, const void *K, const void *V, void *Kc, 
     int nw = static_cast<int>(SMEM_BUDGET / (a.S * a.stage_bytes));
     if (nw > NW_MAX) nw = NW_MAX;
     if (nw < 1) return cudaErrorNotSupported;  // a stage would not fit (hundreds of query heads per KV head)
-    a.logit_scale = s.scale * 1.4426950408889634f / static_cast<float>(a.r);
+    a.logit_scale = s.pool_mode == 1 ? 0.f : s.scale * 1.4426950408889634f / static_cast<float>(a.r);
+    a.pool_max = s.pool_mode == 2 ? 1 : 0;
     a.n_groups = static_cast<int64_t>(s.B) * s.Hkv * (s.N / s.g);
     a.status = status;
     const uint32_t smem = nw * a.S * a.stage_bytes;

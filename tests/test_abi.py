@@ -38,7 +38,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_strings(lib):
-    assert lib.cca_abi_version() == 1
+    assert lib.cca_abi_version() == 2
     for code in (0, -1, -2, -3, -4, 7):
         assert isinstance(api.status_string(code), str) and api.status_string(code)
 
@@ -120,3 +120,10 @@ def test_pool_group_rejects_bad_group(lib):
     prm = api.make_params(1, 4, 4, 1024, 128, 16, 1, api.CCA_BF16)
     assert lib.cca_pool_group(*P[:5], -1, ctypes.byref(prm), None) == api.CCA_ERR_INVALID_ARG
     assert lib.cca_pool_group(*P[:5], 64, ctypes.byref(prm), None) == api.CCA_ERR_INVALID_ARG
+
+
+def test_rejects_unknown_modes(lib):
+    for kw in (dict(window_mode=2), dict(window_mode=-1), dict(pool_mode=3), dict(pool_mode=-1)):
+        prm = api.make_params(1, 2, 2, 256, 128, 16, 32, api.CCA_BF16, **kw)
+        assert lib.cca_attn_fwd(*P, ctypes.byref(prm), None) == api.CCA_ERR_INVALID_ARG
+        assert lib.cca_pool(*P[:5], ctypes.byref(prm), None) == api.CCA_ERR_INVALID_ARG

@@ -98,3 +98,28 @@ def test_incremental_decode_loop():
         rows = [(0, h, pos) for h in range(w.Hq)]
         Oe, Le = oracle.attn_rows(Q, K, V, Kr, Vr, w.g, w.w, rows)
         check_out(O.reshape(-1, w.d), LSE.reshape(-1), Oe, Le, Q.dtype, f"step {pos}")
+
+
+@pytest.mark.parametrize("pool_mode", [1, 2])
+def test_pool_group_variants(pool_mode):
+    w = wl(1, 4, 2, 512, 128, 16, 64)
+    Q, K, V = make_qkv(w, "cuda")
+    Kg = torch.zeros((w.B, w.Hkv, w.N // w.g, w.d), dtype=Q.dtype, device="cuda")
+    Vg = torch.zeros_like(Kg)
+    for j in range(w.N // w.g):
+        api.cca_pool_group(Q[:, :, (j + 1) * w.g - 1].contiguous(), K, V, Kg, Vg, j, w.g, pool_mode=pool_mode)
+    torch.cuda.synchronize()
+    Kr, Vr = oracle.pool(Q, K, V, w.g, pool_mode=pool_mode)
+    check_cores(Kg, Vg, Kr, Vr, Q.dtype, f"pool_group mode {pool_mode}")
+
+
+def test_decode_group_aligned_window():
+    w = wl(1, 4, 2, 2048, 128, 16, 300)
+    Q, K, V = make_qkv(w, "cuda")
+    Kc, Vc = api.cca_pool(Q, K, V, w.g)
+    for pos in (5, 299, 300, 316, 1000, 2047):
+        O, LSE = api.cca_decode_fwd(Q[:, :, pos].contiguous(), K, V, Kc, Vc, pos, w.g, w.w, window_mode=1)
+        torch.cuda.synchronize()
+        rows = [(0, h, pos) for h in range(w.Hq)]
+        Oa, La = oracle.attn_rows(Q, K, V, Kc, Vc, w.g, w.w, rows, window_mode=1)
+        check_out(O.reshape(-1, w.d), LSE.reshape(-1), Oa, La, Q.dtype, f"aligned window pos {pos}")

@@ -127,3 +127,23 @@ def test_causal_attention_comparator():
     torch.cuda.synchronize()
     Or, Lr, _, _ = oracle.prefill(Q, K, V, 1, w.N)
     check_out(O, LSE, Or, Lr, Q.dtype, "causal comparator")
+
+
+VARIANT_CASES = [
+    (wl(1, 4, 2, 1024, 128, 16, 200), 1, 0), (wl(1, 4, 2, 1024, 128, 16, 200), 2, 0),
+    (wl(1, 4, 2, 1024, 128, 16, 200), 0, 1), (wl(2, 2, 2, 1536, 128, 8, 333), 2, 1),
+    (wl(1, 2, 2, 512, 64, 16, 70, "f32"), 1, 1), (wl(1, 2, 1, 512, 128, 8, 100, "f32"), 2, 0),
+    (wl(1, 2, 2, 384, 128, 1, 64), 0, 1),
+]
+
+
+@pytest.mark.parametrize("w,pool_mode,window_mode", VARIANT_CASES,
+                         ids=lambda x: x.name if hasattr(x, "name") else str(x))
+def test_variants_parity(w, pool_mode, window_mode):
+    """Mean / max pooling and the group-aligned window (the pages' ablations)."""
+    Q, K, V = make_qkv(w, "cuda")
+    O, LSE, Kc, Vc = api.cca_prefill(Q, K, V, w.g, w.w, pool_mode=pool_mode, window_mode=window_mode)
+    torch.cuda.synchronize()
+    Or, Lr, Kr, Vr = oracle.prefill(Q, K, V, w.g, w.w, pool_mode=pool_mode, window_mode=window_mode)
+    check_cores(Kc, Vc, Kr, Vr, Q.dtype, f"{w.name} pool {pool_mode}")
+    check_out(O, LSE, Or, Lr, Q.dtype, f"{w.name} pool {pool_mode} window {window_mode}")
