@@ -299,3 +299,48 @@ ALL_PINS = [pin_worked_example, pin_gqa_worked_example, pin_visibility_counts, p
             pin_pool_zero_query_mean, pin_pool_dominant_query_selects, pin_unit_values,
             pin_constant_keys_lse, pin_causality, pin_dense_mask_formulation,
             pin_group_aligned_window_counts, pin_group_aligned_window_no_gap, pin_mean_pooling, pin_max_pooling]
+
+
+def _fd_check(Q, K, V, g, w, pool_mode, window_mode, lib, n_probe=6, seed=0, eps=1e-6):
+    """Central finite differences of sum(G * O) through the C oracle's forward, against
+    the backward oracle's gradient, at a few random coordinates of Q, K and V."""
+    from oracle.backward import prefill_grads
+    rng = np.random.default_rng(seed)
+    G = rng.standard_normal(Q.shape)
+    dQ, dK, dV = prefill_grads(Q, K, V, G, g, w, pool_mode=pool_mode, window_mode=window_mode)
+    for X, dX in ((Q, dQ), (K, dK), (V, dV)):
+        for _ in range(n_probe):
+            idx = tuple(rng.integers(0, s) for s in X.shape)
+            Xp, Xm = X.copy(), X.copy()
+            Xp[idx] += eps
+            Xm[idx] -= eps
+            args_p = [Xp if X is T else T for T in (Q, K, V)]
+            args_m = [Xm if X is T else T for T in (Q, K, V)]
+            Op = oracle.prefill(*args_p, g, w, lib=lib, pool_mode=pool_mode, window_mode=window_mode)[0]
+            Om = oracle.prefill(*args_m, g, w, lib=lib, pool_mode=pool_mode, window_mode=window_mode)[0]
+            fd = ((Op - Om) * G).sum() / (2 * eps)
+            assert abs(fd - dX[idx]) <= 1e-6 * max(1.0, abs(fd)), (idx, fd, dX[idx])
+
+
+def pin_backward_finite_differences(lib):
+    B, Hq, Hkv, N, d = 1, 4, 2, 24, 8
+    Q, K, V = _rand((B, Hq, N, d), 60), _rand((B, Hkv, N, d), 61), _rand((B, Hkv, N, d), 62)
+    for g, w, pm, wm, seed in ((4, 5, 0, 0, 1), (3, 7, 0, 1, 2), (4, 6, 1, 0, 3), (2, 3, 2, 0, 4)):
+        _fd_check(Q, K, V, g, w, pm, wm, lib, seed=seed)
+
+
+def pin_backward_g1_is_causal(lib):
+    # g = 1: the forward is causal attention, so are its gradients (torch SDPA autograd).
+    from oracle.backward import prefill_grads
+    B, H, N, d = 1, 2, 20, 8
+    Q, K, V = _rand((B, H, N, d), 63), _rand((B, H, N, d), 64), _rand((B, H, N, d), 65)
+    G = _rand((B, H, N, d), 66)
+    dQ, dK, dV = prefill_grads(Q, K, V, G, 1, 5)
+    q, k, v = (torch.tensor(t, requires_grad=True) for t in (Q, K, V))
+    o = torch.nn.functional.scaled_dot_product_attention(q, k, v, is_causal=True)
+    o.backward(torch.tensor(G))
+    for a, b in ((dQ, q.grad), (dK, k.grad), (dV, v.grad)):
+        np.testing.assert_allclose(a, b.numpy(), rtol=0, atol=1e-12)
+
+
+BACKWARD_PINS = [pin_backward_finite_differences, pin_backward_g1_is_causal]

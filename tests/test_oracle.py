@@ -75,3 +75,22 @@ def test_pins_catch_mutant(name, mutant_dir):
         except AssertionError:
             caught.append(pin.__name__)
     assert caught, f"no pin caught mutant {name}"
+
+
+@pytest.mark.parametrize("pin", oracle_pins.BACKWARD_PINS, ids=lambda f: f.__name__)
+def test_backward_pin(pin):
+    pin(oracle.load())
+
+
+def test_backward_forward_matches_c_oracle():
+    """The differentiable dense forward of the backward oracle equals the C oracle."""
+    import numpy as np
+    import torch
+    from oracle.backward import dense_forward
+    rng = np.random.default_rng(70)
+    Q, K, V = (rng.standard_normal(s) for s in ((2, 4, 32, 8), (2, 2, 32, 8), (2, 2, 32, 8)))
+    for g, w, pm, wm in ((4, 5, 0, 0), (8, 9, 1, 1), (2, 3, 2, 0)):
+        O, L = dense_forward(torch.tensor(Q), torch.tensor(K), torch.tensor(V), g, w, pool_mode=pm, window_mode=wm)
+        Or, Lr, _, _ = oracle.prefill(Q, K, V, g, w, pool_mode=pm, window_mode=wm)
+        np.testing.assert_allclose(O.numpy(), Or, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(L.numpy(), Lr, rtol=0, atol=1e-12)
