@@ -270,6 +270,9 @@ def run_cca(args, rank, world, local):
         out["decode"] = decode_bench(wl, dev, stream, 50, peaks)
         if args.also_128k and wl is not W.MHA_128K:
             out["decode_128k"] = decode_bench(W.MHA_128K, dev, stream, 50, peaks)
+    if args.backward:
+        out["backward"] = backward_bench(wl, dev, stream, 2, peaks)
+        out["gpu_launches"] += 4 * 2
     if args.comparator:
         out["full_attention_comparator"] = comparator(wl, dev, stream, max(3, args.steps // 4), ms_per_step)
         out["gpu_launches"] += max(3, args.steps // 4)
@@ -315,6 +318,33 @@ def decode_bench(wl, dev, stream, iters, peaks):
             "us_per_step": us, "tokens_per_s": wl.B / (us * 1e-6),
             "gbs": nbytes / (us * 1e-6) / 1e9, "hbm_frac": nbytes / (us * 1e-6) / 1e9 / peaks["hbm_gbs"],
             "algorithmic_bytes": nbytes, "kernel_launches_per_step": 2}
+
+
+def backward_bench(wl, dev, stream, iters, peaks):
+    """Backward pass (dQ, dK, dV of sum(dO * O)) of the whole prefill step."""
+    from sparse_long_context_cca_gb300 import api
+    from sparse_long_context_cca_gb300.inputs import make_qkv
+    Q, K, V = make_qkv(wl, dev)
+    O, LSE, Kc, Vc = api.cca_prefill(Q, K, V, wl.g, wl.w, stream=stream)
+    dO = torch.randn(Q.shape, device=dev, generator=torch.Generator(device=dev).manual_seed(5)).to(Q.dtype)
+    grads = api.cca_prefill_bwd(Q, K, V, Kc, Vc, O, LSE, dO, wl.g, wl.w, stream=stream)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(iters):
+        api.cca_prefill_bwd(Q, K, V, Kc, Vc, O, LSE, dO, wl.g, wl.w, dQ=grads[0], dK=grads[1], dV=grads[2],
+                            stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / iters
+    flops = 2.5 * W.attn_flops(wl)
+    del Q, K, V, O, LSE, Kc, Vc, dO, grads
+    torch.cuda.empty_cache()
+    return {"what": "backward of pooling + fused attention (fp32 CUDA-core kernels)", "ms": ms,
+            "eff_tflops": flops / (ms / 1e3) / 1e12,
+            "algorithmic_unit": "10*d FLOP per (query, visible key, head): q.k, dO.v, dQ, dK, dV",
+            "kernel_launches": 4}
 
 
 def comparator(wl, dev, stream, steps, cca_ms_per_step):
@@ -453,6 +483,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-comparator", dest="comparator", action="store_false")
     ap.add_argument("--no-decode", dest="decode", action="store_false")
+    ap.add_argument("--no-backward", dest="backward", action="store_false")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -184,6 +184,30 @@ int cca_decode_fwd_noalloc(const void *Q, const void *K, const void *V, const vo
 int cca_pool_group(const void *q, const void *K, const void *V, void *Kc, void *Vc, int j,
                    const cca_params_t *params, void *stream);
 
+/*
+ * cca_prefill_bwd - backward pass of CCA prefill (pooling + fused attention):
+ * gradients of the loss sum(dO * O) with respect to Q, K and V.  The pages
+ * fine-tune CCA models ("differentiable fusion", digest page; fine-tuning
+ * settings, OpenReview rebuttal); this is the gradient of the two equations.
+ *   Q, K, V, Kc, Vc  the forward's inputs and core tokens (dtype of params)
+ *   O, LSE           the forward's outputs (cca_attn_fwd)
+ *   dO               [B, Hq, N, d] upstream gradient (dtype of params)
+ *   dQ               [B, Hq, N, d]  fp32, overwritten
+ *   dK, dV           [B, Hkv, N, d] fp32, overwritten (they include the paths
+ *                    through the core tokens back into the pooled groups)
+ *   workspace        caller-owned device buffer of at least
+ *                    cca_prefill_bwd_workspace_size(params) bytes
+ * All pooling and window modes are supported, d in {64, 128}, bf16 or f32.
+ * Max pooling passes each element's gradient to the first row holding the
+ * maximum.  The kernels run on CUDA cores in fp32 (not yet tensor cores).
+ */
+int cca_prefill_bwd(const void *Q, const void *K, const void *V, const void *Kc, const void *Vc,
+                    const void *O, const float *LSE, const void *dO, float *dQ, float *dK, float *dV,
+                    const cca_params_t *params, void *workspace, uint64_t workspace_bytes, void *stream);
+
+/* Bytes of workspace cca_prefill_bwd needs (0 on bad params). */
+uint64_t cca_prefill_bwd_workspace_size(const cca_params_t *params);
+
 /* Static English text for a status code (never NULL). */
 const char *cca_status_string(int status);
 

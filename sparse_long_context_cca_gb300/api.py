@@ -46,7 +46,7 @@ _lib = None
 _lock = threading.Lock()
 
 EXPORTED = ["cca_pool", "cca_attn_fwd", "cca_decode_fwd", "cca_decode_workspace_size", "cca_pool_group",
-            "cca_decode_fwd_noalloc",
+            "cca_decode_fwd_noalloc", "cca_prefill_bwd", "cca_prefill_bwd_workspace_size",
             "cca_status_string", "cca_abi_version", "cca_test_set_wait_limit_ns", "cca_test_skip_q_load"]
 
 
@@ -75,6 +75,10 @@ def load_library():
         lib.cca_decode_fwd.restype = ctypes.c_int
         lib.cca_decode_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, ctypes.c_int, pp, vp]
         lib.cca_decode_fwd_noalloc.restype = ctypes.c_int
+        lib.cca_prefill_bwd.argtypes = [vp] * 11 + [pp, vp, ctypes.c_uint64, vp]
+        lib.cca_prefill_bwd.restype = ctypes.c_int
+        lib.cca_prefill_bwd_workspace_size.argtypes = [pp]
+        lib.cca_prefill_bwd_workspace_size.restype = ctypes.c_uint64
         lib.cca_decode_workspace_size.argtypes = [pp]
         lib.cca_decode_workspace_size.restype = ctypes.c_uint64
         lib.cca_pool_group.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, pp, vp]
@@ -265,3 +269,33 @@ def cca_pool_group(q, K, V, Kc, Vc, j: int, g: int, scale: float = 0.0, stream=N
     if st != CCA_OK:
         raise CcaError(st, "cca_pool_group")
     return Kc, Vc
+
+
+def cca_prefill_bwd(Q, K, V, Kc, Vc, O, LSE, dO, g: int, w: int, scale: float = 0.0, pool_mode: int = 0,
+                    window_mode: int = 0, dQ=None, dK=None, dV=None, workspace=None, stream=None):
+    """Gradients (dQ, dK, dV), fp32, of sum(dO * O) for CCA prefill (pooling + attention)."""
+    lib = load_library()
+    B, Hq, Hkv, N, d = _dims(Q, K)
+    G = N // g if g > 0 else 0
+    for name, t, shape in (("Q", Q, (B, Hq, N, d)), ("K", K, (B, Hkv, N, d)), ("V", V, (B, Hkv, N, d)),
+                           ("Kc", Kc, (B, Hkv, G, d)), ("Vc", Vc, (B, Hkv, G, d)), ("O", O, (B, Hq, N, d)),
+                           ("dO", dO, (B, Hq, N, d))):
+        _check(t, name, Q.dtype, shape)
+    _check(LSE, "LSE", torch.float32, (B, Hq, N))
+    dQ = torch.empty((B, Hq, N, d), dtype=torch.float32, device=Q.device) if dQ is None else dQ
+    dK = torch.empty((B, Hkv, N, d), dtype=torch.float32, device=Q.device) if dK is None else dK
+    dV = torch.empty((B, Hkv, N, d), dtype=torch.float32, device=Q.device) if dV is None else dV
+    _check(dQ, "dQ", torch.float32, (B, Hq, N, d))
+    _check(dK, "dK", torch.float32, (B, Hkv, N, d))
+    _check(dV, "dV", torch.float32, (B, Hkv, N, d))
+    prm = make_params(B, Hq, Hkv, N, d, g, w, _DTYPE[Q.dtype], scale, window_mode=window_mode, pool_mode=pool_mode)
+    need = int(lib.cca_prefill_bwd_workspace_size(ctypes.byref(prm)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=Q.device)
+    nbytes = workspace.numel() * workspace.element_size()
+    st = lib.cca_prefill_bwd(Q.data_ptr(), K.data_ptr(), V.data_ptr(), Kc.data_ptr(), Vc.data_ptr(), O.data_ptr(),
+                             LSE.data_ptr(), dO.data_ptr(), dQ.data_ptr(), dK.data_ptr(), dV.data_ptr(),
+                             ctypes.byref(prm), workspace.data_ptr(), nbytes, _stream_handle(stream))
+    if st != CCA_OK:
+        raise CcaError(st, "cca_prefill_bwd")
+    return dQ, dK, dV

@@ -1,0 +1,349 @@
+// Backward pass of CCA prefill: gradients of the loss sum(dO * O) with respect
+// to Q, K and V, through the fused attention (fusion equation) and through the
+// global-aware pooling (pooling equation) of "Core Context Aware Transformers
+// for Long Context Language Modeling", Method section.
+//
+// With P = softmax over the visible set, D_i = dO_i . O_i and
+// dS_ix = P_ix (dO_i . v_x - D_i) for every visible key x (core or raw token):
+//   dQ_i  = tau * sum_x dS_ix k_x
+//   dK_m  = tau * sum_i dS_im q_i,   dV_m  = sum_i P_im dO_i      (raw tokens)
+//   dKc_j = tau * sum_i dS_ij q_i,   dVc_j = sum_i P_ij dO_i      (cores)
+// and through Kc_j = sum_t a_t k_t, Vc_j = sum_t a_t v_t, a = softmax(s),
+// s_t = (tau / r) qsum . k_t with qsum the sum of the r group-last queries:
+//   da_t = dKc_j . k_t + dVc_j . v_t,   ds_t = a_t (da_t - sum_u a_u da_u)
+//   dk_t += a_t dKc_j + (tau / r) ds_t qsum,   dv_t += a_t dVc_j
+//   dq^h_last += (tau / r) sum_t ds_t k_t      for each of the r heads.
+// Mean pooling has a_t = 1/g and no score gradient; max pooling passes each
+// element's gradient to the row that holds the maximum.
+//
+// Four passes on CUDA cores in fp32 (one warp per row; lane l holds d/32
+// consecutive elements): per query row (dQ, D), per raw token (dK, dV), per
+// core (dKc, dVc into the workspace), per group (pooling backward, added into
+// dK, dV and the group-last rows of dQ).  P is recomputed from the forward's LSE.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "internal.h"
+
+namespace cca {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr float LOG2E = 1.4426950408889634f;
+
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T, int PL>
+__device__ __forceinline__ void load_row(const T *__restrict__ row, int lane, float (&f)[PL]) {
+#pragma unroll
+    for (int e = 0; e < PL; ++e) f[e] = to_f(row[lane * PL + e]);
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(kFull, x, o);
+    return x;
+}
+
+template <int PL>
+__device__ __forceinline__ float dot(const float (&a)[PL], const float (&b)[PL]) {
+    float s = 0.f;
+#pragma unroll
+    for (int e = 0; e < PL; ++e) s = fmaf(a[e], b[e], s);
+    return warp_sum(s);
+}
+
+struct BwdArgs {
+    int B, Hq, Hkv, N, g, w, window_mode, pool_mode;
+    float tau;
+};
+
+__device__ __forceinline__ int lo_of(int i, int w) { return i - w + 1 > 0 ? i - w + 1 : 0; }
+__device__ __forceinline__ int win_of(const BwdArgs &a, int i) {
+    const int lo = lo_of(i, a.w);
+    return a.window_mode ? (lo / a.g) * a.g : lo;
+}
+
+// Pass 1: one warp per query row -> dQ (fp32, before the pooling term) and D.
+template <typename T, int D>
+__global__ void __launch_bounds__(128) bwd_dq_kernel(const T *__restrict__ Q, const T *__restrict__ K,
+                                                     const T *__restrict__ V, const T *__restrict__ Kc,
+                                                     const T *__restrict__ Vc, const T *__restrict__ O,
+                                                     const float *__restrict__ LSE, const T *__restrict__ dO,
+                                                     float *__restrict__ dQ, float *__restrict__ Dbuf,
+                                                     const BwdArgs a) {
+    constexpr int PL = D / 32;
+    const int lane = threadIdx.x & 31;
+    const int64_t u = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (u >= static_cast<int64_t>(a.B) * a.Hq * a.N) return;
+    const int i = static_cast<int>(u % a.N);
+    const int64_t bh = u / a.N;
+    const int64_t bk = (bh / a.Hq) * a.Hkv + (bh % a.Hq) / (a.Hq / a.Hkv);
+    const int64_t G = a.N / a.g;
+    float q[PL], g_o[PL], o[PL], dq[PL];
+    load_row<T, PL>(Q + u * D, lane, q);
+    load_row<T, PL>(dO + u * D, lane, g_o);
+    load_row<T, PL>(O + u * D, lane, o);
+#pragma unroll
+    for (int e = 0; e < PL; ++e) dq[e] = 0.f;
+    const float Di = dot<PL>(g_o, o);
+    const float lse2 = LSE[u] * LOG2E, tau2 = a.tau * LOG2E;
+    auto visit = [&](const T *kr, const T *vr) {
+        float k[PL], v[PL];
+        load_row<T, PL>(kr, lane, k);
+        load_row<T, PL>(vr, lane, v);
+        const float P = exp2f(dot<PL>(q, k) * tau2 - lse2);
+        const float dS = P * (dot<PL>(g_o, v) - Di);
+#pragma unroll
+        for (int e = 0; e < PL; ++e) dq[e] = fmaf(a.tau * dS, k[e], dq[e]);
+    };
+    const int nc = lo_of(i, a.w) / a.g;
+    for (int j = 0; j < nc; ++j) visit(Kc + (bk * G + j) * D, Vc + (bk * G + j) * D);
+    for (int m = win_of(a, i); m <= i; ++m) visit(K + (bk * a.N + m) * D, V + (bk * a.N + m) * D);
+#pragma unroll
+    for (int e = 0; e < PL; ++e) dQ[u * D + lane * PL + e] = dq[e];
+    if (lane == 0) Dbuf[u] = Di;
+}
+
+// Passes 2 and 3: one warp per key row (raw token or core) -> its dK, dV, summed over
+// the query rows [i0, i1] of every query head that reads this KV head.
+template <typename T, int D>
+__device__ __forceinline__ void key_grad(const T *__restrict__ Q, const T *__restrict__ dO,
+                                         const float *__restrict__ LSE, const float *__restrict__ Dbuf,
+                                         const float (&k)[D / 32], const float (&v)[D / 32], int64_t b, int64_t kv,
+                                         int i0, int i1, const BwdArgs &a, int lane, float (&dk)[D / 32],
+                                         float (&dv)[D / 32]) {
+    constexpr int PL = D / 32;
+    const int r = a.Hq / a.Hkv;
+    const float tau2 = a.tau * LOG2E;
+    for (int hh = 0; hh < r; ++hh) {
+        const int64_t bh = b * a.Hq + kv * r + hh;
+        for (int i = i0; i <= i1; ++i) {
+            const int64_t u = bh * a.N + i;
+            float q[PL], g_o[PL];
+            load_row<T, PL>(Q + u * D, lane, q);
+            load_row<T, PL>(dO + u * D, lane, g_o);
+            const float P = exp2f(dot<PL>(q, k) * tau2 - LSE[u] * LOG2E);
+            const float dS = P * (dot<PL>(g_o, v) - Dbuf[u]);
+#pragma unroll
+            for (int e = 0; e < PL; ++e) {
+                dk[e] = fmaf(a.tau * dS, q[e], dk[e]);
+                dv[e] = fmaf(P, g_o[e], dv[e]);
+            }
+        }
+    }
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(128) bwd_dkv_raw_kernel(const T *__restrict__ Q, const T *__restrict__ K,
+                                                          const T *__restrict__ V, const float *__restrict__ LSE,
+                                                          const T *__restrict__ dO, const float *__restrict__ Dbuf,
+                                                          float *__restrict__ dK, float *__restrict__ dV,
+                                                          const BwdArgs a) {
+    constexpr int PL = D / 32;
+    const int lane = threadIdx.x & 31;
+    const int64_t u = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (u >= static_cast<int64_t>(a.B) * a.Hkv * a.N) return;
+    const int m = static_cast<int>(u % a.N);
+    const int64_t bk = u / a.N;
+    float k[PL], v[PL], dk[PL], dv[PL];
+    load_row<T, PL>(K + u * D, lane, k);
+    load_row<T, PL>(V + u * D, lane, v);
+#pragma unroll
+    for (int e = 0; e < PL; ++e) dk[e] = dv[e] = 0.f;
+    // rows whose window [win(i), i] holds m: i in [m, i_max], win() being non-decreasing
+    const int64_t i_last = a.window_mode ? static_cast<int64_t>(m / a.g + 1) * a.g + a.w - 2
+                                         : static_cast<int64_t>(m) + a.w - 1;
+    const int i1 = static_cast<int>(i_last < a.N - 1 ? i_last : a.N - 1);
+    key_grad<T, D>(Q, dO, LSE, Dbuf, k, v, bk / a.Hkv, bk % a.Hkv, m, i1, a, lane, dk, dv);
+#pragma unroll
+    for (int e = 0; e < PL; ++e) {
+        dK[u * D + lane * PL + e] = dk[e];
+        dV[u * D + lane * PL + e] = dv[e];
+    }
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(128) bwd_dkv_core_kernel(const T *__restrict__ Q, const T *__restrict__ Kc,
+                                                           const T *__restrict__ Vc, const float *__restrict__ LSE,
+                                                           const T *__restrict__ dO, const float *__restrict__ Dbuf,
+                                                           float *__restrict__ dKc, float *__restrict__ dVc,
+                                                           const BwdArgs a) {
+    constexpr int PL = D / 32;
+    const int lane = threadIdx.x & 31;
+    const int G = a.N / a.g;
+    const int64_t u = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (u >= static_cast<int64_t>(a.B) * a.Hkv * G) return;
+    const int j = static_cast<int>(u % G);
+    const int64_t bk = u / G;
+    float k[PL], v[PL], dk[PL], dv[PL];
+    load_row<T, PL>(Kc + u * D, lane, k);
+    load_row<T, PL>(Vc + u * D, lane, v);
+#pragma unroll
+    for (int e = 0; e < PL; ++e) dk[e] = dv[e] = 0.f;
+    // core j is visible to row i iff (j+1)*g <= lo(i), i.e. i >= (j+1)*g + w - 1
+    const int64_t i0 = static_cast<int64_t>(j + 1) * a.g + a.w - 1;
+    if (i0 < a.N) key_grad<T, D>(Q, dO, LSE, Dbuf, k, v, bk / a.Hkv, bk % a.Hkv, static_cast<int>(i0), a.N - 1, a, lane, dk, dv);
+#pragma unroll
+    for (int e = 0; e < PL; ++e) {
+        dKc[u * D + lane * PL + e] = dk[e];
+        dVc[u * D + lane * PL + e] = dv[e];
+    }
+}
+
+// Pass 4: one warp per group -> the pooling backward, added into dK, dV and dQ.
+template <typename T, int D>
+__global__ void __launch_bounds__(128) bwd_pool_kernel(const T *__restrict__ Q, const T *__restrict__ K,
+                                                       const T *__restrict__ V, const float *__restrict__ dKc,
+                                                       const float *__restrict__ dVc, float *__restrict__ dQ,
+                                                       float *__restrict__ dK, float *__restrict__ dV, const BwdArgs a) {
+    constexpr int PL = D / 32;
+    const int lane = threadIdx.x & 31;
+    const int G = a.N / a.g;
+    const int64_t u = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (u >= static_cast<int64_t>(a.B) * a.Hkv * G) return;
+    const int j = static_cast<int>(u % G);
+    const int64_t bk = u / G;
+    const int64_t b = bk / a.Hkv, kv = bk % a.Hkv;
+    const int r = a.Hq / a.Hkv, g = a.g;
+    float dkc[PL], dvc[PL];
+#pragma unroll
+    for (int e = 0; e < PL; ++e) {
+        dkc[e] = dKc[u * D + lane * PL + e];
+        dvc[e] = dVc[u * D + lane * PL + e];
+    }
+    const int64_t row0 = bk * a.N + static_cast<int64_t>(j) * g;  // first token of the group
+    if (a.pool_mode == 1) {
+        // mean pooling: every token weighs 1/g
+        for (int t = 0; t < g; ++t)
+#pragma unroll
+            for (int e = 0; e < PL; ++e) {
+                dK[(row0 + t) * D + lane * PL + e] += dkc[e] / g;
+                dV[(row0 + t) * D + lane * PL + e] += dvc[e] / g;
+            }
+        return;
+    }
+    if (a.pool_mode == 2) {
+        // max pooling: each element's gradient goes to the first row holding the maximum
+        float km[PL], vm[PL];
+        int kt[PL], vt[PL];
+        for (int t = 0; t < g; ++t) {
+            float k[PL], v[PL];
+            load_row<T, PL>(K + (row0 + t) * D, lane, k);
+            load_row<T, PL>(V + (row0 + t) * D, lane, v);
+#pragma unroll
+            for (int e = 0; e < PL; ++e) {
+                if (t == 0 || k[e] > km[e]) { km[e] = k[e]; kt[e] = t; }
+                if (t == 0 || v[e] > vm[e]) { vm[e] = v[e]; vt[e] = t; }
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < PL; ++e) {
+            dK[(row0 + kt[e]) * D + lane * PL + e] += dkc[e];
+            dV[(row0 + vt[e]) * D + lane * PL + e] += dvc[e];
+        }
+        return;
+    }
+    // softmax pooling scored by the sum of the r group-last queries (1/r folded into c)
+    const float c = a.tau / r;
+    const int last = (j + 1) * g - 1;
+    float qs[PL];
+#pragma unroll
+    for (int e = 0; e < PL; ++e) qs[e] = 0.f;
+    for (int hh = 0; hh < r; ++hh) {
+        float f[PL];
+        load_row<T, PL>(Q + ((b * a.Hq + kv * r + hh) * a.N + last) * D, lane, f);
+#pragma unroll
+        for (int e = 0; e < PL; ++e) qs[e] += f[e];
+    }
+    // pass A: softmax normaliser of the group scores
+    float mx = -INFINITY, den = 0.f;
+    for (int t = 0; t < g; ++t) {
+        float k[PL];
+        load_row<T, PL>(K + (row0 + t) * D, lane, k);
+        const float s = c * dot<PL>(qs, k);
+        const float mn = fmaxf(mx, s);
+        den = den * expf(mx - mn) + expf(s - mn);
+        mx = mn;
+    }
+    // pass B: sum_u a_u da_u
+    float sad = 0.f;
+    for (int t = 0; t < g; ++t) {
+        float k[PL], v[PL];
+        load_row<T, PL>(K + (row0 + t) * D, lane, k);
+        load_row<T, PL>(V + (row0 + t) * D, lane, v);
+        const float at = expf(c * dot<PL>(qs, k) - mx) / den;
+        sad += at * (dot<PL>(dkc, k) + dot<PL>(dvc, v));
+    }
+    // pass C: per-token gradients and the query-side term
+    float dqs[PL];
+#pragma unroll
+    for (int e = 0; e < PL; ++e) dqs[e] = 0.f;
+    for (int t = 0; t < g; ++t) {
+        float k[PL], v[PL];
+        load_row<T, PL>(K + (row0 + t) * D, lane, k);
+        load_row<T, PL>(V + (row0 + t) * D, lane, v);
+        const float at = expf(c * dot<PL>(qs, k) - mx) / den;
+        const float ds = at * (dot<PL>(dkc, k) + dot<PL>(dvc, v) - sad);
+#pragma unroll
+        for (int e = 0; e < PL; ++e) {
+            dK[(row0 + t) * D + lane * PL + e] += at * dkc[e] + c * ds * qs[e];
+            dV[(row0 + t) * D + lane * PL + e] += at * dvc[e];
+            dqs[e] = fmaf(c * ds, k[e], dqs[e]);
+        }
+    }
+    for (int hh = 0; hh < r; ++hh) {
+        float *dst = dQ + ((b * a.Hq + kv * r + hh) * a.N + last) * D + lane * PL;
+#pragma unroll
+        for (int e = 0; e < PL; ++e) dst[e] += dqs[e];
+    }
+}
+
+template <typename T, int D>
+cudaError_t run(const void *Q, const void *K, const void *V, const void *Kc, const void *Vc, const void *O,
+                const float *LSE, const void *dO, float *dQ, float *dK, float *dV, const Shape &s, float *ws,
+                cudaStream_t stream) {
+    BwdArgs a{s.B, s.Hq, s.Hkv, s.N, s.g, s.w, s.window_mode, s.pool_mode, s.scale};
+    const int64_t G = s.N / s.g;
+    float *Dbuf = ws;
+    float *dKc = Dbuf + ((static_cast<int64_t>(s.B) * s.Hq * s.N + 63) / 64) * 64;
+    float *dVc = dKc + static_cast<int64_t>(s.B) * s.Hkv * G * D;
+    auto blocks = [](int64_t rows) { return static_cast<unsigned>((rows + 3) / 4); };
+    const T *q = static_cast<const T *>(Q), *k = static_cast<const T *>(K), *v = static_cast<const T *>(V);
+    const T *kc = static_cast<const T *>(Kc), *vc = static_cast<const T *>(Vc);
+    const T *o = static_cast<const T *>(O), *dout = static_cast<const T *>(dO);
+    bwd_dq_kernel<T, D><<<blocks(static_cast<int64_t>(s.B) * s.Hq * s.N), 128, 0, stream>>>(q, k, v, kc, vc, o, LSE,
+                                                                                             dout, dQ, Dbuf, a);
+    bwd_dkv_raw_kernel<T, D><<<blocks(static_cast<int64_t>(s.B) * s.Hkv * s.N), 128, 0, stream>>>(q, k, v, LSE, dout,
+                                                                                                   Dbuf, dK, dV, a);
+    bwd_dkv_core_kernel<T, D><<<blocks(static_cast<int64_t>(s.B) * s.Hkv * G), 128, 0, stream>>>(q, kc, vc, LSE, dout,
+                                                                                                 Dbuf, dKc, dVc, a);
+    bwd_pool_kernel<T, D><<<blocks(static_cast<int64_t>(s.B) * s.Hkv * G), 128, 0, stream>>>(q, k, v, dKc, dVc, dQ, dK,
+                                                                                             dV, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+uint64_t prefill_bwd_workspace_bytes(const Shape &s) {
+    const uint64_t rows = ((static_cast<uint64_t>(s.B) * s.Hq * s.N + 63) / 64) * 64;
+    return 4ull * (rows + 2ull * s.B * s.Hkv * (s.N / s.g) * s.d);
+}
+
+cudaError_t launch_prefill_bwd(int dtype, const void *Q, const void *K, const void *V, const void *Kc, const void *Vc,
+                               const void *O, const float *LSE, const void *dO, float *dQ, float *dK, float *dV,
+                               const Shape &s, float *ws, cudaStream_t stream) {
+    if (dtype == 0) {
+        if (s.d == 128) return run<__nv_bfloat16, 128>(Q, K, V, Kc, Vc, O, LSE, dO, dQ, dK, dV, s, ws, stream);
+        if (s.d == 64) return run<__nv_bfloat16, 64>(Q, K, V, Kc, Vc, O, LSE, dO, dQ, dK, dV, s, ws, stream);
+    } else {
+        if (s.d == 128) return run<float, 128>(Q, K, V, Kc, Vc, O, LSE, dO, dQ, dK, dV, s, ws, stream);
+        if (s.d == 64) return run<float, 64>(Q, K, V, Kc, Vc, O, LSE, dO, dQ, dK, dV, s, ws, stream);
+    }
+    return cudaErrorNotSupported;
+}
+
+}  // namespace cca

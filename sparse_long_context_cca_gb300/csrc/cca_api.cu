@@ -145,6 +145,26 @@ int cca_decode_fwd_noalloc(const void *Q, const void *K, const void *V, const vo
                                         static_cast<cudaStream_t>(stream)));
 }
 
+int cca_prefill_bwd(const void *Q, const void *K, const void *V, const void *Kc, const void *Vc, const void *O,
+                    const float *LSE, const void *dO, float *dQ, float *dK, float *dV, const cca_params_t *params,
+                    void *workspace, uint64_t workspace_bytes, void *stream) {
+    int st = check_shape(params, true);
+    if (st != CCA_OK) return st;
+    const void *ptrs[12] = {Q, K, V, Kc, Vc, O, LSE, dO, dQ, dK, dV, workspace};
+    for (const void *q : ptrs)
+        if (q == nullptr || !aligned16(q)) return CCA_ERR_INVALID_ARG;
+    const cca::Shape s = to_shape(params);
+    if (workspace_bytes < cca::prefill_bwd_workspace_bytes(s)) return CCA_ERR_INVALID_ARG;
+    if ((st = check_device()) != CCA_OK) return st;
+    return from_cuda(cca::launch_prefill_bwd(params->dtype, Q, K, V, Kc, Vc, O, LSE, dO, dQ, dK, dV, s,
+                                             static_cast<float *>(workspace), static_cast<cudaStream_t>(stream)));
+}
+
+uint64_t cca_prefill_bwd_workspace_size(const cca_params_t *params) {
+    if (check_shape(params, true) != CCA_OK) return 0;
+    return cca::prefill_bwd_workspace_bytes(to_shape(params));
+}
+
 uint64_t cca_decode_workspace_size(const cca_params_t *params) {
     if (check_shape(params, true) != CCA_OK) return 0;
     return cca::decode_workspace_bytes(to_shape(params));

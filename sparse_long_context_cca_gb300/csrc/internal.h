@@ -41,4 +41,10 @@ cudaError_t decode_noalloc_scratch(float **out);
 cudaError_t launch_pool_group(int dtype, const void *q, const void *K, const void *V, void *Kc, void *Vc,
                               const Shape &s, int j, cudaStream_t stream);
 
+// Backward pass (fp32 gradients; workspace holds D and the core-token gradients).
+uint64_t prefill_bwd_workspace_bytes(const Shape &s);
+cudaError_t launch_prefill_bwd(int dtype, const void *Q, const void *K, const void *V, const void *Kc, const void *Vc,
+                               const void *O, const float *LSE, const void *dO, float *dQ, float *dK, float *dV,
+                               const Shape &s, float *ws, cudaStream_t stream);
+
 }  // namespace cca

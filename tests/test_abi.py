@@ -127,3 +127,16 @@ def test_rejects_unknown_modes(lib):
         prm = api.make_params(1, 2, 2, 256, 128, 16, 32, api.CCA_BF16, **kw)
         assert lib.cca_attn_fwd(*P, ctypes.byref(prm), None) == api.CCA_ERR_INVALID_ARG
         assert lib.cca_pool(*P[:5], ctypes.byref(prm), None) == api.CCA_ERR_INVALID_ARG
+
+
+def test_backward_rejects_bad_arguments(lib):
+    prm = api.make_params(1, 2, 2, 256, 128, 16, 32, api.CCA_BF16)
+    need = lib.cca_prefill_bwd_workspace_size(ctypes.byref(prm))
+    assert need > 0
+    ptrs = [0x1000 * (k + 1) for k in range(11)]
+    assert lib.cca_prefill_bwd(*ptrs, ctypes.byref(prm), 0xC000, need - 16, None) == api.CCA_ERR_INVALID_ARG
+    bad = list(ptrs)
+    bad[8] = 0
+    assert lib.cca_prefill_bwd(*bad, ctypes.byref(prm), 0xC000, need, None) == api.CCA_ERR_INVALID_ARG
+    prm_bad = api.make_params(1, 2, 2, 250, 128, 16, 32, api.CCA_BF16)
+    assert lib.cca_prefill_bwd_workspace_size(ctypes.byref(prm_bad)) == 0
