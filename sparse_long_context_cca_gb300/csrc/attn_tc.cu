@@ -314,7 +314,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         ok = false;
                         break;
                     }
-                    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {  // unrolled: per-half counters stay in registers
                         const Half &x = it.half(h);
                         if (!half_uses(x, it.Tc, t)) continue;
                         if (!ptx::wait_bounded(bar(B_PFULL + h), pf_cnt[h] & 1, abort_flag, lim)) {
