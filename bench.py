@@ -341,10 +341,11 @@ def backward_bench(wl, dev, stream, iters, peaks):
     flops = 2.5 * W.attn_flops(wl)
     del Q, K, V, O, LSE, Kc, Vc, dO, grads
     torch.cuda.empty_cache()
-    return {"what": "backward of pooling + fused attention (fp32 CUDA-core kernels)", "ms": ms,
+    return {"what": "backward of pooling + fused attention (tcgen05 dQ and dK/dV kernels, "
+                    "fp32 CUDA-core pooling backward)", "ms": ms,
             "eff_tflops": flops / (ms / 1e3) / 1e12,
             "algorithmic_unit": "10*d FLOP per (query, visible key, head): q.k, dO.v, dQ, dK, dV",
-            "kernel_launches": 4}
+            "kernel_launches": 3}
 
 
 def comparator(wl, dev, stream, steps, cca_ms_per_step):

@@ -199,7 +199,12 @@ int cca_pool_group(const void *q, const void *K, const void *V, void *Kc, void *
  *                    cca_prefill_bwd_workspace_size(params) bytes
  * All pooling and window modes are supported, d in {64, 128}, bf16 or f32.
  * Max pooling passes each element's gradient to the first row holding the
- * maximum.  The kernels run on CUDA cores in fp32 (not yet tensor cores).
+ * maximum.  bf16 with d = 128 computes the attention gradients on the tensor
+ * cores (bf16 operands, fp32 accumulation, P and dS rounded to bf16 before
+ * their products); every other case, and the pooling backward, runs on CUDA
+ * cores in fp32.  A kernel that gives up waiting writes CCA_ERR_TIMEOUT into
+ * *params.dev_status when that pointer is set (4-byte aligned); the gradients
+ * are then undefined.
  */
 int cca_prefill_bwd(const void *Q, const void *K, const void *V, const void *Kc, const void *Vc,
                     const void *O, const float *LSE, const void *dO, float *dQ, float *dK, float *dV,

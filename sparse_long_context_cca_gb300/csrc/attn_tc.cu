@@ -41,6 +41,7 @@
 
 #include "internal.h"
 #include "sm100_ptx.cuh"
+#include "tma_host.h"
 
 namespace cca {
 namespace {
@@ -536,36 +537,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 }
 
 // ---------------------------------------------------------------- host side
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
-                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
-                                  CUtensorMapFloatOOBfill);
-
-EncodeTiledFn get_encoder() {
-    static EncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(ptr);
-    });
-    return fn;
-}
-
-// [heads, rows, 128] bf16 viewed as a 3-D tensor; box = 64 columns x 128 rows x 1 head.
-bool encode_3d(EncodeTiledFn enc, CUtensorMap *map, const void *ptr, uint64_t rows, uint64_t heads) {
-    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(HD), rows, heads};
-    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(HD) * 2, rows * HD * 2};
-    const cuuint32_t box[3] = {64, 128, 1};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 struct DeviceInfo {
     bool ready = false;
     int sms = 0;
@@ -604,8 +575,9 @@ cudaError_t launch_attn_bf16_tc(const void *Q, const void *K, const void *V, con
     const uint64_t G = static_cast<uint64_t>(s.N / s.g);
     CUtensorMap mQ, mK, mV, mKc, mVc;
     const uint64_t qh = static_cast<uint64_t>(s.B) * s.Hq, kh = static_cast<uint64_t>(s.B) * s.Hkv;
-    if (!encode_3d(enc, &mQ, Q, s.N, qh) || !encode_3d(enc, &mK, K, s.N, kh) || !encode_3d(enc, &mV, V, s.N, kh) ||
-        !encode_3d(enc, &mKc, Kc, G, kh) || !encode_3d(enc, &mVc, Vc, G, kh))
+    if (!encode_3d_bf16_d128(enc, &mQ, Q, s.N, qh) || !encode_3d_bf16_d128(enc, &mK, K, s.N, kh) ||
+        !encode_3d_bf16_d128(enc, &mV, V, s.N, kh) || !encode_3d_bf16_d128(enc, &mKc, Kc, G, kh) ||
+        !encode_3d_bf16_d128(enc, &mVc, Vc, G, kh))
         return cudaErrorInvalidValue;
 
     Params p;

@@ -25,6 +25,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "internal.h"
 
 namespace cca {
@@ -305,7 +307,7 @@ __global__ void __launch_bounds__(128) bwd_pool_kernel(const T *__restrict__ Q, 
 template <typename T, int D>
 cudaError_t run(const void *Q, const void *K, const void *V, const void *Kc, const void *Vc, const void *O,
                 const float *LSE, const void *dO, float *dQ, float *dK, float *dV, const Shape &s, float *ws,
-                cudaStream_t stream) {
+                int32_t *status, cudaStream_t stream) {
     BwdArgs a{s.B, s.Hq, s.Hkv, s.N, s.g, s.w, s.window_mode, s.pool_mode, s.scale};
     const int64_t G = s.N / s.g;
     float *Dbuf = ws;
@@ -315,12 +317,18 @@ cudaError_t run(const void *Q, const void *K, const void *V, const void *Kc, con
     const T *q = static_cast<const T *>(Q), *k = static_cast<const T *>(K), *v = static_cast<const T *>(V);
     const T *kc = static_cast<const T *>(Kc), *vc = static_cast<const T *>(Vc);
     const T *o = static_cast<const T *>(O), *dout = static_cast<const T *>(dO);
-    bwd_dq_kernel<T, D><<<blocks(static_cast<int64_t>(s.B) * s.Hq * s.N), 128, 0, stream>>>(q, k, v, kc, vc, o, LSE,
-                                                                                             dout, dQ, Dbuf, a);
-    bwd_dkv_raw_kernel<T, D><<<blocks(static_cast<int64_t>(s.B) * s.Hkv * s.N), 128, 0, stream>>>(q, k, v, LSE, dout,
-                                                                                                   Dbuf, dK, dV, a);
-    bwd_dkv_core_kernel<T, D><<<blocks(static_cast<int64_t>(s.B) * s.Hkv * G), 128, 0, stream>>>(q, kc, vc, LSE, dout,
-                                                                                                 Dbuf, dKc, dVc, a);
+    if (std::is_same<T, __nv_bfloat16>::value && D == 128) {
+        const cudaError_t e = launch_attn_bwd_tc(Q, K, V, Kc, Vc, O, LSE, dO, dQ, dK, dV, Dbuf, dKc, dVc, s, status,
+                                                 stream);
+        if (e != cudaSuccess) return e;
+    } else {
+        bwd_dq_kernel<T, D><<<blocks(static_cast<int64_t>(s.B) * s.Hq * s.N), 128, 0, stream>>>(
+            q, k, v, kc, vc, o, LSE, dout, dQ, Dbuf, a);
+        bwd_dkv_raw_kernel<T, D><<<blocks(static_cast<int64_t>(s.B) * s.Hkv * s.N), 128, 0, stream>>>(
+            q, k, v, LSE, dout, Dbuf, dK, dV, a);
+        bwd_dkv_core_kernel<T, D><<<blocks(static_cast<int64_t>(s.B) * s.Hkv * G), 128, 0, stream>>>(
+            q, kc, vc, LSE, dout, Dbuf, dKc, dVc, a);
+    }
     bwd_pool_kernel<T, D><<<blocks(static_cast<int64_t>(s.B) * s.Hkv * G), 128, 0, stream>>>(q, k, v, dKc, dVc, dQ, dK,
                                                                                              dV, a);
     return cudaGetLastError();
@@ -335,13 +343,13 @@ uint64_t prefill_bwd_workspace_bytes(const Shape &s) {
 
 cudaError_t launch_prefill_bwd(int dtype, const void *Q, const void *K, const void *V, const void *Kc, const void *Vc,
                                const void *O, const float *LSE, const void *dO, float *dQ, float *dK, float *dV,
-                               const Shape &s, float *ws, cudaStream_t stream) {
+                               const Shape &s, float *ws, int32_t *status, cudaStream_t stream) {
     if (dtype == 0) {
-        if (s.d == 128) return run<__nv_bfloat16, 128>(Q, K, V, Kc, Vc, O, LSE, dO, dQ, dK, dV, s, ws, stream);
-        if (s.d == 64) return run<__nv_bfloat16, 64>(Q, K, V, Kc, Vc, O, LSE, dO, dQ, dK, dV, s, ws, stream);
+        if (s.d == 128) return run<__nv_bfloat16, 128>(Q, K, V, Kc, Vc, O, LSE, dO, dQ, dK, dV, s, ws, status, stream);
+        if (s.d == 64) return run<__nv_bfloat16, 64>(Q, K, V, Kc, Vc, O, LSE, dO, dQ, dK, dV, s, ws, status, stream);
     } else {
-        if (s.d == 128) return run<float, 128>(Q, K, V, Kc, Vc, O, LSE, dO, dQ, dK, dV, s, ws, stream);
-        if (s.d == 64) return run<float, 64>(Q, K, V, Kc, Vc, O, LSE, dO, dQ, dK, dV, s, ws, stream);
+        if (s.d == 128) return run<float, 128>(Q, K, V, Kc, Vc, O, LSE, dO, dQ, dK, dV, s, ws, status, stream);
+        if (s.d == 64) return run<float, 64>(Q, K, V, Kc, Vc, O, LSE, dO, dQ, dK, dV, s, ws, status, stream);
     }
     return cudaErrorNotSupported;
 }

@@ -1,0 +1,525 @@
+// Tensor-core backward of the fused core/local attention (bf16, d = 128): the
+// gradient of the fusion equation of "Core Context Aware Transformers for Long
+// Context Language Modeling" (Method section), with P recomputed from the
+// forward's LSE.  Notation as in bwd.cu: dS = P (dO.v - D), D_i = dO_i . O_i.
+//
+// Two kernels, 128 threads each; thread 0 issues the TMA copies and the
+// tcgen05.mma instructions, thread t owns TMEM lane t for the element-wise work.
+//
+//  dq kernel, one 128-row query tile of one (b, h) per CTA, over the same key
+//  tiles as the forward (cores, then the band):
+//     S = Q K^T, dP = dO V^T (both SS, fp32 in TMEM)  ->  dS (bf16, over S)
+//     dQ += dS K  (A = dS in TMEM, B = K tile read MN-major)
+//  TMEM: S | dP | dQ.  K/V tiles are double-buffered: the next tile's copy is
+//  in flight while this one is processed.
+//
+//  dkv kernel, one 128-key tile (raw tokens or cores) of one (b, kv) per CTA,
+//  over the query tiles of the r query heads that see any of its keys:
+//     S^T = K Q^T, dP^T = V dO^T  ->  P^T over S^T, dS^T over dP^T (bf16)
+//     dV += P^T dO,  dK += dS^T Q   (A in TMEM, B = Q / dO tiles read MN-major)
+//  TMEM: S^T | dP^T | dK | dV.  Q/dO tiles are double-buffered.
+//
+// The pooling backward (bwd.cu) then adds the paths through the core tokens.
+// Every wait is bounded; a time-out anywhere becomes a CTA-wide exit agreed on
+// with __syncthreads_or: the copies and MMAs in flight are waited for (again
+// bounded), TMEM is freed and CCA_ERR_TIMEOUT is written to the status word.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "internal.h"
+#include "sm100_ptx.cuh"
+#include "tma_host.h"
+
+namespace cca {
+
+extern unsigned long long g_wait_limit_ns;
+
+namespace {
+
+constexpr int BT = 128;  // rows per tile (queries or keys)
+constexpr int HD = 128;
+constexpr uint32_t TILE_BYTES = BT * HD * 2;
+constexpr uint32_t HALF_BYTES = TILE_BYTES / 2;
+constexpr uint32_t IDESC_SS = ptx::idesc_bf16_f32(128, 128, 0, 0);  // K-major A and B
+constexpr uint32_t IDESC_TS = ptx::idesc_bf16_f32(128, 128, 0, 1);  // A in TMEM, B MN-major
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr int32_t STATUS_TIMEOUT = -4;
+// six tiles (two resident, two double-buffered pairs), alignment slack, barriers + TMEM slot, LSE/D staging
+constexpr uint32_t CTRL_BYTES = 128;
+constexpr uint32_t SMEM_BYTES = 6 * TILE_BYTES + 1024 + CTRL_BYTES + 2 * 2 * BT * 4;
+
+struct BwdTcParams {
+    int B, Hq, Hkv, N, g, w, window_mode, G;
+    float tau;
+    const float *LSE;
+    const __nv_bfloat16 *O, *dO;
+    float *Dbuf;          // written by the dq kernel, read by the dkv kernel
+    float *dQ, *dK, *dV;  // fp32 outputs
+    float *dKc, *dVc;     // fp32 core-token gradients (workspace)
+    int32_t *status;
+    unsigned long long wait_limit_ns;
+};
+
+__device__ __forceinline__ int lo_of(int i, int w) { return i - w + 1 > 0 ? i - w + 1 : 0; }
+__device__ __forceinline__ int win_of(const BwdTcParams &p, int i) {
+    const int lo = lo_of(i, p.w);
+    return p.window_mode ? (lo / p.g) * p.g : lo;
+}
+
+__device__ __forceinline__ float bf(uint32_t w, int hi) {
+    return __uint_as_float(hi ? (w & 0xffff0000u) : (w << 16));
+}
+
+// Shared-memory carve-up common to both kernels: six 32 KB tiles from a
+// 1024-aligned base, then barriers, the TMEM slot and two staging arrays.
+struct Smem {
+    uint32_t tile[6];  // shared addresses
+    uint64_t *bars;    // [0] resident pair, [1..2] double buffer, [3] mma, [4] drain
+    uint32_t *tmem_slot;
+    float *stage;      // 2 x 2 x BT floats
+};
+
+__device__ __forceinline__ Smem carve(uint8_t *raw) {
+    Smem s;
+    const uint32_t r = ptx::smem_addr(raw);
+    const uint32_t base = (r + 1023u) & ~1023u;
+    uint8_t *g = raw + (base - r);
+    for (int k = 0; k < 6; ++k) s.tile[k] = base + k * TILE_BYTES;
+    s.bars = reinterpret_cast<uint64_t *>(g + 6 * TILE_BYTES);
+    s.tmem_slot = reinterpret_cast<uint32_t *>(g + 6 * TILE_BYTES + 64);
+    s.stage = reinterpret_cast<float *>(g + 6 * TILE_BYTES + CTRL_BYTES);
+    return s;
+}
+
+__device__ __forceinline__ void load_tile(const void *map, uint32_t bar, uint32_t dst, int y, int z) {
+    ptx::tma_load_3d(map, bar, dst, 0, y, z);
+    ptx::tma_load_3d(map, bar, dst + HALF_BYTES, 64, y, z);
+}
+
+// Block-level wait: every thread polls, the CTA agrees on the outcome.  On a
+// time-out thread 0 gives the awaited operation one more bounded wait so that
+// nothing is still writing shared memory when the CTA leaves.
+struct Waiter {
+    uint64_t limit;
+    volatile int flag;
+    __device__ __forceinline__ bool operator()(uint32_t bar, uint32_t parity) {
+        const bool mine = ptx::wait_bounded(bar, parity, &flag, limit);
+        if (!__syncthreads_or(!mine)) return true;
+        if (threadIdx.x == 0) {
+            flag = 0;
+            ptx::wait_bounded(bar, parity, &flag, limit);
+        }
+        return false;
+    }
+};
+
+__device__ __forceinline__ uint32_t tmem_setup(const Smem &sm, int nbars) {
+    if (threadIdx.x == 0) {
+        for (int k = 0; k < nbars; ++k) ptx::mbar_init(ptx::smem_addr(&sm.bars[k]), 1);
+        ptx::fence_mbar_init();
+    }
+    if (threadIdx.x < 32) {
+        ptx::tmem_alloc(ptx::smem_addr(sm.tmem_slot), 512);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    return *sm.tmem_slot;
+}
+
+// Leaves the CTA: after an abort, waits (bounded) for every tcgen05 op issued so far;
+// then frees TMEM and reports the time-out.
+__device__ __forceinline__ void tmem_teardown(const Smem &sm, uint32_t tmem, bool ok, const BwdTcParams &p) {
+    if (!ok && threadIdx.x == 0) {
+        volatile int flag = 0;
+        const uint32_t drain = ptx::smem_addr(&sm.bars[4]);
+        ptx::tc_commit(drain);
+        ptx::wait_bounded(drain, 0, &flag, p.wait_limit_ns);
+        if (p.status != nullptr) atomicCAS(p.status, 0, STATUS_TIMEOUT);
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, 512);
+    }
+}
+
+// ---------------------------------------------------------------- dQ
+__global__ void __launch_bounds__(128, 1)
+    bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
+                     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                     const __grid_constant__ CUtensorMap tmKc, const __grid_constant__ CUtensorMap tmVc,
+                     const BwdTcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const Smem sm = carve(smem_raw);
+    const uint32_t sQ = sm.tile[0], sdO = sm.tile[1];
+    const uint32_t b_qd = ptx::smem_addr(&sm.bars[0]), b_mma = ptx::smem_addr(&sm.bars[3]);
+    const int t = threadIdx.x, warp = t >> 5;
+    const int BH = p.B * p.Hq, n_qt = (p.N + BT - 1) / BT;
+    const int qt = n_qt - 1 - static_cast<int>(blockIdx.x / BH);  // heaviest tiles first
+    const int bh = static_cast<int>(blockIdx.x % BH);
+    const int kvz = (bh / p.Hq) * p.Hkv + (bh % p.Hq) / (p.Hq / p.Hkv);
+    const int i0 = qt * BT, i1 = min(i0 + BT - 1, p.N - 1);
+    const int lo0 = win_of(p, i0);
+    const int Tc = (lo_of(i1, p.w) / p.g + BT - 1) / BT;  // core tiles
+    const int T = Tc + (i1 - lo0) / BT + 1;               // + band tiles
+
+    const uint32_t tmem = tmem_setup(sm, 5);
+    const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
+    Waiter wait{p.wait_limit_ns, 0};
+
+    auto issue_kv = [&](int tt) {
+        const bool core = tt < Tc;
+        const int y0 = core ? tt * BT : lo0 + (tt - Tc) * BT;
+        const uint32_t bar = ptx::smem_addr(&sm.bars[1 + (tt & 1)]);
+        ptx::mbar_arrive_expect_tx(bar, 2 * TILE_BYTES);
+        load_tile(core ? (const void *)&tmKc : (const void *)&tmK, bar, sm.tile[2 + 2 * (tt & 1)], y0, kvz);
+        load_tile(core ? (const void *)&tmVc : (const void *)&tmV, bar, sm.tile[3 + 2 * (tt & 1)], y0, kvz);
+    };
+    if (t == 0) {
+        ptx::mbar_arrive_expect_tx(b_qd, 2 * TILE_BYTES);
+        load_tile(&tmQ, b_qd, sQ, i0, bh);
+        load_tile(&tmdO, b_qd, sdO, i0, bh);
+        issue_kv(0);
+    }
+
+    // this thread's row: D = dO . O (also stored for the dkv kernel) and the LSE in log2 units
+    const int i = i0 + t;
+    const bool valid = i < p.N;
+    float Di = 0.f, lse2 = 0.f;
+    if (valid) {
+        const int64_t u = static_cast<int64_t>(bh) * p.N + i;
+        const uint4 *o4 = reinterpret_cast<const uint4 *>(p.O + u * HD);
+        const uint4 *d4 = reinterpret_cast<const uint4 *>(p.dO + u * HD);
+#pragma unroll 4
+        for (int c = 0; c < HD / 8; ++c) {
+            const uint4 a = o4[c], b = d4[c];
+            const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) Di += bf(aw[k], 0) * bf(bw[k], 0) + bf(aw[k], 1) * bf(bw[k], 1);
+        }
+        lse2 = p.LSE[u] * LOG2E;
+        p.Dbuf[u] = Di;
+    }
+    const int lo_i = win_of(p, i), nc_i = lo_of(i, p.w) / p.g;
+    const float c1 = p.tau * LOG2E;
+    const uint64_t dQd = ptx::smem_desc_sw128(sQ, 16, 1024), ddOd = ptx::smem_desc_sw128(sdO, 16, 1024);
+
+    bool ok = wait(b_qd, 0);
+    uint32_t mma_phase = 0;
+    for (int tt = 0; ok && tt < T; ++tt) {
+        const bool core = tt < Tc;
+        const int y0 = core ? tt * BT : lo0 + (tt - Tc) * BT;
+        const uint32_t sK = sm.tile[2 + 2 * (tt & 1)], sV = sm.tile[3 + 2 * (tt & 1)];
+        if (!(ok = wait(ptx::smem_addr(&sm.bars[1 + (tt & 1)]), (tt >> 1) & 1))) break;
+        if (t == 0) {
+            if (tt + 1 < T) issue_kv(tt + 1);  // its buffer was last read by tile tt-1's finished MMAs
+            ptx::tc_fence_after();
+            ptx::mma_ss_k128(tmem + 0, dQd, ptx::smem_desc_sw128(sK, 16, 1024), IDESC_SS, 0u);     // S  = Q K^T
+            ptx::mma_ss_k128(tmem + 128, ddOd, ptx::smem_desc_sw128(sV, 16, 1024), IDESC_SS, 0u);  // dP = dO V^T
+            ptx::tc_commit(b_mma);
+        }
+        if (!(ok = wait(b_mma, mma_phase++ & 1))) break;
+        ptx::tc_fence_after();
+        // dS = P (dP - D) on this row's visible columns; bf16 pairs written over S
+        int c_lo = 0, c_hi = BT - 1;
+        if (core) {
+            c_hi = min(nc_i - y0, BT) - 1;
+        } else {
+            c_lo = max(lo_i - y0, 0);
+            c_hi = min(i - y0, BT - 1);
+        }
+        if (!valid) c_hi = -1;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+            uint32_t s[32], dp[32];
+            ptx::tmem_ld32(tmem + lane_addr + c * 32, s);
+            ptx::tmem_ld32(tmem + lane_addr + 128 + c * 32, dp);
+            ptx::tmem_wait_ld(s);
+            ptx::reg_touch(dp);
+            uint32_t pk[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                float d2[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int col = c * 32 + 2 * k + e;
+                    const bool vis = col >= c_lo && col <= c_hi;
+                    const float pr = vis ? ptx::ex2(fmaf(__uint_as_float(s[2 * k + e]), c1, -lse2)) : 0.f;
+                    d2[e] = pr * (__uint_as_float(dp[2 * k + e]) - Di);
+                }
+                pk[k] = ptx::pack_bf16x2(d2[0], d2[1]);
+            }
+            ptx::tmem_st16(tmem + lane_addr + c * 16, pk);
+        }
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        __syncthreads();
+        if (t == 0) {
+            ptx::tc_fence_after();
+            ptx::mma_ts_k128(tmem + 256, tmem + 0, ptx::smem_desc_sw128(sK, HALF_BYTES, 1024), IDESC_TS,
+                             tt > 0 ? 1u : 0u);  // dQ += dS K
+            ptx::tc_commit(b_mma);
+        }
+        if (!(ok = wait(b_mma, mma_phase++ & 1))) break;
+    }
+    if (ok) {
+        ptx::tc_fence_after();
+        float *dst = p.dQ + (static_cast<int64_t>(bh) * p.N + i) * HD;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+            uint32_t o[32];
+            ptx::tmem_ld32(tmem + lane_addr + 256 + c * 32, o);
+            ptx::tmem_wait_ld(o);
+            if (valid) {
+#pragma unroll
+                for (int k = 0; k < 32; k += 4)
+                    *reinterpret_cast<float4 *>(dst + c * 32 + k) =
+                        make_float4(__uint_as_float(o[k]) * p.tau, __uint_as_float(o[k + 1]) * p.tau,
+                                    __uint_as_float(o[k + 2]) * p.tau, __uint_as_float(o[k + 3]) * p.tau);
+            }
+        }
+    }
+    tmem_teardown(sm, tmem, ok, p);
+}
+
+// ---------------------------------------------------------------- dK, dV
+__global__ void __launch_bounds__(128, 1)
+    bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
+                      const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                      const __grid_constant__ CUtensorMap tmKc, const __grid_constant__ CUtensorMap tmVc,
+                      const BwdTcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const Smem sm = carve(smem_raw);
+    const uint32_t sK = sm.tile[0], sV = sm.tile[1];
+    const uint32_t b_kv = ptx::smem_addr(&sm.bars[0]), b_mma = ptx::smem_addr(&sm.bars[3]);
+    const int t = threadIdx.x, warp = t >> 5;
+    const int BK = p.B * p.Hkv;
+    const int n_core_t = (p.G + BT - 1) / BT;
+    // core tiles first (they are seen by the most query rows), then raw-token tiles
+    const int idx = static_cast<int>(blockIdx.x / BK);
+    const int bk = static_cast<int>(blockIdx.x % BK);
+    const bool core = idx < n_core_t;
+    const int y0 = core ? idx * BT : (idx - n_core_t) * BT;
+    const int n_keys = core ? p.G : p.N;
+    const int r = p.Hq / p.Hkv;
+    const int b = bk / p.Hkv, kv = bk % p.Hkv;
+    // the query rows that see at least one key of the tile
+    int r_lo, r_hi;
+    if (core) {
+        r_lo = (y0 + 1) * p.g + p.w - 1;  // core j is seen from row (j+1)g + w - 1 on
+        r_hi = p.N - 1;
+    } else {
+        const int m_last = min(y0 + BT - 1, p.N - 1);
+        const int64_t last = p.window_mode ? static_cast<int64_t>(m_last / p.g + 1) * p.g + p.w - 2
+                                           : static_cast<int64_t>(m_last) + p.w - 1;
+        r_lo = y0;
+        r_hi = static_cast<int>(last < p.N - 1 ? last : p.N - 1);
+    }
+    const int qt_lo = r_lo / BT;
+    const int nq = r_lo <= r_hi ? r_hi / BT - qt_lo + 1 : 0;
+    const int n_it = nq * r;  // (head, query tile) pairs, head-major
+
+    const uint32_t tmem = tmem_setup(sm, 5);
+    const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
+    Waiter wait{p.wait_limit_ns, 0};
+    const int m = y0 + t;  // this thread's key (core index or token)
+    const float c1 = p.tau * LOG2E;
+
+    auto bh_of = [&](int it) { return b * p.Hq + kv * r + it / nq; };
+    auto i0_of = [&](int it) { return (qt_lo + it % nq) * BT; };
+    auto issue_q = [&](int it) {
+        const uint32_t bar = ptx::smem_addr(&sm.bars[1 + (it & 1)]);
+        ptx::mbar_arrive_expect_tx(bar, 2 * TILE_BYTES);
+        load_tile(&tmQ, bar, sm.tile[2 + 2 * (it & 1)], i0_of(it), bh_of(it));
+        load_tile(&tmdO, bar, sm.tile[3 + 2 * (it & 1)], i0_of(it), bh_of(it));
+    };
+    if (t == 0) {
+        ptx::mbar_arrive_expect_tx(b_kv, 2 * TILE_BYTES);
+        load_tile(core ? (const void *)&tmKc : (const void *)&tmK, b_kv, sK, y0, bk);
+        load_tile(core ? (const void *)&tmVc : (const void *)&tmV, b_kv, sV, y0, bk);
+        if (n_it > 0) issue_q(0);
+    }
+    const uint64_t dKk = ptx::smem_desc_sw128(sK, 16, 1024), dVk = ptx::smem_desc_sw128(sV, 16, 1024);
+
+    bool ok = wait(b_kv, 0);
+    uint32_t mma_phase = 0;
+    for (int it = 0; ok && it < n_it; ++it) {
+        const int bh = bh_of(it), i0 = i0_of(it);
+        const uint32_t sQ = sm.tile[2 + 2 * (it & 1)], sdO = sm.tile[3 + 2 * (it & 1)];
+        float *s_lse = sm.stage + (it & 1) * 2 * BT, *s_D = s_lse + BT;
+        const int iq = i0 + t;  // the row whose LSE and D this thread stages
+        s_lse[t] = iq < p.N ? p.LSE[static_cast<int64_t>(bh) * p.N + iq] * LOG2E : 0.f;
+        s_D[t] = iq < p.N ? p.Dbuf[static_cast<int64_t>(bh) * p.N + iq] : 0.f;
+        if (!(ok = wait(ptx::smem_addr(&sm.bars[1 + (it & 1)]), (it >> 1) & 1))) break;
+        if (t == 0) {
+            if (it + 1 < n_it) issue_q(it + 1);  // its buffer was last read by pair it-1's finished MMAs
+            ptx::tc_fence_after();
+            ptx::mma_ss_k128(tmem + 0, dKk, ptx::smem_desc_sw128(sQ, 16, 1024), IDESC_SS, 0u);     // S^T  = K Q^T
+            ptx::mma_ss_k128(tmem + 128, dVk, ptx::smem_desc_sw128(sdO, 16, 1024), IDESC_SS, 0u);  // dP^T = V dO^T
+            ptx::tc_commit(b_mma);
+        }
+        if (!(ok = wait(b_mma, mma_phase++ & 1))) break;
+        ptx::tc_fence_after();
+        // this key's visible query columns [q_lo, q_hi] of the tile
+        int q_lo, q_hi;
+        if (m >= n_keys) {
+            q_lo = 0;
+            q_hi = -1;
+        } else if (core) {
+            q_lo = max((m + 1) * p.g + p.w - 1 - i0, 0);
+            q_hi = min(p.N - 1 - i0, BT - 1);
+        } else {
+            const int64_t last = p.window_mode ? static_cast<int64_t>(m / p.g + 1) * p.g + p.w - 2
+                                               : static_cast<int64_t>(m) + p.w - 1;
+            q_lo = max(m - i0, 0);
+            const int last_i = static_cast<int>(last < p.N - 1 ? last : p.N - 1);
+            q_hi = min(last_i - i0, BT - 1);
+        }
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+            uint32_t s[32], dp[32];
+            ptx::tmem_ld32(tmem + lane_addr + c * 32, s);
+            ptx::tmem_ld32(tmem + lane_addr + 128 + c * 32, dp);
+            ptx::tmem_wait_ld(s);
+            ptx::reg_touch(dp);
+            uint32_t pp[16], dd[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                float pv[2], dv[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int col = c * 32 + 2 * k + e;
+                    const bool vis = col >= q_lo && col <= q_hi;
+                    const float pr = vis ? ptx::ex2(fmaf(__uint_as_float(s[2 * k + e]), c1, -s_lse[col])) : 0.f;
+                    pv[e] = pr;
+                    dv[e] = pr * (__uint_as_float(dp[2 * k + e]) - s_D[col]);
+                }
+                pp[k] = ptx::pack_bf16x2(pv[0], pv[1]);
+                dd[k] = ptx::pack_bf16x2(dv[0], dv[1]);
+            }
+            ptx::tmem_st16(tmem + lane_addr + c * 16, pp);        // P^T  over S^T
+            ptx::tmem_st16(tmem + lane_addr + 128 + c * 16, dd);  // dS^T over dP^T
+        }
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        __syncthreads();
+        if (t == 0) {
+            ptx::tc_fence_after();
+            const uint32_t acc = it > 0 ? 1u : 0u;
+            ptx::mma_ts_k128(tmem + 384, tmem + 0, ptx::smem_desc_sw128(sdO, HALF_BYTES, 1024), IDESC_TS,
+                             acc);  // dV += P^T dO
+            ptx::mma_ts_k128(tmem + 256, tmem + 128, ptx::smem_desc_sw128(sQ, HALF_BYTES, 1024), IDESC_TS,
+                             acc);  // dK += dS^T Q
+            ptx::tc_commit(b_mma);
+        }
+        if (!(ok = wait(b_mma, mma_phase++ & 1))) break;
+    }
+    if (ok) {
+        const bool mine = m < n_keys;
+        float *dk = (core ? p.dKc : p.dK) + (static_cast<int64_t>(bk) * n_keys + m) * HD;
+        float *dv = (core ? p.dVc : p.dV) + (static_cast<int64_t>(bk) * n_keys + m) * HD;
+        ptx::tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+            uint32_t a[32], v[32];
+            if (n_it > 0) {
+                ptx::tmem_ld32(tmem + lane_addr + 256 + c * 32, a);
+                ptx::tmem_ld32(tmem + lane_addr + 384 + c * 32, v);
+                ptx::tmem_wait_ld(a);
+                ptx::reg_touch(v);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 32; ++k) a[k] = v[k] = 0u;
+            }
+            if (mine) {
+#pragma unroll
+                for (int k = 0; k < 32; k += 4) {
+                    *reinterpret_cast<float4 *>(dk + c * 32 + k) =
+                        make_float4(__uint_as_float(a[k]) * p.tau, __uint_as_float(a[k + 1]) * p.tau,
+                                    __uint_as_float(a[k + 2]) * p.tau, __uint_as_float(a[k + 3]) * p.tau);
+                    *reinterpret_cast<float4 *>(dv + c * 32 + k) =
+                        make_float4(__uint_as_float(v[k]), __uint_as_float(v[k + 1]), __uint_as_float(v[k + 2]),
+                                    __uint_as_float(v[k + 3]));
+                }
+            }
+        }
+    }
+    tmem_teardown(sm, tmem, ok, p);
+}
+
+struct Attr {
+    bool done = false;
+    cudaError_t err = cudaSuccess;
+};
+
+}  // namespace
+
+cudaError_t launch_attn_bwd_tc(const void *Q, const void *K, const void *V, const void *Kc, const void *Vc,
+                               const void *O, const float *LSE, const void *dO, float *dQ, float *dK, float *dV,
+                               float *Dbuf, float *dKc, float *dVc, const Shape &s, int32_t *status,
+                               cudaStream_t stream) {
+    EncodeTiledFn enc = get_encoder();
+    if (enc == nullptr) return cudaErrorNotSupported;
+    static std::mutex mu;
+    static Attr attr[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        Attr &a = attr[dev & 63];
+        if (!a.done) {
+            a.err = cudaFuncSetAttribute(bwd_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+            if (a.err == cudaSuccess)
+                a.err = cudaFuncSetAttribute(bwd_dkv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             SMEM_BYTES);
+            a.done = true;
+        }
+        if (a.err != cudaSuccess) return a.err;
+    }
+    const uint64_t G = static_cast<uint64_t>(s.N / s.g);
+    const uint64_t qh = static_cast<uint64_t>(s.B) * s.Hq, kh = static_cast<uint64_t>(s.B) * s.Hkv;
+    CUtensorMap mQ, mdO, mK, mV, mKc, mVc;
+    if (!encode_3d_bf16_d128(enc, &mQ, Q, s.N, qh) || !encode_3d_bf16_d128(enc, &mdO, dO, s.N, qh) ||
+        !encode_3d_bf16_d128(enc, &mK, K, s.N, kh) || !encode_3d_bf16_d128(enc, &mV, V, s.N, kh) ||
+        !encode_3d_bf16_d128(enc, &mKc, Kc, G, kh) || !encode_3d_bf16_d128(enc, &mVc, Vc, G, kh))
+        return cudaErrorInvalidValue;
+    BwdTcParams p;
+    p.B = s.B;
+    p.Hq = s.Hq;
+    p.Hkv = s.Hkv;
+    p.N = s.N;
+    p.g = s.g;
+    p.w = s.w;
+    p.window_mode = s.window_mode;
+    p.G = static_cast<int>(G);
+    p.tau = s.scale;
+    p.LSE = LSE;
+    p.O = static_cast<const __nv_bfloat16 *>(O);
+    p.dO = static_cast<const __nv_bfloat16 *>(dO);
+    p.Dbuf = Dbuf;
+    p.dQ = dQ;
+    p.dK = dK;
+    p.dV = dV;
+    p.dKc = dKc;
+    p.dVc = dVc;
+    p.status = status;
+    p.wait_limit_ns = g_wait_limit_ns;
+    const unsigned n_qt = static_cast<unsigned>((s.N + BT - 1) / BT);
+    bwd_dq_tc_kernel<<<n_qt * static_cast<unsigned>(qh), 128, SMEM_BYTES, stream>>>(mQ, mdO, mK, mV, mKc, mVc, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const unsigned n_kt = static_cast<unsigned>((G + BT - 1) / BT + (s.N + BT - 1) / BT);
+    bwd_dkv_tc_kernel<<<n_kt * static_cast<unsigned>(kh), 128, SMEM_BYTES, stream>>>(mQ, mdO, mK, mV, mKc, mVc,
+                                                                                      p);
+    return cudaGetLastError();
+}
+
+}  // namespace cca

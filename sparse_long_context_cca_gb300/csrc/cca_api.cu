@@ -155,9 +155,12 @@ int cca_prefill_bwd(const void *Q, const void *K, const void *V, const void *Kc,
         if (q == nullptr || !aligned16(q)) return CCA_ERR_INVALID_ARG;
     const cca::Shape s = to_shape(params);
     if (workspace_bytes < cca::prefill_bwd_workspace_bytes(s)) return CCA_ERR_INVALID_ARG;
+    if (params->dev_status != nullptr && (reinterpret_cast<uintptr_t>(params->dev_status) & 3u) != 0)
+        return CCA_ERR_INVALID_ARG;
     if ((st = check_device()) != CCA_OK) return st;
     return from_cuda(cca::launch_prefill_bwd(params->dtype, Q, K, V, Kc, Vc, O, LSE, dO, dQ, dK, dV, s,
-                                             static_cast<float *>(workspace), static_cast<cudaStream_t>(stream)));
+                                             static_cast<float *>(workspace), params->dev_status,
+                                             static_cast<cudaStream_t>(stream)));
 }
 
 uint64_t cca_prefill_bwd_workspace_size(const cca_params_t *params) {

@@ -43,8 +43,15 @@ cudaError_t launch_pool_group(int dtype, const void *q, const void *K, const voi
 
 // Backward pass (fp32 gradients; workspace holds D and the core-token gradients).
 uint64_t prefill_bwd_workspace_bytes(const Shape &s);
+// bf16 with d = 128 runs the attention part on the tensor cores (launch_attn_bwd_tc).
 cudaError_t launch_prefill_bwd(int dtype, const void *Q, const void *K, const void *V, const void *Kc, const void *Vc,
                                const void *O, const float *LSE, const void *dO, float *dQ, float *dK, float *dV,
-                               const Shape &s, float *ws, cudaStream_t stream);
+                               const Shape &s, float *ws, int32_t *status, cudaStream_t stream);
+// Tensor-core attention backward (bf16, d = 128): writes dQ (all rows), D = dO.O into Dbuf,
+// dK/dV of the raw tokens and dKc/dVc of the cores; the pooling backward is not included.
+cudaError_t launch_attn_bwd_tc(const void *Q, const void *K, const void *V, const void *Kc, const void *Vc,
+                               const void *O, const float *LSE, const void *dO, float *dQ, float *dK, float *dV,
+                               float *Dbuf, float *dKc, float *dVc, const Shape &s, int32_t *status,
+                               cudaStream_t stream);
 
 }  // namespace cca

@@ -22,6 +22,14 @@ CASES = [
     (wl(1, 2, 2, 256, 64, 4, 20, "f32"), 1, 0), (wl(1, 2, 1, 320, 64, 5, 40, "f32"), 2, 0),
     (wl(1, 4, 4, 512, 128, 16, 64), 0, 0), (wl(2, 4, 2, 512, 128, 16, 100), 0, 1),
     (wl(1, 2, 2, 256, 128, 1, 40), 0, 0),
+    # several core tiles (G = 260), ragged last tile, GQA r = 4
+    (wl(1, 4, 1, 1040, 128, 4, 70), 0, 0),
+    # window of one token, mean pooling, group-aligned window
+    (wl(1, 2, 2, 640, 128, 8, 1), 1, 1),
+    # max pooling, window wider than a tile
+    (wl(1, 2, 2, 384, 128, 16, 300), 2, 0),
+    # window covers the whole sequence: no core is ever visible
+    (wl(1, 2, 2, 256, 128, 16, 512), 0, 0),
 ]
 
 
