@@ -213,6 +213,38 @@ int cca_prefill_bwd(const void *Q, const void *K, const void *V, const void *Kc,
 /* Bytes of workspace cca_prefill_bwd needs (0 on bad params). */
 uint64_t cca_prefill_bwd_workspace_size(const cca_params_t *params);
 
+/*
+ * cca_prefill_host - the whole prefill step (cca_pool, then cca_attn_fwd) on
+ * HOST buffers: Q, K, V are copied to the device, pooled and attended, and O
+ * (plus LSE, Kc, Vc when asked for) copied back.  The (batch, KV head) pairs
+ * are independent problems (the pooling equation and the fusion equation of
+ * the digest page, Method section, never mix them), so the call cuts them into
+ * about eight slices of consecutive pairs and pipelines the slices over three
+ * streams: copies in, kernels on `stream`, copies out.  The copies of one slice
+ * overlap the kernels of another.
+ *   hQ, hK, hV    host (or any UVA-addressable) [B,Hq,N,d] / [B,Hkv,N,d] inputs
+ *   hO            host [B,Hq,N,d] output, dtype of params
+ *   hLSE          host [B,Hq,N] fp32 output, or NULL to skip it
+ *   hKc, hVc      host [B,Hkv,N/g,d] outputs, or both NULL to skip them
+ *   workspace     device buffer, 16-byte aligned, of at least
+ *                 cca_prefill_host_workspace_size(params) bytes (three slice buffers)
+ * Host buffers should be page-locked (cudaHostAlloc / cudaHostRegister): the
+ * copies from and to pageable memory are correct, but the driver stages them
+ * and the host may block on each, which removes the overlap.
+ * The call returns once everything is enqueued.  Work is ordered after what is
+ * already queued on `stream`, and `stream` resumes only after the last copy-out,
+ * so synchronising `stream` makes every output valid on the host.  The internal
+ * streams and events are kept per device for later calls.  Errors: as
+ * cca_attn_fwd, checked before anything is enqueued; a CUDA failure after some
+ * slices were enqueued returns CCA_ERR_CUDA with the outputs undefined.
+ */
+int cca_prefill_host(const void *hQ, const void *hK, const void *hV, void *hO, float *hLSE, void *hKc,
+                     void *hVc, const cca_params_t *params, void *workspace, uint64_t workspace_bytes,
+                     void *stream);
+
+/* Device bytes of workspace cca_prefill_host needs (0 on bad params). */
+uint64_t cca_prefill_host_workspace_size(const cca_params_t *params);
+
 /* Static English text for a status code (never NULL). */
 const char *cca_status_string(int status);
 

@@ -47,6 +47,7 @@ _lock = threading.Lock()
 
 EXPORTED = ["cca_pool", "cca_attn_fwd", "cca_decode_fwd", "cca_decode_workspace_size", "cca_pool_group",
             "cca_decode_fwd_noalloc", "cca_prefill_bwd", "cca_prefill_bwd_workspace_size",
+            "cca_prefill_host", "cca_prefill_host_workspace_size",
             "cca_status_string", "cca_abi_version", "cca_test_set_wait_limit_ns", "cca_test_skip_q_load"]
 
 
@@ -79,6 +80,10 @@ def load_library():
         lib.cca_prefill_bwd.restype = ctypes.c_int
         lib.cca_prefill_bwd_workspace_size.argtypes = [pp]
         lib.cca_prefill_bwd_workspace_size.restype = ctypes.c_uint64
+        lib.cca_prefill_host.argtypes = [vp] * 7 + [pp, vp, ctypes.c_uint64, vp]
+        lib.cca_prefill_host.restype = ctypes.c_int
+        lib.cca_prefill_host_workspace_size.argtypes = [pp]
+        lib.cca_prefill_host_workspace_size.restype = ctypes.c_uint64
         lib.cca_decode_workspace_size.argtypes = [pp]
         lib.cca_decode_workspace_size.restype = ctypes.c_uint64
         lib.cca_pool_group.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, pp, vp]
@@ -299,3 +304,68 @@ def cca_prefill_bwd(Q, K, V, Kc, Vc, O, LSE, dO, g: int, w: int, scale: float = 
     if st != CCA_OK:
         raise CcaError(st, "cca_prefill_bwd")
     return dQ, dK, dV
+
+
+def _check_host(t: torch.Tensor, name: str, dtype, shape):
+    if not isinstance(t, torch.Tensor) or t.device.type != "cpu":
+        raise ValueError(f"{name} must be a CPU tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def prefill_host_workspace_size(B, Hq, Hkv, N, d, g, w, dtype) -> int:
+    prm = make_params(B, Hq, Hkv, N, d, g, w, _DTYPE[dtype])
+    return int(load_library().cca_prefill_host_workspace_size(ctypes.byref(prm)))
+
+
+def cca_prefill_host(Q, K, V, g: int, w: int, scale: float = 0.0, out=None, with_lse: bool = True,
+                     with_cores: bool = False, workspace=None, device=None, stream=None, pool_mode: int = 0,
+                     window_mode: int = 0):
+    """The prefill step on HOST tensors (pinned for overlap): the library copies Q, K, V in,
+    pools, attends and copies the outputs back, pipelined over slices of KV heads.
+    Returns (O, LSE or None, Kc or None, Vc or None) as CPU tensors; `out` may hold them
+    preallocated.  The outputs are valid once `stream` has been synchronised."""
+    lib = load_library()
+    B, Hq, Hkv, N, d = _dims(Q, K)
+    if Q.dtype not in _DTYPE:
+        raise ValueError(f"unsupported dtype {Q.dtype}")
+    G = N // g if g > 0 else 0
+    _check_host(Q, "Q", Q.dtype, (B, Hq, N, d))
+    _check_host(K, "K", Q.dtype, (B, Hkv, N, d))
+    _check_host(V, "V", Q.dtype, (B, Hkv, N, d))
+    pin = Q.is_pinned()
+    if out is None:
+        O = torch.empty((B, Hq, N, d), dtype=Q.dtype, pin_memory=pin)
+        LSE = torch.empty((B, Hq, N), dtype=torch.float32, pin_memory=pin) if with_lse else None
+        Kc = torch.empty((B, Hkv, G, d), dtype=Q.dtype, pin_memory=pin) if with_cores else None
+        Vc = torch.empty((B, Hkv, G, d), dtype=Q.dtype, pin_memory=pin) if with_cores else None
+    else:
+        O, LSE, Kc, Vc = out
+    _check_host(O, "O", Q.dtype, (B, Hq, N, d))
+    if LSE is not None:
+        _check_host(LSE, "LSE", torch.float32, (B, Hq, N))
+    if (Kc is None) != (Vc is None):
+        raise ValueError("Kc and Vc must be given together")
+    if Kc is not None:
+        _check_host(Kc, "Kc", Q.dtype, (B, Hkv, G, d))
+        _check_host(Vc, "Vc", Q.dtype, (B, Hkv, G, d))
+    prm = make_params(B, Hq, Hkv, N, d, g, w, _DTYPE[Q.dtype], scale, window_mode=window_mode,
+                      pool_mode=pool_mode)
+    need = int(lib.cca_prefill_host_workspace_size(ctypes.byref(prm)))
+    if workspace is None:
+        dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    if not workspace.is_cuda or workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"workspace must be a CUDA buffer of at least {need} bytes")
+    ptr = (lambda t: None if t is None else t.data_ptr())
+    with torch.cuda.device(workspace.device):
+        st = lib.cca_prefill_host(Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(), ptr(LSE), ptr(Kc),
+                                  ptr(Vc), ctypes.byref(prm), workspace.data_ptr(),
+                                  workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    if st != CCA_OK:
+        raise CcaError(st, "cca_prefill_host")
+    return O, LSE, Kc, Vc

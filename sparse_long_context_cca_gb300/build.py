@@ -11,7 +11,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libcca.so")
-SOURCES = ["cca_api.cu", "pool.cu", "attn_f32.cu", "attn_tc.cu", "decode.cu", "bwd.cu", "bwd_tc.cu"]
+SOURCES = ["cca_api.cu", "pool.cu", "attn_f32.cu", "attn_tc.cu", "decode.cu", "bwd.cu", "bwd_tc.cu", "host_pipeline.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include")]
 

@@ -186,6 +186,30 @@ int cca_pool_group(const void *q, const void *K, const void *V, void *Kc, void *
                                             static_cast<cudaStream_t>(stream)));
 }
 
+uint64_t cca_prefill_host_workspace_size(const cca_params_t *params) {
+    if (check_shape(params, true) != CCA_OK) return 0;
+    return cca::prefill_host_workspace_bytes(to_shape(params), params->dtype);
+}
+
+int cca_prefill_host(const void *hQ, const void *hK, const void *hV, void *hO, float *hLSE, void *hKc, void *hVc,
+                     const cca_params_t *params, void *workspace, uint64_t workspace_bytes, void *stream) {
+    int st = check_shape(params, true);
+    if (st != CCA_OK) return st;
+    const void *ptrs[5] = {hQ, hK, hV, hO, workspace};
+    for (const void *q : ptrs)
+        if (q == nullptr) return CCA_ERR_INVALID_ARG;
+    if (!aligned16(workspace)) return CCA_ERR_INVALID_ARG;
+    if ((hKc == nullptr) != (hVc == nullptr)) return CCA_ERR_INVALID_ARG;
+    if (params->dev_status != nullptr && (reinterpret_cast<uintptr_t>(params->dev_status) & 3u) != 0)
+        return CCA_ERR_INVALID_ARG;
+    if (params->dtype == CCA_BF16 && params->d != 128) return CCA_ERR_UNSUPPORTED;
+    const cca::Shape s = to_shape(params);
+    if (workspace_bytes < cca::prefill_host_workspace_bytes(s, params->dtype)) return CCA_ERR_INVALID_ARG;
+    if ((st = check_device()) != CCA_OK) return st;
+    return from_cuda(cca::launch_prefill_host(params->dtype, hQ, hK, hV, hO, hLSE, hKc, hVc, s, workspace,
+                                              params->dev_status, static_cast<cudaStream_t>(stream)));
+}
+
 const char *cca_status_string(int status) {
     switch (status) {
         case CCA_OK: return "ok";

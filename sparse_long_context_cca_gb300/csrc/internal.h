@@ -54,4 +54,10 @@ cudaError_t launch_attn_bwd_tc(const void *Q, const void *K, const void *V, cons
                                float *Dbuf, float *dKc, float *dVc, const Shape &s, int32_t *status,
                                cudaStream_t stream);
 
+// Prefill on host buffers, pipelined over slices of (batch, KV head) pairs (host_pipeline.cu).
+uint64_t prefill_host_workspace_bytes(const Shape &s, int dtype);
+cudaError_t launch_prefill_host(int dtype, const void *hQ, const void *hK, const void *hV, void *hO, float *hLSE,
+                                void *hKc, void *hVc, const Shape &s, void *workspace, int32_t *status,
+                                cudaStream_t stream);
+
 }  // namespace cca

@@ -140,3 +140,41 @@ def test_backward_rejects_bad_arguments(lib):
     assert lib.cca_prefill_bwd(*bad, ctypes.byref(prm), 0xC000, need, None) == api.CCA_ERR_INVALID_ARG
     prm_bad = api.make_params(1, 2, 2, 250, 128, 16, 32, api.CCA_BF16)
     assert lib.cca_prefill_bwd_workspace_size(ctypes.byref(prm_bad)) == 0
+
+
+def test_prefill_host_rejects_bad_arguments(lib):
+    prm = api.make_params(2, 4, 2, 256, 128, 16, 32, api.CCA_BF16)
+    need = lib.cca_prefill_host_workspace_size(ctypes.byref(prm))
+    ptrs = [0x1000 * (k + 1) for k in range(7)]
+    ws = 0x10000
+    # 4 (batch, KV head) pairs -> slices of one pair, three slice buffers of
+    # Q, O (2 query heads each), K, V, LSE, Kc, Vc, each rounded up to 256 bytes
+    up = lambda x: (x + 255) // 256 * 256
+    q, kv, c, lse = 2 * 256 * 128 * 2, 256 * 128 * 2, 16 * 128 * 2, 2 * 256 * 4
+    assert need == 3 * (2 * up(q) + 2 * up(kv) + up(lse) + 2 * up(c))
+    assert lib.cca_prefill_host(*ptrs, ctypes.byref(prm), ws, need - 1, None) == api.CCA_ERR_INVALID_ARG
+    for k in (0, 1, 2, 3):
+        bad = list(ptrs)
+        bad[k] = None
+        assert lib.cca_prefill_host(*bad, ctypes.byref(prm), ws, need, None) == api.CCA_ERR_INVALID_ARG
+    only_kc = list(ptrs)
+    only_kc[6] = None
+    assert lib.cca_prefill_host(*only_kc, ctypes.byref(prm), ws, need, None) == api.CCA_ERR_INVALID_ARG
+    assert lib.cca_prefill_host(*ptrs, ctypes.byref(prm), None, need, None) == api.CCA_ERR_INVALID_ARG
+    assert lib.cca_prefill_host(*ptrs, ctypes.byref(prm), ws + 8, need, None) == api.CCA_ERR_INVALID_ARG
+    prm64 = api.make_params(2, 4, 2, 256, 64, 16, 32, api.CCA_BF16)
+    need64 = lib.cca_prefill_host_workspace_size(ctypes.byref(prm64))
+    assert lib.cca_prefill_host(*ptrs, ctypes.byref(prm64), ws, need64, None) == api.CCA_ERR_UNSUPPORTED
+    bad_shape = api.make_params(2, 4, 2, 250, 128, 16, 32, api.CCA_BF16)
+    assert lib.cca_prefill_host_workspace_size(ctypes.byref(bad_shape)) == 0
+    # a large problem is cut into about eight slices and keeps three buffers
+    big = api.make_params(1, 32, 32, 32768, 128, 16, 1024, api.CCA_BF16)
+    per_pair = 2 * 32768 * 128 * 2 * 2 + 32768 * 4 + 2 * 2048 * 128 * 2
+    assert lib.cca_prefill_host_workspace_size(ctypes.byref(big)) == 3 * 4 * per_pair
+
+
+def test_prefill_host_binding_requires_cpu_tensors(lib):
+    import torch
+    Q = torch.zeros(1, 2, 32, 128, dtype=torch.bfloat16, device="meta")
+    with pytest.raises(ValueError):
+        api.cca_prefill_host(Q, Q, Q, 16, 8)
