@@ -18,8 +18,9 @@
 // Roles (320 threads):
 //   warp 0       TMA producer: the two Q tiles of an item, then K(t), V(t) for
 //                every tile t into a ring of NS 32 KB slots (128-byte swizzle);
-//   warp 1       MMA issuer (one thread): S_h = Q_h K^T (both operands in shared
-//                memory) and O_h += P_h V (P_h in tensor memory, V MN-major);
+//   warp 1       MMA issuer (the whole warp, one elected lane issues): S_h = Q_h K^T
+//                (both operands in shared memory) and O_h += P_h V (P_h in tensor
+//                memory, V MN-major);
 //   warps 2..5   softmax + epilogue of half A, warps 6..9 the same for half B.
 //                A warp may only touch TMEM lanes 32*(warp%4) .. +31, so each
 //                group of four consecutive warps covers the 128 lanes once;
@@ -166,6 +167,11 @@ __device__ __forceinline__ Item make_item(const Params &p, int k) {
     return it;
 }
 
+// Parity of the FULL barrier of the ring slot holding K for ring index u (u even).
+// Only K slots complete a FULL barrier (the tile's V copy completes the same one),
+// and with NS odd an even u reaches each slot once every 2*NS indices.
+__device__ __forceinline__ uint32_t k_full_parity(uint32_t u) { return (u / (2 * NS)) & 1; }
+
 __device__ __forceinline__ void report_timeout(const Params &p) {
     if (p.status != nullptr) atomicCAS(p.status, 0, static_cast<int32_t>(-4));
 }
@@ -194,9 +200,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         for (int h = 0; h < 2; ++h) {
             ptx::mbar_init(bar(B_SFULL + h), 1);
-            ptx::mbar_init(bar(B_PFULL + h), 128);
+            ptx::mbar_init(bar(B_PFULL + h), 4);  // one arrive per softmax warp
             ptx::mbar_init(bar(B_PVDONE + h), 1);
-            ptx::mbar_init(bar(B_OFREE + h), 128);
+            ptx::mbar_init(bar(B_OFREE + h), 4);
         }
         ptx::mbar_init(bar(B_DRAIN), 1);
         *abort_flag = 0;
@@ -235,34 +241,44 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         ptx::tma_load_3d(&tmQ, bar(B_QFULL), dst + HALF_BYTES, 64, row0, it.bh);
                     }
                 }
-                for (int t = 0; ok && t < it.T; ++t) {
+                for (int t = 0; ok && t < it.T; ++t, u += 2) {
                     const bool core = t < it.Tc;
                     const int y = core ? t * BN : it.lo0 + (t - it.Tc) * BN;
-                    for (int kv = 0; kv < 2; ++kv, ++u) {
-                        const int slot = u % NS;
-                        if (!ptx::wait_bounded(bar(B_EMPTY + slot), ((u / NS) & 1) ^ 1, abort_flag, lim)) {
-                            ok = false;
-                            break;
-                        }
-                        const void *map = core ? (kv ? (const void *)&tmVc : (const void *)&tmKc)
-                                               : (kv ? (const void *)&tmV : (const void *)&tmK);
-                        const uint32_t dst = base + OFF_RING + slot * TILE_BYTES;
-                        ptx::mbar_arrive_expect_tx(bar(B_FULL + slot), TILE_BYTES);
-                        ptx::tma_load_3d(map, bar(B_FULL + slot), dst, 0, y, it.kvz);
-                        ptx::tma_load_3d(map, bar(B_FULL + slot), dst + HALF_BYTES, 64, y, it.kvz);
+                    // K(t) goes to ring slot u % NS, V(t) to the next one; both copies
+                    // complete the K slot's FULL barrier (u is even, see k_full_parity)
+                    const int ks = u % NS, vs = (u + 1) % NS;
+                    if (!ptx::wait_bounded(bar(B_EMPTY + ks), ((u / NS) & 1) ^ 1, abort_flag, lim) ||
+                        !ptx::wait_bounded(bar(B_EMPTY + vs), (((u + 1) / NS) & 1) ^ 1, abort_flag, lim)) {
+                        ok = false;
+                        break;
                     }
+                    const uint32_t full = bar(B_FULL + ks);
+                    const uint32_t kdst = base + OFF_RING + ks * TILE_BYTES;
+                    const uint32_t vdst = base + OFF_RING + vs * TILE_BYTES;
+                    const void *mk = core ? (const void *)&tmKc : (const void *)&tmK;
+                    const void *mv = core ? (const void *)&tmVc : (const void *)&tmV;
+                    ptx::mbar_arrive_expect_tx(full, 2 * TILE_BYTES);
+                    ptx::tma_load_3d(mk, full, kdst, 0, y, it.kvz);
+                    ptx::tma_load_3d(mk, full, kdst + HALF_BYTES, 64, y, it.kvz);
+                    ptx::tma_load_3d(mv, full, vdst, 0, y, it.kvz);
+                    ptx::tma_load_3d(mv, full, vdst + HALF_BYTES, 64, y, it.kvz);
                 }
             }
             if (*abort_flag) {
                 // Let the copies already issued land before the CTA exits.
                 volatile int never = 0;
-                for (uint32_t v = u > NS ? u - NS : 0; v < u; ++v)
-                    ptx::wait_bounded(bar(B_FULL + v % NS), (v / NS) & 1, &never, lim);
+                for (uint32_t v = u > 2 * NS ? u - 2 * NS : 0; v < u; v += 2)
+                    ptx::wait_bounded(bar(B_FULL + v % NS), k_full_parity(v), &never, lim);
                 if (!p.skip_q_load && n_iter > 0)
                     ptx::wait_bounded(bar(B_QFULL), (n_iter - 1) & 1, &never, lim);
             }
-        } else if (warp == 1 && lane == 0) {
+        } else if (warp == 1) {
             // ------------------------------------------------------------ MMA issuer
+            // The whole warp runs the issuer with identical values in every lane; the
+            // MMAs and commits are issued by one elected lane.
+            auto wwait = [&](uint32_t b, uint32_t parity) -> bool {
+                return __all_sync(0xffffffffu, ptx::wait_bounded(b, parity, abort_flag, lim));
+            };
             uint32_t ubase = 0;
             int n_iter = 0;
             uint32_t kpend = 0;  // pending S issues per ring slot, 2 bits per slot
@@ -276,7 +292,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             bool ok = true;
             for (int k = blockIdx.x; ok && k < p.n_items; k += gridDim.x, ++n_iter) {
                 const Item it = make_item(p, k);
-                if (!ptx::wait_bounded(bar(B_QFULL), n_iter & 1, abort_flag, lim)) break;
+                if (!wwait(bar(B_QFULL), n_iter & 1)) break;
                 int s_left = half_count(it.hA) + half_count(it.hB);
                 // S_h = Q_h K(t)^T into S_h.  The first user of a ring slot waits for the copy.
                 auto issue_s = [&](int h, int t) -> bool {
@@ -284,17 +300,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const int slot = uk % NS;
                     uint32_t pend = (kpend >> (2 * slot)) & 3u;
                     if (pend == 0) {
-                        if (!ptx::wait_bounded(bar(B_FULL + slot), (uk / NS) & 1, abort_flag, lim)) return false;
+                        // the tile's first S: wait for its K and V copies
+                        if (!wwait(bar(B_FULL + slot), k_full_parity(uk))) return false;
                         pend = (half_uses(it.hA, it.Tc, t) ? 1u : 0u) + (half_uses(it.hB, it.Tc, t) ? 1u : 0u);
                     }
                     ptx::tc_fence_after();
-                    ptx::mma_ss_k128(tmem + TM_S + h * BN, h ? dq1 : dq0, dk0 + static_cast<uint64_t>(slot) * (TILE_BYTES >> 4),
+                    ptx::mma_ss_k128_warp(tmem + TM_S + h * BN, h ? dq1 : dq0, dk0 + static_cast<uint64_t>(slot) * (TILE_BYTES >> 4),
                                      IDESC_QK, 0u);
-                    ptx::tc_commit(bar(B_SFULL + h));
+                    ptx::tc_commit_warp(bar(B_SFULL + h));
                     --pend;
                     kpend = (kpend & ~(3u << (2 * slot))) | (pend << (2 * slot));
-                    if (pend == 0) ptx::tc_commit(bar(B_EMPTY + slot));
-                    if (--s_left == 0) ptx::tc_commit(bar(B_QFREE));
+                    if (pend == 0) ptx::tc_commit_warp(bar(B_EMPTY + slot));
+                    if (--s_left == 0) ptx::tc_commit_warp(bar(B_QFREE));
                     return true;
                 };
                 // Prologue: first S of each half, earliest tile first, so that the issuer
@@ -309,30 +326,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 bool first_pv[2] = {true, true};
                 for (int t = 0; ok && t < it.T; ++t) {
+                    // V(t) has landed: the tile's first S waited for its K and V together
                     const uint32_t uv = ubase + 2 * t + 1;
                     const int vslot = uv % NS;
-                    if (!ptx::wait_bounded(bar(B_FULL + vslot), (uv / NS) & 1, abort_flag, lim)) {
-                        ok = false;
-                        break;
-                    }
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {  // unrolled: per-half counters stay in registers
                         const Half &x = it.half(h);
                         if (!half_uses(x, it.Tc, t)) continue;
-                        if (!ptx::wait_bounded(bar(B_PFULL + h), pf_cnt[h] & 1, abort_flag, lim)) {
+                        if (!wwait(bar(B_PFULL + h), pf_cnt[h] & 1)) {
                             ok = false;
                             break;
                         }
                         ++pf_cnt[h];
                         if (first_pv[h]) {
                             // the epilogue of this half's previous item must have read O_h
-                            if (!ptx::wait_bounded(bar(B_OFREE + h), (n_half[h] & 1) ^ 1, abort_flag, lim)) {
+                            if (!wwait(bar(B_OFREE + h), (n_half[h] & 1) ^ 1)) {
                                 ok = false;
                                 break;
                             }
                         }
                         ptx::tc_fence_after();
-                        ptx::mma_ts_k128(tmem + TM_O + h * HD, tmem + TM_S + h * BN,
+                        ptx::mma_ts_k128_warp(tmem + TM_O + h * HD, tmem + TM_S + h * BN,
                                          dv0 + static_cast<uint64_t>(vslot) * (TILE_BYTES >> 4), IDESC_PV,
                                          first_pv[h] ? 0u : 1u);
                         first_pv[h] = false;
@@ -343,18 +357,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                 break;
                             }
                         } else {
-                            ptx::tc_commit(bar(B_PVDONE + h));
+                            ptx::tc_commit_warp(bar(B_PVDONE + h));
                         }
                     }
                     if (!ok) break;
-                    ptx::tc_commit(bar(B_EMPTY + vslot));
+                    ptx::tc_commit_warp(bar(B_EMPTY + vslot));
                 }
                 ubase += 2 * it.T;
                 n_half[0] += it.hA.valid ? 1 : 0;
                 n_half[1] += it.hB.valid ? 1 : 0;
             }
             // Whatever was issued must complete before tensor memory is freed.
-            ptx::tc_commit(bar(B_DRAIN));
+            ptx::tc_commit_warp(bar(B_DRAIN));
             volatile int never = 0;
             ptx::wait_bounded(bar(B_DRAIN), 0, &never, lim);
         }
@@ -489,7 +503,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 ptx::tmem_wait_st();
                 ptx::tc_fence_before();
-                ptx::mbar_arrive(bar(B_PFULL + h));
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar(B_PFULL + h));
             }
             if (!ok) break;
             // ---- epilogue: O_h / l -> bf16, LSE
@@ -521,7 +536,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
             ptx::tc_fence_before();
-            ptx::mbar_arrive(bar(B_OFREE + h));
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar(B_OFREE + h));
             if (valid) p.LSE[static_cast<int64_t>(it.bh) * p.N + i] = (m + __log2f(l)) * 0.6931471805599453f;
             ++n_done;
         }

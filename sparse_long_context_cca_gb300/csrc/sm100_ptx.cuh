@@ -194,6 +194,68 @@ __device__ __forceinline__ void mma_ts_k128(uint32_t d_tmem, uint32_t a_tmem, ui
         : "memory");
 }
 
+// Warp-collective forms: the whole warp executes them with warp-uniform operands and
+// elect.sync picks the one lane that issues.  Issuing from a full warp keeps the
+// descriptors in uniform registers, which roughly halves the issue cost per MMA
+// compared with a branch that only one lane enters.
+__device__ __forceinline__ void tc_commit_warp(uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void mma_ss_k128_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t.reg .b64 a, b;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+        "add.s64 a, %1, 2;\n\tadd.s64 b, %2, 2;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, 1;\n\t"
+        "add.s64 a, %1, 4;\n\tadd.s64 b, %2, 4;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, 1;\n\t"
+        "add.s64 a, %1, 6;\n\tadd.s64 b, %2, 6;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, 1;\n\t"
+        "add.s64 a, %1, 1024;\n\tadd.s64 b, %2, 1024;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, 1;\n\t"
+        "add.s64 a, %1, 1026;\n\tadd.s64 b, %2, 1026;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, 1;\n\t"
+        "add.s64 a, %1, 1028;\n\tadd.s64 b, %2, 1028;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, 1;\n\t"
+        "add.s64 a, %1, 1030;\n\tadd.s64 b, %2, 1030;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, 1;\n\t"
+        "}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_ts_k128_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t.reg .b32 a;\n\t.reg .b64 b;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+        "add.u32 a, %1, 8;\n\tadd.s64 b, %2, 128;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, 1;\n\t"
+        "add.u32 a, %1, 16;\n\tadd.s64 b, %2, 256;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, 1;\n\t"
+        "add.u32 a, %1, 24;\n\tadd.s64 b, %2, 384;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, 1;\n\t"
+        "add.u32 a, %1, 32;\n\tadd.s64 b, %2, 512;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, 1;\n\t"
+        "add.u32 a, %1, 40;\n\tadd.s64 b, %2, 640;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, 1;\n\t"
+        "add.u32 a, %1, 48;\n\tadd.s64 b, %2, 768;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, 1;\n\t"
+        "add.u32 a, %1, 56;\n\tadd.s64 b, %2, 896;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, 1;\n\t"
+        "}"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Thread t of the warp reads TMEM lane (warp quarter base + t), 32 consecutive
 // 32-bit columns starting at taddr's column.  Values are valid only after tmem_wait_ld.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
