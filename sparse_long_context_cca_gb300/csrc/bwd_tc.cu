@@ -218,14 +218,17 @@ __global__ void __launch_bounds__(128, 1)
         const int y0 = core ? tt * BT : lo0 + (tt - Tc) * BT;
         const uint32_t sK = sm.tile[2 + 2 * (tt & 1)], sV = sm.tile[3 + 2 * (tt & 1)];
         if (!(ok = wait(ptx::smem_addr(&sm.bars[1 + (tt & 1)]), (tt >> 1) & 1))) break;
-        if (t == 0) {
-            if (tt + 1 < T) issue_kv(tt + 1);  // its buffer was last read by tile tt-1's finished MMAs
+        if (warp == 0) {
+            // queued behind the previous tile's dQ MMA, which still reads dS from S
             ptx::tc_fence_after();
-            ptx::mma_ss_k128(tmem + 0, dQd, ptx::smem_desc_sw128(sK, 16, 1024), IDESC_SS, 0u);     // S  = Q K^T
-            ptx::mma_ss_k128(tmem + 128, ddOd, ptx::smem_desc_sw128(sV, 16, 1024), IDESC_SS, 0u);  // dP = dO V^T
-            ptx::tc_commit(b_mma);
+            ptx::mma_ss_k128_warp(tmem + 0, dQd, ptx::smem_desc_sw128(sK, 16, 1024), IDESC_SS, 0u);     // S  = Q K^T
+            ptx::mma_ss_k128_warp(tmem + 128, ddOd, ptx::smem_desc_sw128(sV, 16, 1024), IDESC_SS, 0u);  // dP = dO V^T
+            ptx::tc_commit_warp(b_mma);
         }
         if (!(ok = wait(b_mma, mma_phase++ & 1))) break;
+        // MMAs complete in issue order, so the previous tile's dQ MMA is done: its K/V
+        // buffer takes the next tile's copy
+        if (t == 0 && tt + 1 < T) issue_kv(tt + 1);
         ptx::tc_fence_after();
         // dS = P (dP - D) on this row's visible columns; bf16 pairs written over S
         int c_lo = 0, c_hi = BT - 1;
@@ -261,13 +264,15 @@ __global__ void __launch_bounds__(128, 1)
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         __syncthreads();
-        if (t == 0) {
+        if (warp == 0) {
             ptx::tc_fence_after();
-            ptx::mma_ts_k128(tmem + 256, tmem + 0, ptx::smem_desc_sw128(sK, HALF_BYTES, 1024), IDESC_TS,
-                             tt > 0 ? 1u : 0u);  // dQ += dS K
-            ptx::tc_commit(b_mma);
+            ptx::mma_ts_k128_warp(tmem + 256, tmem + 0, ptx::smem_desc_sw128(sK, HALF_BYTES, 1024), IDESC_TS,
+                                  tt > 0 ? 1u : 0u);  // dQ += dS K, completion covered by the next wait
         }
-        if (!(ok = wait(b_mma, mma_phase++ & 1))) break;
+    }
+    if (ok) {
+        if (warp == 0) ptx::tc_commit_warp(b_mma);
+        ok = wait(b_mma, mma_phase++ & 1);
     }
     if (ok) {
         ptx::tc_fence_after();
@@ -358,14 +363,16 @@ __global__ void __launch_bounds__(128, 1)
         s_lse[t] = iq < p.N ? p.LSE[static_cast<int64_t>(bh) * p.N + iq] * LOG2E : 0.f;
         s_D[t] = iq < p.N ? p.Dbuf[static_cast<int64_t>(bh) * p.N + iq] : 0.f;
         if (!(ok = wait(ptx::smem_addr(&sm.bars[1 + (it & 1)]), (it >> 1) & 1))) break;
-        if (t == 0) {
-            if (it + 1 < n_it) issue_q(it + 1);  // its buffer was last read by pair it-1's finished MMAs
+        if (warp == 0) {
+            // queued behind the previous pair's dV/dK MMAs, which still read P^T and dS^T
             ptx::tc_fence_after();
-            ptx::mma_ss_k128(tmem + 0, dKk, ptx::smem_desc_sw128(sQ, 16, 1024), IDESC_SS, 0u);     // S^T  = K Q^T
-            ptx::mma_ss_k128(tmem + 128, dVk, ptx::smem_desc_sw128(sdO, 16, 1024), IDESC_SS, 0u);  // dP^T = V dO^T
-            ptx::tc_commit(b_mma);
+            ptx::mma_ss_k128_warp(tmem + 0, dKk, ptx::smem_desc_sw128(sQ, 16, 1024), IDESC_SS, 0u);     // S^T  = K Q^T
+            ptx::mma_ss_k128_warp(tmem + 128, dVk, ptx::smem_desc_sw128(sdO, 16, 1024), IDESC_SS, 0u);  // dP^T = V dO^T
+            ptx::tc_commit_warp(b_mma);
         }
         if (!(ok = wait(b_mma, mma_phase++ & 1))) break;
+        // in-order completion: the previous pair's MMAs are done, its Q/dO buffer is free
+        if (t == 0 && it + 1 < n_it) issue_q(it + 1);
         ptx::tc_fence_after();
         // this key's visible query columns [q_lo, q_hi] of the tile
         int q_lo, q_hi;
@@ -410,16 +417,18 @@ __global__ void __launch_bounds__(128, 1)
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         __syncthreads();
-        if (t == 0) {
+        if (warp == 0) {
             ptx::tc_fence_after();
             const uint32_t acc = it > 0 ? 1u : 0u;
-            ptx::mma_ts_k128(tmem + 384, tmem + 0, ptx::smem_desc_sw128(sdO, HALF_BYTES, 1024), IDESC_TS,
-                             acc);  // dV += P^T dO
-            ptx::mma_ts_k128(tmem + 256, tmem + 128, ptx::smem_desc_sw128(sQ, HALF_BYTES, 1024), IDESC_TS,
-                             acc);  // dK += dS^T Q
-            ptx::tc_commit(b_mma);
+            ptx::mma_ts_k128_warp(tmem + 384, tmem + 0, ptx::smem_desc_sw128(sdO, HALF_BYTES, 1024), IDESC_TS,
+                                  acc);  // dV += P^T dO
+            ptx::mma_ts_k128_warp(tmem + 256, tmem + 128, ptx::smem_desc_sw128(sQ, HALF_BYTES, 1024), IDESC_TS,
+                                  acc);  // dK += dS^T Q; completion covered by the next wait
         }
-        if (!(ok = wait(b_mma, mma_phase++ & 1))) break;
+    }
+    if (ok && n_it > 0) {
+        if (warp == 0) ptx::tc_commit_warp(b_mma);
+        ok = wait(b_mma, mma_phase++ & 1);
     }
     if (ok) {
         const bool mine = m < n_keys;
