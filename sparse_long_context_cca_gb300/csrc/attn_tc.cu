@@ -57,7 +57,7 @@ constexpr int NUM_THREADS = 320;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_S = 0;    // S_h at h * 128
 constexpr uint32_t TM_O = 256;  // O_h at 256 + h * 128
-constexpr float LAZY_RESCALE_LOG2 = 8.0f;  // keep a stale max while it is within 2^8
+constexpr float LAZY_RESCALE_LOG2 = 16.0f;  // keep a stale max while it is within 2^16
 
 constexpr uint32_t IDESC_QK = ptx::idesc_bf16_f32(BM, BN, 0, 0);  // Q, K both K-major
 constexpr uint32_t IDESC_PV = ptx::idesc_bf16_f32(BM, HD, 0, 1);  // P (TMEM), V MN-major
