@@ -17,13 +17,14 @@
 extern "C" {
 #endif
 
-/* Per-wait time limit in nanoseconds for later bf16 attention launches
- * (default 1e9, i.e. one second). */
+/* Per-wait time limit in nanoseconds for later bf16 tensor-core launches,
+ * forward and backward (default 1e9, i.e. one second). */
 void cca_test_set_wait_limit_ns(unsigned long long ns);
 
 /* on != 0: later bf16 attention launches never load the query tile, so the
- * tensor-core issuer's first wait runs out and the kernel reports a time-out.
- * on == 0 restores normal operation. */
+ * tensor-core issuer's first wait runs out and the kernel reports a time-out;
+ * the tensor-core backward kernels issue no copies at all, so their first wait
+ * runs out the same way.  on == 0 restores normal operation. */
 void cca_test_skip_q_load(int on);
 
 #ifdef __cplusplus

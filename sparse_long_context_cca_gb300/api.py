@@ -277,8 +277,11 @@ def cca_pool_group(q, K, V, Kc, Vc, j: int, g: int, scale: float = 0.0, stream=N
 
 
 def cca_prefill_bwd(Q, K, V, Kc, Vc, O, LSE, dO, g: int, w: int, scale: float = 0.0, pool_mode: int = 0,
-                    window_mode: int = 0, dQ=None, dK=None, dV=None, workspace=None, stream=None):
-    """Gradients (dQ, dK, dV), fp32, of sum(dO * O) for CCA prefill (pooling + attention)."""
+                    window_mode: int = 0, dQ=None, dK=None, dV=None, workspace=None, stream=None,
+                    dev_status=None):
+    """Gradients (dQ, dK, dV), fp32, of sum(dO * O) for CCA prefill (pooling + attention).
+    dev_status: optional int32 CUDA tensor of one element that receives CCA_ERR_TIMEOUT
+    if a tensor-core kernel gives up waiting."""
     lib = load_library()
     B, Hq, Hkv, N, d = _dims(Q, K)
     G = N // g if g > 0 else 0
@@ -293,7 +296,12 @@ def cca_prefill_bwd(Q, K, V, Kc, Vc, O, LSE, dO, g: int, w: int, scale: float = 
     _check(dQ, "dQ", torch.float32, (B, Hq, N, d))
     _check(dK, "dK", torch.float32, (B, Hkv, N, d))
     _check(dV, "dV", torch.float32, (B, Hkv, N, d))
-    prm = make_params(B, Hq, Hkv, N, d, g, w, _DTYPE[Q.dtype], scale, window_mode=window_mode, pool_mode=pool_mode)
+    status_ptr = None
+    if dev_status is not None:
+        _check(dev_status, "dev_status", torch.int32, (1,))
+        status_ptr = dev_status.data_ptr()
+    prm = make_params(B, Hq, Hkv, N, d, g, w, _DTYPE[Q.dtype], scale, status_ptr, window_mode=window_mode,
+                      pool_mode=pool_mode)
     need = int(lib.cca_prefill_bwd_workspace_size(ctypes.byref(prm)))
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=Q.device)

@@ -37,6 +37,7 @@
 namespace cca {
 
 extern unsigned long long g_wait_limit_ns;
+extern int g_skip_q_load;
 
 namespace {
 
@@ -62,6 +63,7 @@ struct BwdTcParams {
     float *dKc, *dVc;     // fp32 core-token gradients (workspace)
     int32_t *status;
     unsigned long long wait_limit_ns;
+    int skip_loads;  // test hook: issue no copies, so the first wait runs out
 };
 
 __device__ __forceinline__ int lo_of(int i, int w) { return i - w + 1 > 0 ? i - w + 1 : 0; }
@@ -182,7 +184,7 @@ __global__ void __launch_bounds__(128, 1)
         load_tile(core ? (const void *)&tmKc : (const void *)&tmK, bar, sm.tile[2 + 2 * (tt & 1)], y0, kvz);
         load_tile(core ? (const void *)&tmVc : (const void *)&tmV, bar, sm.tile[3 + 2 * (tt & 1)], y0, kvz);
     };
-    if (t == 0) {
+    if (t == 0 && !p.skip_loads) {
         ptx::mbar_arrive_expect_tx(b_qd, 2 * TILE_BYTES);
         load_tile(&tmQ, b_qd, sQ, i0, bh);
         load_tile(&tmdO, b_qd, sdO, i0, bh);
@@ -228,7 +230,7 @@ __global__ void __launch_bounds__(128, 1)
         if (!(ok = wait(b_mma, mma_phase++ & 1))) break;
         // MMAs complete in issue order, so the previous tile's dQ MMA is done: its K/V
         // buffer takes the next tile's copy
-        if (t == 0 && tt + 1 < T) issue_kv(tt + 1);
+        if (t == 0 && tt + 1 < T && !p.skip_loads) issue_kv(tt + 1);
         ptx::tc_fence_after();
         // dS = P (dP - D) on this row's visible columns; bf16 pairs written over S
         int c_lo = 0, c_hi = BT - 1;
@@ -345,7 +347,7 @@ __global__ void __launch_bounds__(128, 1)
         load_tile(&tmQ, bar, sm.tile[2 + 2 * (it & 1)], i0_of(it), bh_of(it));
         load_tile(&tmdO, bar, sm.tile[3 + 2 * (it & 1)], i0_of(it), bh_of(it));
     };
-    if (t == 0) {
+    if (t == 0 && !p.skip_loads) {
         ptx::mbar_arrive_expect_tx(b_kv, 2 * TILE_BYTES);
         load_tile(core ? (const void *)&tmKc : (const void *)&tmK, b_kv, sK, y0, bk);
         load_tile(core ? (const void *)&tmVc : (const void *)&tmV, b_kv, sV, y0, bk);
@@ -372,7 +374,7 @@ __global__ void __launch_bounds__(128, 1)
         }
         if (!(ok = wait(b_mma, mma_phase++ & 1))) break;
         // in-order completion: the previous pair's MMAs are done, its Q/dO buffer is free
-        if (t == 0 && it + 1 < n_it) issue_q(it + 1);
+        if (t == 0 && it + 1 < n_it && !p.skip_loads) issue_q(it + 1);
         ptx::tc_fence_after();
         // this key's visible query columns [q_lo, q_hi] of the tile
         int q_lo, q_hi;
@@ -521,6 +523,7 @@ cudaError_t launch_attn_bwd_tc(const void *Q, const void *K, const void *V, cons
     p.dVc = dVc;
     p.status = status;
     p.wait_limit_ns = g_wait_limit_ns;
+    p.skip_loads = g_skip_q_load;
     const unsigned n_qt = static_cast<unsigned>((s.N + BT - 1) / BT);
     bwd_dq_tc_kernel<<<n_qt * static_cast<unsigned>(qh), 128, SMEM_BYTES, stream>>>(mQ, mdO, mK, mV, mKc, mVc, p);
     e = cudaGetLastError();
