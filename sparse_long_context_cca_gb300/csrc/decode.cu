@@ -74,7 +74,7 @@ struct DecodeArgs {
 
 // Partials: ws[((b*Hq + h) * MAX_SPLITS + s) * (D + 2) + {0..D-1: o, D: m, D+1: l}]
 template <typename T, int D, int R>
-__global__ void __launch_bounds__(DEC_WARPS * 32) decode_split_kernel(const T *__restrict__ Q, const T *__restrict__ K,
+__global__ void __launch_bounds__(DEC_WARPS * 32, R == 1 ? 4 : 1) decode_split_kernel(const T *__restrict__ Q, const T *__restrict__ K,
                                                                       const T *__restrict__ V,
                                                                       const T *__restrict__ Kc,
                                                                       const T *__restrict__ Vc, float *__restrict__ ws,
@@ -117,8 +117,9 @@ __global__ void __launch_bounds__(DEC_WARPS * 32) decode_split_kernel(const T *_
     const T *kr = K + static_cast<int64_t>(bk) * a.Ncap * D + cl * E;
     const T *vr = V + static_cast<int64_t>(bk) * a.Ncap * D + cl * E;
 
-    for (int xb = wx0; xb < wx1; xb += RPI * UNROLL) {
-        uint4 kk[UNROLL], vv[UNROLL];
+    // Software-pipelined over batches of RPI * UNROLL keys: the next batch's loads are
+    // in flight while the current one is scored (two register sets, used alternately).
+    auto load_batch = [&](int xb, uint4 (&kk)[UNROLL], uint4 (&vv)[UNROLL]) {
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
             const int x = xb + u * RPI + sub;
@@ -131,12 +132,16 @@ __global__ void __launch_bounds__(DEC_WARPS * 32) decode_split_kernel(const T *_
                 kk[u] = vv[u] = make_uint4(0, 0, 0, 0);
             }
         }
+    };
+    // One online-softmax update per batch: all logits first, then one max and one
+    // rescale per query head, then the batch's exponentials and weighted values.
+    auto score_batch = [&](int xb, const uint4 (&kk)[UNROLL], const uint4 (&vv)[UNROLL]) {
+        float xl[UNROLL][R];
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
             const bool valid = xb + u * RPI + sub < wx1;
-            float kf[E], vf[E];
+            float kf[E];
             VT::unpack(kk[u], kf);
-            VT::unpack(vv[u], vf);
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 float dot = 0.f;
@@ -144,18 +149,45 @@ __global__ void __launch_bounds__(DEC_WARPS * 32) decode_split_kernel(const T *_
                 for (int e = 0; e < E; ++e) dot = fmaf(q[r][e], kf[e], dot);
 #pragma unroll
                 for (int off = LPR / 2; off > 0; off >>= 1) dot += __shfl_xor_sync(kFull, dot, off);
-                if (valid) {
-                    const float xl = dot * a.scale_log2;
-                    const float mn = fmaxf(m[r], xl);
-                    const float corr = ptx::ex2(m[r] - mn);
-                    const float p = ptx::ex2(xl - mn);
-                    l[r] = l[r] * corr + p;
-#pragma unroll
-                    for (int e = 0; e < E; ++e) o[r][e] = fmaf(p, vf[e], o[r][e] * corr);
-                    m[r] = mn;
-                }
+                xl[u][r] = valid ? dot * a.scale_log2 : -INFINITY;
             }
         }
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            float mb = xl[0][r];
+#pragma unroll
+            for (int u = 1; u < UNROLL; ++u) mb = fmaxf(mb, xl[u][r]);
+            const float mn = fmaxf(m[r], mb);
+            if (mn == -INFINITY) continue;  // nothing visible yet in this lane group
+            const float corr = ptx::ex2(m[r] - mn);  // 0 when m was -inf
+            l[r] *= corr;
+#pragma unroll
+            for (int e = 0; e < E; ++e) o[r][e] *= corr;
+            m[r] = mn;
+        }
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            float vf[E];
+            VT::unpack(vv[u], vf);
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                // masked keys (and lane groups that have seen nothing yet) add nothing
+                const float p = xl[u][r] == -INFINITY ? 0.f : ptx::ex2(xl[u][r] - m[r]);
+                l[r] += p;
+#pragma unroll
+                for (int e = 0; e < E; ++e) o[r][e] = fmaf(p, vf[e], o[r][e]);
+            }
+        }
+    };
+    constexpr int STEP = RPI * UNROLL;
+    uint4 k0[UNROLL], v0[UNROLL], k1[UNROLL], v1[UNROLL];
+    if (wx0 < wx1) load_batch(wx0, k0, v0);
+    for (int xb = wx0; xb < wx1; xb += 2 * STEP) {
+        if (xb + STEP < wx1) load_batch(xb + STEP, k1, v1);
+        score_batch(xb, k0, v0);
+        if (xb + STEP >= wx1) break;
+        if (xb + 2 * STEP < wx1) load_batch(xb + 2 * STEP, k0, v0);
+        score_batch(xb + STEP, k1, v1);
     }
     // merge the RPI key subgroups of the warp (lanes with the same column chunk)
 #pragma unroll
@@ -210,18 +242,37 @@ __global__ void __launch_bounds__(DEC_WARPS * 32) decode_split_kernel(const T *_
 template <typename T, int D>
 __global__ void __launch_bounds__(D) decode_combine_kernel(const float *__restrict__ ws, T *__restrict__ O,
                                                            float *__restrict__ LSE, int splits) {
+    static_assert(D >= MAX_SPLITS, "one thread per split for the weights");
+    constexpr int NW = D / 32;
+    __shared__ float sh_f[MAX_SPLITS];
+    __shared__ float sh_wm[NW], sh_wl[NW];
     const int bh = blockIdx.x;
-    const int c = threadIdx.x;
+    const int c = threadIdx.x, lane = c & 31, warp = c >> 5;
     const float *base = ws + static_cast<int64_t>(bh) * MAX_SPLITS * (D + 2);
-    float mx = -INFINITY;
-    for (int s = 0; s < splits; ++s) mx = fmaxf(mx, base[s * (D + 2) + D]);
-    float acc = 0.f, lsum = 0.f;
-    for (int s = 0; s < splits; ++s) {
-        const float ms = base[s * (D + 2) + D];
-        const float f = (ms == -INFINITY) ? 0.f : ptx::ex2(ms - mx);
-        acc += base[s * (D + 2) + c] * f;
-        lsum += base[s * (D + 2) + D + 1] * f;
-    }
+    // split weights in parallel: thread s reads split s's (max, sum)
+    const float ms = c < splits ? base[c * (D + 2) + D] : -INFINITY;
+    const float ls = c < splits ? base[c * (D + 2) + D + 1] : 0.f;
+    float mx = ms;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
+    if (lane == 0) sh_wm[warp] = mx;
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < NW; ++w) mx = fmaxf(mx, sh_wm[w]);
+    const float f = (ms == -INFINITY) ? 0.f : ptx::ex2(ms - mx);
+    if (c < MAX_SPLITS) sh_f[c] = f;
+    float lw = ls * f;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) lw += __shfl_xor_sync(kFull, lw, off);
+    if (lane == 0) sh_wl[warp] = lw;
+    __syncthreads();
+    float lsum = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) lsum += sh_wl[w];
+    // column c: independent loads of every split's partial, unrolled so they overlap
+    float acc = 0.f;
+#pragma unroll 8
+    for (int s = 0; s < splits; ++s) acc = fmaf(base[s * (D + 2) + c], sh_f[s], acc);
     const float val = acc / lsum;
     if constexpr (sizeof(T) == 2) {
         O[static_cast<int64_t>(bh) * D + c] = __float2bfloat16_rn(val);
