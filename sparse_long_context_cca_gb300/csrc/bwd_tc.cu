@@ -3,8 +3,10 @@
 // Context Language Modeling" (Method section), with P recomputed from the
 // forward's LSE.  Notation as in bwd.cu: dS = P (dO.v - D), D_i = dO_i . O_i.
 //
-// Two kernels, 128 threads each; thread 0 issues the TMA copies and the
-// tcgen05.mma instructions, thread t owns TMEM lane t for the element-wise work.
+// Two kernels, 256 threads each.  Thread 0 issues the TMA copies, warp 0 the
+// tcgen05.mma instructions (one elected lane).  For the element-wise work warps w
+// and w + 4 share TMEM lanes 32*(w%4)..+31 and split the 128 columns, 64 each.
+// The fp32 results leave through shared memory and tiled TMA stores.
 //
 //  dq kernel, one 128-row query tile of one (b, h) per CTA, over the same key
 //  tiles as the forward (cores, then the band):
@@ -42,6 +44,7 @@ extern int g_skip_q_load;
 namespace {
 
 constexpr int BT = 128;  // rows per tile (queries or keys)
+constexpr int NTHREADS = 256;
 constexpr int HD = 128;
 constexpr uint32_t TILE_BYTES = BT * HD * 2;
 constexpr uint32_t HALF_BYTES = TILE_BYTES / 2;
@@ -58,9 +61,7 @@ struct BwdTcParams {
     float tau;
     const float *LSE;
     const __nv_bfloat16 *O, *dO;
-    float *Dbuf;          // written by the dq kernel, read by the dkv kernel
-    float *dQ, *dK, *dV;  // fp32 outputs
-    float *dKc, *dVc;     // fp32 core-token gradients (workspace)
+    float *Dbuf;  // written by the dq kernel, read by the dkv kernel
     int32_t *status;
     unsigned long long wait_limit_ns;
     int skip_loads;  // test hook: issue no copies, so the first wait runs out
@@ -152,17 +153,56 @@ __device__ __forceinline__ void tmem_teardown(const Smem &sm, uint32_t tmem, boo
     }
 }
 
+// Writes this thread's 64 fp32 values (columns [64*ch, 64*ch + 64) of TMEM row `row`,
+// starting at TMEM column `tcol`) times `scale` into the shared-memory staging of a
+// 128 x 128 fp32 tile: four 128-byte-swizzled boxes of 32 columns x 128 rows, 16 KB
+// each, as the tiled store expects.  Rows in a group of 8 write different 16-byte
+// chunks, so the stores do not collide in banks.
+__device__ __forceinline__ void stage_f32_rows(uint32_t tmem_row_addr, int tcol, int ch, int row, float scale,
+                                               bool zero, uint32_t stage) {
+#pragma unroll 1
+    for (int j = 0; j < 2; ++j) {
+        const int c = 2 * ch + j;  // 32-column box
+        uint32_t v[32];
+        if (!zero) {
+            ptx::tmem_ld32(tmem_row_addr + tcol + c * 32, v);
+            ptx::tmem_wait_ld(v);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) v[k] = 0u;
+        }
+        const uint32_t rbase = stage + c * (BT * 128) + row * 128;
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            ptx::st_shared_v4(rbase + ((q ^ (row & 7)) << 4), __uint_as_float(v[4 * q]) * scale,
+                              __uint_as_float(v[4 * q + 1]) * scale, __uint_as_float(v[4 * q + 2]) * scale,
+                              __uint_as_float(v[4 * q + 3]) * scale);
+    }
+}
+
+// Thread 0 stores a staged 128 x 128 fp32 tile (four boxes) at rows [y, y + 128) of head z;
+// rows past the tensor's end are not written.
+__device__ __forceinline__ void store_tile_f32(const CUtensorMap *map, uint32_t stage, int y, int z) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) ptx::tma_store_3d(map, stage + c * (BT * 128), c * 32, y, z);
+    ptx::bulk_commit_group();
+}
+
 // ---------------------------------------------------------------- dQ
-__global__ void __launch_bounds__(128, 1)
+// 256 threads: warps w and w + 4 share TMEM lanes 32*(w%4)..+31 (the rows) and split the
+// 128 columns, 64 each (ch = w / 4).
+__global__ void __launch_bounds__(NTHREADS, 1)
     bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
                      const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                      const __grid_constant__ CUtensorMap tmKc, const __grid_constant__ CUtensorMap tmVc,
-                     const BwdTcParams p) {
+                     const __grid_constant__ CUtensorMap tmdQ, const BwdTcParams p) {
     extern __shared__ uint8_t smem_raw[];
     const Smem sm = carve(smem_raw);
     const uint32_t sQ = sm.tile[0], sdO = sm.tile[1];
     const uint32_t b_qd = ptx::smem_addr(&sm.bars[0]), b_mma = ptx::smem_addr(&sm.bars[3]);
-    const int t = threadIdx.x, warp = t >> 5;
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const int quarter = warp & 3, ch = warp >> 2;
+    const int row = quarter * 32 + lane;
     const int BH = p.B * p.Hq, n_qt = (p.N + BT - 1) / BT;
     const int qt = n_qt - 1 - static_cast<int>(blockIdx.x / BH);  // heaviest tiles first
     const int bh = static_cast<int>(blockIdx.x % BH);
@@ -173,7 +213,7 @@ __global__ void __launch_bounds__(128, 1)
     const int T = Tc + (i1 - lo0) / BT + 1;               // + band tiles
 
     const uint32_t tmem = tmem_setup(sm, 5);
-    const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     Waiter wait{p.wait_limit_ns, 0};
 
     auto issue_kv = [&](int tt) {
@@ -191,24 +231,28 @@ __global__ void __launch_bounds__(128, 1)
         issue_kv(0);
     }
 
-    // this thread's row: D = dO . O (also stored for the dkv kernel) and the LSE in log2 units
-    const int i = i0 + t;
+    // this thread's row: D = dO . O (the two column halves add their partial sums; also
+    // stored for the dkv kernel) and the LSE in log2 units
+    const int i = i0 + row;
     const bool valid = i < p.N;
-    float Di = 0.f, lse2 = 0.f;
+    float Dpart = 0.f, lse2 = 0.f;
+    const int64_t u = static_cast<int64_t>(bh) * p.N + i;
     if (valid) {
-        const int64_t u = static_cast<int64_t>(bh) * p.N + i;
-        const uint4 *o4 = reinterpret_cast<const uint4 *>(p.O + u * HD);
-        const uint4 *d4 = reinterpret_cast<const uint4 *>(p.dO + u * HD);
+        const uint4 *o4 = reinterpret_cast<const uint4 *>(p.O + u * HD) + ch * 8;
+        const uint4 *d4 = reinterpret_cast<const uint4 *>(p.dO + u * HD) + ch * 8;
 #pragma unroll 4
-        for (int c = 0; c < HD / 8; ++c) {
+        for (int c = 0; c < 8; ++c) {
             const uint4 a = o4[c], b = d4[c];
             const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-            for (int k = 0; k < 4; ++k) Di += bf(aw[k], 0) * bf(bw[k], 0) + bf(aw[k], 1) * bf(bw[k], 1);
+            for (int k = 0; k < 4; ++k) Dpart += bf(aw[k], 0) * bf(bw[k], 0) + bf(aw[k], 1) * bf(bw[k], 1);
         }
         lse2 = p.LSE[u] * LOG2E;
-        p.Dbuf[u] = Di;
     }
+    sm.stage[t] = Dpart;
+    __syncthreads();
+    const float Di = sm.stage[row] + sm.stage[BT + row];
+    if (valid && ch == 0) p.Dbuf[u] = Di;
     const int lo_i = win_of(p, i), nc_i = lo_of(i, p.w) / p.g;
     const float c1 = p.tau * LOG2E;
     const uint64_t dQd = ptx::smem_desc_sw128(sQ, 16, 1024), ddOd = ptx::smem_desc_sw128(sdO, 16, 1024);
@@ -232,7 +276,9 @@ __global__ void __launch_bounds__(128, 1)
         // buffer takes the next tile's copy
         if (t == 0 && tt + 1 < T && !p.skip_loads) issue_kv(tt + 1);
         ptx::tc_fence_after();
-        // dS = P (dP - D) on this row's visible columns; bf16 pairs written over S
+        // dS = P (dP - D) on this row's visible columns.  The half ch reads S and dP
+        // columns [64ch, 64ch + 64) and writes their bf16 dS pairs to S columns
+        // [64ch, 64ch + 32), which it has already read.
         int c_lo = 0, c_hi = BT - 1;
         if (core) {
             c_hi = min(nc_i - y0, BT) - 1;
@@ -242,7 +288,8 @@ __global__ void __launch_bounds__(128, 1)
         }
         if (!valid) c_hi = -1;
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int j = 0; j < 2; ++j) {
+            const int c = 2 * ch + j;
             uint32_t s[32], dp[32];
             ptx::tmem_ld32(tmem + lane_addr + c * 32, s);
             ptx::tmem_ld32(tmem + lane_addr + 128 + c * 32, dp);
@@ -261,15 +308,15 @@ __global__ void __launch_bounds__(128, 1)
                 }
                 pk[k] = ptx::pack_bf16x2(d2[0], d2[1]);
             }
-            ptx::tmem_st16(tmem + lane_addr + c * 16, pk);
+            ptx::tmem_st16(tmem + lane_addr + ch * 64 + j * 16, pk);
         }
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         __syncthreads();
         if (warp == 0) {
             ptx::tc_fence_after();
-            ptx::mma_ts_k128_warp(tmem + 256, tmem + 0, ptx::smem_desc_sw128(sK, HALF_BYTES, 1024), IDESC_TS,
-                                  tt > 0 ? 1u : 0u);  // dQ += dS K, completion covered by the next wait
+            ptx::mma_ts_k128_split_warp(tmem + 256, tmem + 0, ptx::smem_desc_sw128(sK, HALF_BYTES, 1024), IDESC_TS,
+                                        tt > 0 ? 1u : 0u);  // dQ += dS K, completion covered by the next wait
         }
     }
     if (ok) {
@@ -277,36 +324,37 @@ __global__ void __launch_bounds__(128, 1)
         ok = wait(b_mma, mma_phase++ & 1);
     }
     if (ok) {
+        // dQ * tau through shared memory (the first K/V buffer, idle now) to a tiled store
         ptx::tc_fence_after();
-        float *dst = p.dQ + (static_cast<int64_t>(bh) * p.N + i) * HD;
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-            uint32_t o[32];
-            ptx::tmem_ld32(tmem + lane_addr + 256 + c * 32, o);
-            ptx::tmem_wait_ld(o);
-            if (valid) {
-#pragma unroll
-                for (int k = 0; k < 32; k += 4)
-                    *reinterpret_cast<float4 *>(dst + c * 32 + k) =
-                        make_float4(__uint_as_float(o[k]) * p.tau, __uint_as_float(o[k + 1]) * p.tau,
-                                    __uint_as_float(o[k + 2]) * p.tau, __uint_as_float(o[k + 3]) * p.tau);
-            }
+        const uint32_t stage = sm.tile[2];
+        stage_f32_rows(tmem + lane_addr, 256, ch, row, p.tau, false, stage);
+        ptx::fence_proxy_async_smem();
+        __syncthreads();
+        if (t == 0) {
+            store_tile_f32(&tmdQ, stage, i0, bh);
+            ptx::bulk_wait_all();
         }
     }
     tmem_teardown(sm, tmem, ok, p);
 }
 
 // ---------------------------------------------------------------- dK, dV
-__global__ void __launch_bounds__(128, 1)
+// 256 threads: rows are keys, and the two warps on a TMEM lane quarter split each query
+// tile's 128 columns, 64 each.
+__global__ void __launch_bounds__(NTHREADS, 1)
     bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
                       const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                       const __grid_constant__ CUtensorMap tmKc, const __grid_constant__ CUtensorMap tmVc,
+                      const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
+                      const __grid_constant__ CUtensorMap tmdKc, const __grid_constant__ CUtensorMap tmdVc,
                       const BwdTcParams p) {
     extern __shared__ uint8_t smem_raw[];
     const Smem sm = carve(smem_raw);
     const uint32_t sK = sm.tile[0], sV = sm.tile[1];
     const uint32_t b_kv = ptx::smem_addr(&sm.bars[0]), b_mma = ptx::smem_addr(&sm.bars[3]);
-    const int t = threadIdx.x, warp = t >> 5;
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const int quarter = warp & 3, ch = warp >> 2;
+    const int row = quarter * 32 + lane;
     const int BK = p.B * p.Hkv;
     const int n_core_t = (p.G + BT - 1) / BT;
     // core tiles first (they are seen by the most query rows), then raw-token tiles
@@ -334,9 +382,9 @@ __global__ void __launch_bounds__(128, 1)
     const int n_it = nq * r;  // (head, query tile) pairs, head-major
 
     const uint32_t tmem = tmem_setup(sm, 5);
-    const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     Waiter wait{p.wait_limit_ns, 0};
-    const int m = y0 + t;  // this thread's key (core index or token)
+    const int m = y0 + row;  // this thread's key (core index or token)
     const float c1 = p.tau * LOG2E;
 
     auto bh_of = [&](int it) { return b * p.Hq + kv * r + it / nq; };
@@ -354,6 +402,9 @@ __global__ void __launch_bounds__(128, 1)
         if (n_it > 0) issue_q(0);
     }
     const uint64_t dKk = ptx::smem_desc_sw128(sK, 16, 1024), dVk = ptx::smem_desc_sw128(sV, 16, 1024);
+    // this key's visible query rows, as a function of the query tile's first row
+    int64_t key_last = 0;
+    if (!core) key_last = p.window_mode ? static_cast<int64_t>(m / p.g + 1) * p.g + p.w - 2 : static_cast<int64_t>(m) + p.w - 1;
 
     bool ok = wait(b_kv, 0);
     uint32_t mma_phase = 0;
@@ -361,9 +412,11 @@ __global__ void __launch_bounds__(128, 1)
         const int bh = bh_of(it), i0 = i0_of(it);
         const uint32_t sQ = sm.tile[2 + 2 * (it & 1)], sdO = sm.tile[3 + 2 * (it & 1)];
         float *s_lse = sm.stage + (it & 1) * 2 * BT, *s_D = s_lse + BT;
-        const int iq = i0 + t;  // the row whose LSE and D this thread stages
-        s_lse[t] = iq < p.N ? p.LSE[static_cast<int64_t>(bh) * p.N + iq] * LOG2E : 0.f;
-        s_D[t] = iq < p.N ? p.Dbuf[static_cast<int64_t>(bh) * p.N + iq] : 0.f;
+        if (t < BT) {  // stage the query tile's LSE (log2 units) and D
+            const int iq = i0 + t;
+            s_lse[t] = iq < p.N ? p.LSE[static_cast<int64_t>(bh) * p.N + iq] * LOG2E : 0.f;
+            s_D[t] = iq < p.N ? p.Dbuf[static_cast<int64_t>(bh) * p.N + iq] : 0.f;
+        }
         if (!(ok = wait(ptx::smem_addr(&sm.bars[1 + (it & 1)]), (it >> 1) & 1))) break;
         if (warp == 0) {
             // queued behind the previous pair's dV/dK MMAs, which still read P^T and dS^T
@@ -385,14 +438,15 @@ __global__ void __launch_bounds__(128, 1)
             q_lo = max((m + 1) * p.g + p.w - 1 - i0, 0);
             q_hi = min(p.N - 1 - i0, BT - 1);
         } else {
-            const int64_t last = p.window_mode ? static_cast<int64_t>(m / p.g + 1) * p.g + p.w - 2
-                                               : static_cast<int64_t>(m) + p.w - 1;
+            const int last_i = static_cast<int>(key_last < p.N - 1 ? key_last : p.N - 1);
             q_lo = max(m - i0, 0);
-            const int last_i = static_cast<int>(last < p.N - 1 ? last : p.N - 1);
             q_hi = min(last_i - i0, BT - 1);
         }
+        // the half ch handles query columns [64ch, 64ch + 64): P^T to S^T columns
+        // [64ch, 64ch + 32), dS^T to dP^T columns [64ch, 64ch + 32), both already read
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int j = 0; j < 2; ++j) {
+            const int c = 2 * ch + j;
             uint32_t s[32], dp[32];
             ptx::tmem_ld32(tmem + lane_addr + c * 32, s);
             ptx::tmem_ld32(tmem + lane_addr + 128 + c * 32, dp);
@@ -413,8 +467,8 @@ __global__ void __launch_bounds__(128, 1)
                 pp[k] = ptx::pack_bf16x2(pv[0], pv[1]);
                 dd[k] = ptx::pack_bf16x2(dv[0], dv[1]);
             }
-            ptx::tmem_st16(tmem + lane_addr + c * 16, pp);        // P^T  over S^T
-            ptx::tmem_st16(tmem + lane_addr + 128 + c * 16, dd);  // dS^T over dP^T
+            ptx::tmem_st16(tmem + lane_addr + ch * 64 + j * 16, pp);        // P^T  over S^T
+            ptx::tmem_st16(tmem + lane_addr + 128 + ch * 64 + j * 16, dd);  // dS^T over dP^T
         }
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
@@ -422,10 +476,10 @@ __global__ void __launch_bounds__(128, 1)
         if (warp == 0) {
             ptx::tc_fence_after();
             const uint32_t acc = it > 0 ? 1u : 0u;
-            ptx::mma_ts_k128_warp(tmem + 384, tmem + 0, ptx::smem_desc_sw128(sdO, HALF_BYTES, 1024), IDESC_TS,
-                                  acc);  // dV += P^T dO
-            ptx::mma_ts_k128_warp(tmem + 256, tmem + 128, ptx::smem_desc_sw128(sQ, HALF_BYTES, 1024), IDESC_TS,
-                                  acc);  // dK += dS^T Q; completion covered by the next wait
+            ptx::mma_ts_k128_split_warp(tmem + 384, tmem + 0, ptx::smem_desc_sw128(sdO, HALF_BYTES, 1024), IDESC_TS,
+                                        acc);  // dV += P^T dO
+            ptx::mma_ts_k128_split_warp(tmem + 256, tmem + 128, ptx::smem_desc_sw128(sQ, HALF_BYTES, 1024),
+                                        IDESC_TS, acc);  // dK += dS^T Q; completion covered by the next wait
         }
     }
     if (ok && n_it > 0) {
@@ -433,33 +487,18 @@ __global__ void __launch_bounds__(128, 1)
         ok = wait(b_mma, mma_phase++ & 1);
     }
     if (ok) {
-        const bool mine = m < n_keys;
-        float *dk = (core ? p.dKc : p.dK) + (static_cast<int64_t>(bk) * n_keys + m) * HD;
-        float *dv = (core ? p.dVc : p.dV) + (static_cast<int64_t>(bk) * n_keys + m) * HD;
+        // dK * tau and dV through shared memory (the Q/dO buffers, idle now) to tiled stores;
+        // a tile no query row sees stores zeros
         ptx::tc_fence_after();
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-            uint32_t a[32], v[32];
-            if (n_it > 0) {
-                ptx::tmem_ld32(tmem + lane_addr + 256 + c * 32, a);
-                ptx::tmem_ld32(tmem + lane_addr + 384 + c * 32, v);
-                ptx::tmem_wait_ld(a);
-                ptx::reg_touch(v);
-            } else {
-#pragma unroll
-                for (int k = 0; k < 32; ++k) a[k] = v[k] = 0u;
-            }
-            if (mine) {
-#pragma unroll
-                for (int k = 0; k < 32; k += 4) {
-                    *reinterpret_cast<float4 *>(dk + c * 32 + k) =
-                        make_float4(__uint_as_float(a[k]) * p.tau, __uint_as_float(a[k + 1]) * p.tau,
-                                    __uint_as_float(a[k + 2]) * p.tau, __uint_as_float(a[k + 3]) * p.tau);
-                    *reinterpret_cast<float4 *>(dv + c * 32 + k) =
-                        make_float4(__uint_as_float(v[k]), __uint_as_float(v[k + 1]), __uint_as_float(v[k + 2]),
-                                    __uint_as_float(v[k + 3]));
-                }
-            }
+        const uint32_t stk = sm.tile[2], stv = sm.tile[4];
+        stage_f32_rows(tmem + lane_addr, 256, ch, row, p.tau, n_it == 0, stk);
+        stage_f32_rows(tmem + lane_addr, 384, ch, row, 1.f, n_it == 0, stv);
+        ptx::fence_proxy_async_smem();
+        __syncthreads();
+        if (t == 0) {
+            store_tile_f32(core ? &tmdKc : &tmdK, stk, y0, bk);
+            store_tile_f32(core ? &tmdVc : &tmdV, stv, y0, bk);
+            ptx::bulk_wait_all();
         }
     }
     tmem_teardown(sm, tmem, ok, p);
@@ -497,10 +536,13 @@ cudaError_t launch_attn_bwd_tc(const void *Q, const void *K, const void *V, cons
     }
     const uint64_t G = static_cast<uint64_t>(s.N / s.g);
     const uint64_t qh = static_cast<uint64_t>(s.B) * s.Hq, kh = static_cast<uint64_t>(s.B) * s.Hkv;
-    CUtensorMap mQ, mdO, mK, mV, mKc, mVc;
+    CUtensorMap mQ, mdO, mK, mV, mKc, mVc, mdQ, mdK, mdV, mdKc, mdVc;
     if (!encode_3d_bf16_d128(enc, &mQ, Q, s.N, qh) || !encode_3d_bf16_d128(enc, &mdO, dO, s.N, qh) ||
         !encode_3d_bf16_d128(enc, &mK, K, s.N, kh) || !encode_3d_bf16_d128(enc, &mV, V, s.N, kh) ||
-        !encode_3d_bf16_d128(enc, &mKc, Kc, G, kh) || !encode_3d_bf16_d128(enc, &mVc, Vc, G, kh))
+        !encode_3d_bf16_d128(enc, &mKc, Kc, G, kh) || !encode_3d_bf16_d128(enc, &mVc, Vc, G, kh) ||
+        !encode_3d_f32_d128(enc, &mdQ, dQ, s.N, qh) || !encode_3d_f32_d128(enc, &mdK, dK, s.N, kh) ||
+        !encode_3d_f32_d128(enc, &mdV, dV, s.N, kh) || !encode_3d_f32_d128(enc, &mdKc, dKc, G, kh) ||
+        !encode_3d_f32_d128(enc, &mdVc, dVc, G, kh))
         return cudaErrorInvalidValue;
     BwdTcParams p;
     p.B = s.B;
@@ -516,21 +558,17 @@ cudaError_t launch_attn_bwd_tc(const void *Q, const void *K, const void *V, cons
     p.O = static_cast<const __nv_bfloat16 *>(O);
     p.dO = static_cast<const __nv_bfloat16 *>(dO);
     p.Dbuf = Dbuf;
-    p.dQ = dQ;
-    p.dK = dK;
-    p.dV = dV;
-    p.dKc = dKc;
-    p.dVc = dVc;
     p.status = status;
     p.wait_limit_ns = g_wait_limit_ns;
     p.skip_loads = g_skip_q_load;
     const unsigned n_qt = static_cast<unsigned>((s.N + BT - 1) / BT);
-    bwd_dq_tc_kernel<<<n_qt * static_cast<unsigned>(qh), 128, SMEM_BYTES, stream>>>(mQ, mdO, mK, mV, mKc, mVc, p);
+    bwd_dq_tc_kernel<<<n_qt * static_cast<unsigned>(qh), NTHREADS, SMEM_BYTES, stream>>>(mQ, mdO, mK, mV, mKc, mVc,
+                                                                                         mdQ, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const unsigned n_kt = static_cast<unsigned>((G + BT - 1) / BT + (s.N + BT - 1) / BT);
-    bwd_dkv_tc_kernel<<<n_kt * static_cast<unsigned>(kh), 128, SMEM_BYTES, stream>>>(mQ, mdO, mK, mV, mKc, mVc,
-                                                                                      p);
+    bwd_dkv_tc_kernel<<<n_kt * static_cast<unsigned>(kh), NTHREADS, SMEM_BYTES, stream>>>(
+        mQ, mdO, mK, mV, mKc, mVc, mdK, mdV, mdKc, mdVc, p);
     return cudaGetLastError();
 }
 
