@@ -24,6 +24,29 @@ import torch
 from . import widen
 
 
+def pool_dense(q, k, v, g: int, tau: float, pool_mode: int = 0):
+    """Differentiable pooling -> (Kc, Vc) [B, Hkv, N/g, d].  Max pooling takes, per
+    element, the group's first row holding the maximum (a gather at the first argmax),
+    so at ties the whole gradient goes to that row: the reading the library documents
+    for the subgradient of max."""
+    B, Hq, N, d = q.shape
+    Hkv = k.shape[1]
+    r, G = Hq // Hkv, N // g
+    Kg = k.reshape(B, Hkv, G, g, d)
+    Vg = v.reshape(B, Hkv, G, g, d)
+    if pool_mode == 2:
+        ik = Kg.argmax(dim=3, keepdim=True)  # first maximal row (torch returns the first)
+        iv = Vg.argmax(dim=3, keepdim=True)
+        return Kg.gather(3, ik).squeeze(3), Vg.gather(3, iv).squeeze(3)
+    if pool_mode == 1:
+        a = torch.full((B, Hkv, G, g), 1.0 / g, dtype=q.dtype)
+    else:
+        qlast = q[:, :, g - 1::g].reshape(B, Hkv, r, G, d)
+        s = tau * torch.einsum("bkrjc,bkjtc->bkjt", qlast, Kg) / r
+        a = torch.softmax(s, dim=-1)
+    return torch.einsum("bkjt,bkjtc->bkjc", a, Kg), torch.einsum("bkjt,bkjtc->bkjc", a, Vg)
+
+
 def dense_forward(q, k, v, g: int, w: int, scale: float | None = None, pool_mode: int = 0,
                   window_mode: int = 0):
     """Differentiable fp64 forward: returns (O [B,Hq,N,d], LSE [B,Hq,N])."""
@@ -31,19 +54,7 @@ def dense_forward(q, k, v, g: int, w: int, scale: float | None = None, pool_mode
     Hkv = k.shape[1]
     r, G = Hq // Hkv, N // g
     tau = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    Kg = k.reshape(B, Hkv, G, g, d)
-    Vg = v.reshape(B, Hkv, G, g, d)
-    if pool_mode == 2:
-        Kc, Vc = Kg.amax(dim=3), Vg.amax(dim=3)
-    else:
-        if pool_mode == 1:
-            a = torch.full((B, Hkv, G, g), 1.0 / g, dtype=q.dtype)
-        else:
-            qlast = q[:, :, g - 1::g].reshape(B, Hkv, r, G, d)
-            s = tau * torch.einsum("bkrjc,bkjtc->bkjt", qlast, Kg) / r
-            a = torch.softmax(s, dim=-1)
-        Kc = torch.einsum("bkjt,bkjtc->bkjc", a, Kg)
-        Vc = torch.einsum("bkjt,bkjtc->bkjc", a, Vg)
+    Kc, Vc = pool_dense(q, k, v, g, tau, pool_mode)
     i = torch.arange(N)[:, None]
     lo = torch.clamp(i - w + 1, min=0)
     n_core = lo // g

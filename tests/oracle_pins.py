@@ -343,4 +343,25 @@ def pin_backward_g1_is_causal(lib):
         np.testing.assert_allclose(a, b.numpy(), rtol=0, atol=1e-12)
 
 
-BACKWARD_PINS = [pin_backward_finite_differences, pin_backward_g1_is_causal]
+def pin_backward_max_pool_ties(lib):
+    # Max pooling at a tie: the whole gradient of a core element goes to the group's first
+    # row holding the maximum, none to the later equal rows (the documented subgradient).
+    from oracle.backward import pool_dense
+    B, H, N, d, g = 1, 1, 8, 4, 4
+    k = np.zeros((B, H, N, d))
+    k[0, 0, 1] = k[0, 0, 3] = [2.0, 1.0, 5.0, 0.5]  # rows 1 and 3 of group 0 tie at the maximum
+    k[0, 0, 4:] = _rand((4, d), 67)
+    kt = torch.tensor(k, requires_grad=True)
+    vt = torch.tensor(k.copy(), requires_grad=True)
+    Kc, Vc = pool_dense(torch.zeros((B, H, N, d), dtype=torch.float64), kt, vt, g, 1.0, pool_mode=2)
+    (Kc.sum() + 2.0 * Vc.sum()).backward()
+    gk, gv = kt.grad.numpy()[0, 0], vt.grad.numpy()[0, 0]
+    np.testing.assert_array_equal(gk[1], np.ones(d))
+    np.testing.assert_array_equal(gk[[0, 2, 3]], np.zeros((3, d)))
+    np.testing.assert_array_equal(gv[1], 2.0 * np.ones(d))
+    np.testing.assert_array_equal(gv[3], np.zeros(d))
+    # every element of every group sends its gradient to exactly one row
+    np.testing.assert_array_equal(gk.reshape(2, g, d).sum(axis=1), np.ones((2, d)))
+
+
+BACKWARD_PINS = [pin_backward_finite_differences, pin_backward_g1_is_causal, pin_backward_max_pool_ties]
