@@ -377,3 +377,30 @@ def cca_prefill_host(Q, K, V, g: int, w: int, scale: float = 0.0, out=None, with
     if st != CCA_OK:
         raise CcaError(st, "cca_prefill_host")
     return O, LSE, Kc, Vc
+
+
+class CcaAttentionFunction(torch.autograd.Function):
+    """Autograd wrapper of the prefill step: forward = cca_prefill (pooling + fused
+    attention), backward = cca_prefill_bwd.  Both run in the library's kernels; this
+    class only saves tensors and casts the fp32 gradients to the inputs' dtype."""
+
+    @staticmethod
+    def forward(ctx, Q, K, V, g, w, scale, pool_mode, window_mode):
+        Q, K, V = Q.contiguous(), K.contiguous(), V.contiguous()
+        O, LSE, Kc, Vc = cca_prefill(Q, K, V, g, w, scale, pool_mode=pool_mode, window_mode=window_mode)
+        ctx.save_for_backward(Q, K, V, Kc, Vc, O, LSE)
+        ctx.cfg = (g, w, scale, pool_mode, window_mode)
+        return O
+
+    @staticmethod
+    def backward(ctx, dO):
+        Q, K, V, Kc, Vc, O, LSE = ctx.saved_tensors
+        g, w, scale, pool_mode, window_mode = ctx.cfg
+        dQ, dK, dV = cca_prefill_bwd(Q, K, V, Kc, Vc, O, LSE, dO.contiguous().to(Q.dtype), g, w, scale,
+                                     pool_mode=pool_mode, window_mode=window_mode)
+        return dQ.to(Q.dtype), dK.to(K.dtype), dV.to(V.dtype), None, None, None, None, None
+
+
+def cca_attention(Q, K, V, g: int, w: int, scale: float = 0.0, pool_mode: int = 0, window_mode: int = 0):
+    """CCA attention output O [B, Hq, N, d] with gradients for Q, K and V (prefill step)."""
+    return CcaAttentionFunction.apply(Q, K, V, g, w, scale, pool_mode, window_mode)
