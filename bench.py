@@ -265,17 +265,25 @@ def run_cca(args, rank, world, local):
                           "attn_frac": W.attn_flops(wl2) / (am / 1e3) / 1e12 / peaks["bf16_tflops"],
                           "pool_gbs": W.pool_bytes(wl2) / (pm / 1e3) / 1e9,
                           "pool_frac": W.pool_bytes(wl2) / (pm / 1e3) / 1e9 / peaks["hbm_gbs"]}
-        out["gpu_launches"] += 2 * max(3, args.steps // 4)
+    if args.sweep:
+        # the other synthetic workloads (GQA 64K and the g x w sweep), same method, 3 timed steps
+        rows = []
+        for wl3 in [W.GQA_64K] + W.sweep():
+            tot, pm, am = measure(wl3, 3, 3)
+            rows.append({"workload": wl3.name, "tokens_per_s": wl3.B * wl3.N / (tot / 3 / 1e3),
+                         "attn_ms": am, "attn_eff_tflops": W.attn_flops(wl3) / (am / 1e3) / 1e12,
+                         "attn_frac": W.attn_flops(wl3) / (am / 1e3) / 1e12 / peaks["bf16_tflops"],
+                         "pool_ms": pm, "pool_gbs": W.pool_bytes(wl3) / (pm / 1e3) / 1e9,
+                         "pool_frac": W.pool_bytes(wl3) / (pm / 1e3) / 1e9 / peaks["hbm_gbs"]})
+        out["sweep"] = rows
     if args.decode:
         out["decode"] = decode_bench(wl, dev, stream, 50, peaks)
         if args.also_128k and wl is not W.MHA_128K:
             out["decode_128k"] = decode_bench(W.MHA_128K, dev, stream, 50, peaks)
     if args.backward:
         out["backward"] = backward_bench(wl, dev, stream, 2, peaks)
-        out["gpu_launches"] += 4 * 2
     if args.comparator:
         out["full_attention_comparator"] = comparator(wl, dev, stream, max(3, args.steps // 4), ms_per_step)
-        out["gpu_launches"] += max(3, args.steps // 4)
     if not args.no_e2e:
         out["e2e"] = e2e(wl, dev, stream, max(3, args.steps // 2), world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -481,6 +489,8 @@ def main():
     ap.add_argument("--no-comparator", dest="comparator", action="store_false")
     ap.add_argument("--no-decode", dest="decode", action="store_false")
     ap.add_argument("--no-backward", dest="backward", action="store_false")
+    ap.add_argument("--sweep", action="store_true",
+                    help="also time the GQA 64K workload and the 12 g x w sweep points")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

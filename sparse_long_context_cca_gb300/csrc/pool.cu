@@ -29,7 +29,7 @@ namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int NW_MAX = 12;                 // warps per CTA (each feeds and consumes its own ring)
-constexpr int S_MAX = 4;                   // ring stages per warp
+constexpr int S_MAX = 8;                   // ring stages per warp
 constexpr uint32_t CHUNK_BYTES = 4096;     // bytes of K (and of V) per chunk
 constexpr uint32_t SMEM_BUDGET = 224 * 1024;
 constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;
@@ -76,6 +76,7 @@ struct VecTraits<float> {
 struct PoolArgs {
     int Hq, Hkv, N, g, r;
     int S;                 // ring stages per warp
+    uint32_t v_off;        // bytes of one chunk's K rows (V follows them, then the query rows)
     uint32_t stage_bytes;  // K chunk + V chunk + r query rows
     float logit_scale;     // tau * log2(e) / r (0 for mean pooling: equal weights)
     int pool_max;          // element-wise max pooling instead of weighted sums
@@ -137,12 +138,12 @@ __global__ void __launch_bounds__(NW_MAX * 32) pool_kernel(const T *__restrict__
         ptx::mbar_arrive_expect_tx(bar, 2 * kv_bytes + (ch == 0 ? a.r * ROW_BYTES : 0));
         const int64_t row0 = bk * a.N + j * a.g + t0;
         ptx::bulk_load(stage, K + row0 * D, kv_bytes, bar);
-        ptx::bulk_load(stage + CHUNK_BYTES, V + row0 * D, kv_bytes, bar);
+        ptx::bulk_load(stage + a.v_off, V + row0 * D, kv_bytes, bar);
         if (ch == 0) {
             const int64_t b = bk / a.Hkv, kv = bk % a.Hkv;
             const int64_t last = (j + 1) * a.g - 1;
             for (int hh = 0; hh < a.r; ++hh)
-                ptx::bulk_load(stage + 2 * CHUNK_BYTES + hh * ROW_BYTES,
+                ptx::bulk_load(stage + 2 * a.v_off + hh * ROW_BYTES,
                                Q + ((b * a.Hq + kv * a.r + hh) * static_cast<int64_t>(a.N) + last) * D, ROW_BYTES,
                                bar);
         }
@@ -176,7 +177,7 @@ __global__ void __launch_bounds__(NW_MAX * 32) pool_kernel(const T *__restrict__
             l = 0.f;
             for (int hh = 0; hh < a.r; ++hh) {
                 float f[E];
-                VT::unpack(lds16(stage + 2 * CHUNK_BYTES + hh * ROW_BYTES + cl * 16), f);
+                VT::unpack(lds16(stage + 2 * a.v_off + hh * ROW_BYTES + cl * 16), f);
 #pragma unroll
                 for (int e = 0; e < E; ++e) q[e] += f[e];
             }
@@ -189,7 +190,7 @@ __global__ void __launch_bounds__(NW_MAX * 32) pool_kernel(const T *__restrict__
             const int t = it * RPI + sub;
             if (t < rows) {
                 kr[it] = lds16(stage + t * ROW_BYTES + cl * 16);
-                vr[it] = lds16(stage + CHUNK_BYTES + t * ROW_BYTES + cl * 16);
+                vr[it] = lds16(stage + a.v_off + t * ROW_BYTES + cl * 16);
             } else {
                 kr[it] = vr[it] = make_uint4(0, 0, 0, 0);
             }
@@ -342,13 +343,24 @@ cudaError_t launch_typed(const void *Q, const void *K, const void *V, void *Kc, 
     a.N = s.N;
     a.g = s.g;
     a.r = s.Hq / s.Hkv;
-    a.stage_bytes = 2 * CHUNK_BYTES + static_cast<uint32_t>(a.r) * ROW;
-    // two stages per warp and as many warps as fit (up to NW_MAX): more warps hide the
-    // latency of the per-chunk arithmetic, two stages keep a copy in flight per warp
-    a.S = 2;
-    int nw = static_cast<int>(SMEM_BUDGET / (a.S * a.stage_bytes));
-    if (nw > NW_MAX) nw = NW_MAX;
-    if (nw < 1) return cudaErrorNotSupported;  // a stage would not fit (hundreds of query heads per KV head)
+    // A chunk carries at most min(g, CHUNK_BYTES / row) rows, so a stage holds just that
+    // much K and V plus the r query rows.  NW_MAX warps (more warps hide the per-chunk
+    // arithmetic), and as many stages as the budget allows (small groups give small
+    // stages, so more of them keep the same bytes in flight); at least two stages per
+    // warp, trading warps for stages when a stage is large.
+    const uint32_t chunk_rows = static_cast<uint32_t>(s.g) < CHUNK_BYTES / ROW ? static_cast<uint32_t>(s.g)
+                                                                               : CHUNK_BYTES / ROW;
+    a.v_off = chunk_rows * ROW;
+    a.stage_bytes = 2 * a.v_off + static_cast<uint32_t>(a.r) * ROW;
+    int nw = NW_MAX;
+    a.S = static_cast<int>(SMEM_BUDGET / (nw * a.stage_bytes));
+    if (a.S > S_MAX) a.S = S_MAX;
+    if (a.S < 2) {
+        a.S = 2;
+        nw = static_cast<int>(SMEM_BUDGET / (a.S * a.stage_bytes));
+        if (nw > NW_MAX) nw = NW_MAX;
+        if (nw < 1) return cudaErrorNotSupported;  // a stage would not fit (hundreds of query heads per KV head)
+    }
     a.logit_scale = s.pool_mode == 1 ? 0.f : s.scale * 1.4426950408889634f / static_cast<float>(a.r);
     a.pool_max = s.pool_mode == 2 ? 1 : 0;
     a.n_groups = static_cast<int64_t>(s.B) * s.Hkv * (s.N / s.g);
