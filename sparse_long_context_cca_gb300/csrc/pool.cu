@@ -124,16 +124,18 @@ __global__ void __launch_bounds__(NW_MAX * 32) pool_kernel(const T *__restrict__
     const int64_t my_groups = gw < a.n_groups ? (a.n_groups - 1 - gw) / tw + 1 : 0;
     const int64_t n_chunks = my_groups * nch;
 
-    // lane 0: bring chunk c of this warp's stream into stage c % S
-    auto issue = [&](int64_t c) {
-        const int64_t gid = gw + (c / nch) * tw;
-        const int ch = static_cast<int>(c % nch);
-        const int64_t j = gid % G;
-        const int64_t bk = gid / G;
+    // Lane 0 brings the warp's chunks into its ring in stream order.  The cursor
+    // (stage, chunk of the group, group index j, (b, kv) row bk) advances by counting,
+    // so no chunk pays for a 64-bit division.
+    int is = 0, ich = 0;
+    int64_t ij = gw % G, ibk = gw / G;
+    auto issue = [&]() {
+        const int ch = ich;
+        const int64_t j = ij, bk = ibk;
         const int t0 = ch * RS;
         const int rows = min(RS, a.g - t0);
-        const uint32_t stage = ring + static_cast<uint32_t>(c % a.S) * a.stage_bytes;
-        const uint32_t bar = ptx::smem_addr(&bars[wib][c % a.S]);
+        const uint32_t stage = ring + static_cast<uint32_t>(is) * a.stage_bytes;
+        const uint32_t bar = ptx::smem_addr(&bars[wib][is]);
         const uint32_t kv_bytes = rows * ROW_BYTES;
         ptx::mbar_arrive_expect_tx(bar, 2 * kv_bytes + (ch == 0 ? a.r * ROW_BYTES : 0));
         const int64_t row0 = bk * a.N + j * a.g + t0;
@@ -147,22 +149,31 @@ __global__ void __launch_bounds__(NW_MAX * 32) pool_kernel(const T *__restrict__
                                Q + ((b * a.Hq + kv * a.r + hh) * static_cast<int64_t>(a.N) + last) * D, ROW_BYTES,
                                bar);
         }
+        if (++is == a.S) is = 0;
+        if (++ich == nch) {
+            ich = 0;
+            ij += tw;  // next group of this warp: gid += tw
+            if (ij >= G) {
+                ibk += ij / G;
+                ij %= G;
+            }
+        }
     };
     if (lane == 0)
-        for (int64_t c = 0; c < n_chunks && c < a.S; ++c) issue(c);
+        for (int64_t c = 0; c < n_chunks && c < a.S; ++c) issue();
     __syncwarp();
 
     float q[E], ak[E], av[E];
     float m = -INFINITY, l = 0.f;
     int64_t c = 0;
+    int st = 0, ch = 0;   // consumer's stage and chunk-of-group counters
+    uint32_t ph = 0;      // parity of the stage barrier's current use
+    int64_t gid = gw;     // consumer's group
     for (; c < n_chunks; ++c) {
-        const int st = static_cast<int>(c % a.S);
         const uint32_t stage = ring + st * a.stage_bytes;
         volatile int *af = &abort_flag;
-        if (!__all_sync(kFull, ptx::wait_bounded(ptx::smem_addr(&bars[wib][st]), (c / a.S) & 1, af,
-                                                  WAIT_LIMIT_NS)))
+        if (!__all_sync(kFull, ptx::wait_bounded(ptx::smem_addr(&bars[wib][st]), ph, af, WAIT_LIMIT_NS)))
             break;
-        const int ch = static_cast<int>(c % nch);
         const int t0 = ch * RS;
         const int rows = min(RS, a.g - t0);
         if (ch == 0) {
@@ -253,7 +264,7 @@ __global__ void __launch_bounds__(NW_MAX * 32) pool_kernel(const T *__restrict__
         // every lane has read the stage: refill it with chunk c + S
         ptx::fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0 && c + a.S < n_chunks) issue(c + a.S);
+        if (lane == 0 && c + a.S < n_chunks) issue();
 
         if (ch == nch - 1) {
             // group done: combine the RPI row-subgroups, normalise, store
@@ -290,7 +301,6 @@ __global__ void __launch_bounds__(NW_MAX * 32) pool_kernel(const T *__restrict__
                 kt[e] *= inv;
                 vt[e] *= inv;
             }
-            const int64_t gid = gw + (c / nch) * tw;
             const int64_t orow = gid * static_cast<int64_t>(D) + cl * E;  // gid = (b*Hkv + kv)*G + j
             if (RPI >= 2) {
                 if (sub == 0) *reinterpret_cast<uint4 *>(Kc + orow) = VT::pack(kt);
@@ -299,6 +309,14 @@ __global__ void __launch_bounds__(NW_MAX * 32) pool_kernel(const T *__restrict__
                 *reinterpret_cast<uint4 *>(Kc + orow) = VT::pack(kt);
                 *reinterpret_cast<uint4 *>(Vc + orow) = VT::pack(vt);
             }
+        }
+        if (++st == a.S) {
+            st = 0;
+            ph ^= 1u;
+        }
+        if (++ch == nch) {
+            ch = 0;
+            gid += tw;
         }
     }
     if (c < n_chunks) {
