@@ -13,6 +13,7 @@
 #include <stdint.h>
 
 #include "internal.h"
+#include "visibility.cuh"
 
 namespace cca {
 namespace {
@@ -75,9 +76,8 @@ __global__ void __launch_bounds__(128) attn_f32_kernel(const float *__restrict__
         st.q[e] = Q[u * D + lane * PL + e];
         st.o[e] = 0.f;
     }
-    const int64_t lo_w = i - w + 1 > 0 ? i - w + 1 : 0;
-    const int64_t n_core = lo_w / g;
-    const int64_t lo = window_mode ? n_core * g : lo_w;  // first raw token of the window
+    const int64_t n_core = visible_cores(static_cast<int>(i), w, g);
+    const int64_t lo = window_start(static_cast<int>(i), w, g, window_mode);  // first raw token of the window
     const float *kc = Kc + bk * G * D;
     const float *vc = Vc + bk * G * D;
     for (int64_t j = 0; j < n_core; ++j) st.step(kc + j * D, vc + j * D, lane, scale_log2);

@@ -43,6 +43,7 @@
 #include "internal.h"
 #include "sm100_ptx.cuh"
 #include "tma_host.h"
+#include "visibility.cuh"
 
 namespace cca {
 namespace {
@@ -93,12 +94,9 @@ struct Params {
     int skip_q_load;  // test hook: never load Q, so the pipeline waits run out
 };
 
-__device__ __forceinline__ int lo_of(int i, int w) { return i - w + 1 > 0 ? i - w + 1 : 0; }
+__device__ __forceinline__ int lo_of(int i, int w) { return window_lo(i, w); }
 // first raw token of row i's window (cores stay j < lo(i)/g in both modes)
-__device__ __forceinline__ int win_of(const Params &p, int i) {
-    const int lo = lo_of(i, p.w);
-    return p.window_mode ? (lo / p.g) * p.g : lo;
-}
+__device__ __forceinline__ int win_of(const Params &p, int i) { return window_start(i, p.w, p.g, p.window_mode); }
 
 // The tile sequence of one work item and which half uses which tile.  Per-half
 // fields are scalars chosen with selects (no runtime-indexed arrays, which

@@ -28,6 +28,7 @@
 #include <type_traits>
 
 #include "internal.h"
+#include "visibility.cuh"
 
 namespace cca {
 namespace {
@@ -63,11 +64,8 @@ struct BwdArgs {
     float tau;
 };
 
-__device__ __forceinline__ int lo_of(int i, int w) { return i - w + 1 > 0 ? i - w + 1 : 0; }
-__device__ __forceinline__ int win_of(const BwdArgs &a, int i) {
-    const int lo = lo_of(i, a.w);
-    return a.window_mode ? (lo / a.g) * a.g : lo;
-}
+__device__ __forceinline__ int lo_of(int i, int w) { return window_lo(i, w); }
+__device__ __forceinline__ int win_of(const BwdArgs &a, int i) { return window_start(i, a.w, a.g, a.window_mode); }
 
 // Pass 1: one warp per query row -> dQ (fp32, before the pooling term) and D.
 template <typename T, int D>

@@ -35,6 +35,7 @@
 #include "internal.h"
 #include "sm100_ptx.cuh"
 #include "tma_host.h"
+#include "visibility.cuh"
 
 namespace cca {
 
@@ -67,11 +68,8 @@ struct BwdTcParams {
     int skip_loads;  // test hook: issue no copies, so the first wait runs out
 };
 
-__device__ __forceinline__ int lo_of(int i, int w) { return i - w + 1 > 0 ? i - w + 1 : 0; }
-__device__ __forceinline__ int win_of(const BwdTcParams &p, int i) {
-    const int lo = lo_of(i, p.w);
-    return p.window_mode ? (lo / p.g) * p.g : lo;
-}
+__device__ __forceinline__ int lo_of(int i, int w) { return window_lo(i, w); }
+__device__ __forceinline__ int win_of(const BwdTcParams &p, int i) { return window_start(i, p.w, p.g, p.window_mode); }
 
 __device__ __forceinline__ float bf(uint32_t w, int hi) {
     return __uint_as_float(hi ? (w & 0xffff0000u) : (w << 16));

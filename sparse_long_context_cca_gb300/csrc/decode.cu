@@ -18,6 +18,7 @@
 
 #include "internal.h"
 #include "sm100_ptx.cuh"
+#include "visibility.cuh"
 
 namespace cca {
 namespace {
@@ -401,9 +402,8 @@ cudaError_t launch_decode_typed(const void *Q, const void *K, const void *V, con
     a.Ncap = s.N;
     a.g = s.g;
     a.pos = pos;
-    const int lo = pos - s.w + 1 > 0 ? pos - s.w + 1 : 0;
-    a.n_core = lo / s.g;
-    a.lo = s.window_mode ? a.n_core * s.g : lo;  // first raw token of the window
+    a.n_core = visible_cores(pos, s.w, s.g);
+    a.lo = window_start(pos, s.w, s.g, s.window_mode);  // first raw token of the window
     a.L = a.n_core + (pos - a.lo + 1);
     a.splits = decode_splits(a.L);
     a.scale_log2 = s.scale * 1.4426950408889634f;
