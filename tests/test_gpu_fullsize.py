@@ -69,3 +69,11 @@ def test_gqa_64k():
 @pytest.mark.parametrize("wl", sweep(), ids=lambda w: w.name)
 def test_sweep(wl):
     check_workload(wl, [(1, 7)], n_random=24)
+
+
+def test_mha_1m_tokens():
+    """The largest context exercised: one million tokens (B1, 2 heads), where the last row
+    sees 65,472 cores plus its 1024-token window; sampled rows and groups of both heads."""
+    from sparse_long_context_cca_gb300.workloads import Workload
+    wl = Workload("mha B1 H2 d128 N1048576 g16 w1024", 1, 2, 2, 1 << 20, 128, 16, 1024, "bf16", 31, 0.01)
+    check_workload(wl, [(0, 0), (0, 1)], n_random=24)
