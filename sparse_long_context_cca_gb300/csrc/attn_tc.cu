@@ -92,6 +92,7 @@ struct Params {
     int32_t *status;
     unsigned long long wait_limit_ns;
     int skip_q_load;  // test hook: never load Q, so the pipeline waits run out
+    int o_align32;    // O is 32-byte aligned: the epilogue may use 32-byte stores
 };
 
 __device__ __forceinline__ int lo_of(int i, int w) { return window_lo(i, w); }
@@ -514,28 +515,39 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const bool valid = i < p.N;
             const float inv = 1.f / l;
             __nv_bfloat16 *orow = p.O + (static_cast<int64_t>(it.bh) * p.N + i) * HD;
+            uint32_t o[4][32];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t o[32];
-                ptx::tmem_ld32(tO + c * 32, o);
-                ptx::tmem_wait_ld(o);
-                uint4 v[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    v[q].x = ptx::pack_bf16x2(__uint_as_float(o[8 * q + 0]) * inv, __uint_as_float(o[8 * q + 1]) * inv);
-                    v[q].y = ptx::pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
-                    v[q].z = ptx::pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv);
-                    v[q].w = ptx::pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
-                }
-                if (valid) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) dst[q] = v[q];
-                }
-            }
+            for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tO + c * 32, o[c]);
+            ptx::tmem_wait_ld(o[0]);
+            ptx::reg_touch(o[1]);
+            ptx::reg_touch(o[2]);
+            ptx::reg_touch(o[3]);
+            // O_h is in registers: the issuer may start this half's next item
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(bar(B_OFREE + h));
+            // O / l as bf16, one 32-byte sector per store (two 16-byte stores if O is
+            // only 16-byte aligned)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    uint32_t v[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        v[k] = ptx::pack_bf16x2(__uint_as_float(o[c][16 * q + 2 * k]) * inv,
+                                                __uint_as_float(o[c][16 * q + 2 * k + 1]) * inv);
+                    if (valid) {
+                        if (p.o_align32) {
+                            ptx::st_global_v8(orow + c * 32 + q * 16, v);
+                        } else {
+                            uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32 + q * 16);
+                            dst[0] = make_uint4(v[0], v[1], v[2], v[3]);
+                            dst[1] = make_uint4(v[4], v[5], v[6], v[7]);
+                        }
+                    }
+                }
+            }
             if (valid) p.LSE[static_cast<int64_t>(it.bh) * p.N + i] = (m + __log2f(l)) * 0.6931471805599453f;
             ++n_done;
         }
@@ -610,6 +622,7 @@ cudaError_t launch_attn_bf16_tc(const void *Q, const void *K, const void *V, con
     p.status = dev_status;
     p.wait_limit_ns = g_wait_limit_ns;
     p.skip_q_load = g_skip_q_load;
+    p.o_align32 = (reinterpret_cast<uintptr_t>(O) & 31u) == 0 ? 1 : 0;
     const unsigned grid = static_cast<unsigned>(p.n_items < di.sms ? p.n_items : di.sms);
     attn_bf16_tc_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(mQ, mK, mV, mKc, mVc, p);
     return cudaGetLastError();

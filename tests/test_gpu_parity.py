@@ -147,3 +147,19 @@ def test_variants_parity(w, pool_mode, window_mode):
     Or, Lr, Kr, Vr = oracle.prefill(Q, K, V, w.g, w.w, pool_mode=pool_mode, window_mode=window_mode)
     check_cores(Kc, Vc, Kr, Vr, Q.dtype, f"{w.name} pool {pool_mode}")
     check_out(O, LSE, Or, Lr, Q.dtype, f"{w.name} pool {pool_mode} window {window_mode}")
+
+
+def test_output_alignment_16_bytes():
+    """O only 16-byte aligned (the ABI minimum) takes the epilogue's 16-byte stores and gives
+    the same bits as a 32-byte-aligned O."""
+    w = wl(1, 2, 2, 384, 128, 16, 100)
+    Q, K, V = make_qkv(w, "cuda")
+    Kc, Vc = api.cca_pool(Q, K, V, w.g)
+    O1, L1 = api.cca_attn_fwd(Q, K, V, Kc, Vc, w.g, w.w)
+    buf = torch.empty(Q.numel() + 16, dtype=Q.dtype, device="cuda")
+    assert buf.data_ptr() % 32 == 0
+    O2 = buf[8:8 + Q.numel()].view(Q.shape)  # 16 bytes past a 32-byte boundary
+    assert O2.data_ptr() % 32 == 16
+    O2, L2 = api.cca_attn_fwd(Q, K, V, Kc, Vc, w.g, w.w, O=O2)
+    torch.cuda.synchronize()
+    assert torch.equal(O1, O2) and torch.equal(L1, L2)
