@@ -133,6 +133,12 @@ __device__ __forceinline__ int half_next(const Half &x, int Tc, int t) {
 }
 __device__ __forceinline__ int half_count(const Half &x) { return x.valid ? x.tc + x.kh - x.kl : 0; }
 
+// Largest step between consecutive tiles of a half: only the step from its last core tile
+// to its first local tile can exceed 1.
+__device__ __forceinline__ int half_max_step(const Half &x, int Tc) {
+    return (x.valid && x.tc > 0) ? Tc + x.kl - (x.tc - 1) : 1;
+}
+
 __device__ __forceinline__ Half make_half(const Params &p, int a, int lo0) {
     Half x;
     x.a = a;
@@ -323,44 +329,108 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         if (x.valid) ok = issue_s(h, half_first(x, it.Tc));
                     }
                 }
-                bool first_pv[2] = {true, true};
-                for (int t = 0; ok && t < it.T; ++t) {
-                    // V(t) has landed: the tile's first S waited for its K and V together
-                    const uint32_t uv = ubase + 2 * t + 1;
-                    const int vslot = uv % NS;
+                // The tile loop.  After a half's PV on tile t the issuer starts S on the
+                // half's next tile, which first waits for that tile's copies; with a ring of
+                // two and a half tiles whose earlier slots only this loop frees, that wait can
+                // end only if the next tile is at most t + 2.  With the window aligned to groups
+                // of more than 128 tokens, half B's band can start further than that after its
+                // last core tile, so items with such a step take the second copy of the loop,
+                // which holds the S back (defer[h]) until the loop is two tiles short of it.
+                // The copies are separate so that the common loop carries none of that logic.
+                if (half_max_step(it.hA, it.Tc) <= 2 && half_max_step(it.hB, it.Tc) <= 2) {
+                    bool first_pv[2] = {true, true};
+                    for (int t = 0; ok && t < it.T; ++t) {
+                        // V(t) has landed: the tile's first S waited for its K and V together
+                        const uint32_t uv = ubase + 2 * t + 1;
+                        const int vslot = uv % NS;
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {  // unrolled: per-half counters stay in registers
-                        const Half &x = it.half(h);
-                        if (!half_uses(x, it.Tc, t)) continue;
-                        if (!wwait(bar(B_PFULL + h), pf_cnt[h] & 1)) {
-                            ok = false;
-                            break;
-                        }
-                        ++pf_cnt[h];
-                        if (first_pv[h]) {
-                            // the epilogue of this half's previous item must have read O_h
-                            if (!wwait(bar(B_OFREE + h), (n_half[h] & 1) ^ 1)) {
+                        for (int h = 0; h < 2; ++h) {  // unrolled: per-half counters stay in registers
+                            const Half &x = it.half(h);
+                            if (!half_uses(x, it.Tc, t)) continue;
+                            if (!wwait(bar(B_PFULL + h), pf_cnt[h] & 1)) {
                                 ok = false;
                                 break;
                             }
-                        }
-                        ptx::tc_fence_after();
-                        ptx::mma_ts_k128_warp(tmem + TM_O + h * HD, tmem + TM_S + h * BN,
-                                         dv0 + static_cast<uint64_t>(vslot) * (TILE_BYTES >> 4), IDESC_PV,
-                                         first_pv[h] ? 0u : 1u);
-                        first_pv[h] = false;
-                        const int tn = half_next(x, it.Tc, t);
-                        if (tn >= 0) {
-                            if (!issue_s(h, tn)) {
-                                ok = false;
-                                break;
+                            ++pf_cnt[h];
+                            if (first_pv[h]) {
+                                // the epilogue of this half's previous item must have read O_h
+                                if (!wwait(bar(B_OFREE + h), (n_half[h] & 1) ^ 1)) {
+                                    ok = false;
+                                    break;
+                                }
                             }
-                        } else {
-                            ptx::tc_commit_warp(bar(B_PVDONE + h));
+                            ptx::tc_fence_after();
+                            ptx::mma_ts_k128_warp(tmem + TM_O + h * HD, tmem + TM_S + h * BN,
+                                             dv0 + static_cast<uint64_t>(vslot) * (TILE_BYTES >> 4), IDESC_PV,
+                                             first_pv[h] ? 0u : 1u);
+                            first_pv[h] = false;
+                            const int tn = half_next(x, it.Tc, t);
+                            if (tn >= 0) {
+                                if (!issue_s(h, tn)) {
+                                    ok = false;
+                                    break;
+                                }
+                            } else {
+                                ptx::tc_commit_warp(bar(B_PVDONE + h));
+                            }
                         }
+                        if (!ok) break;
+                        ptx::tc_commit_warp(bar(B_EMPTY + vslot));
                     }
-                    if (!ok) break;
-                    ptx::tc_commit_warp(bar(B_EMPTY + vslot));
+                } else {
+                    bool first_pv[2] = {true, true};
+                    int defer[2] = {-1, -1};
+                    for (int t = 0; ok && t < it.T; ++t) {
+                        // V(t) has landed: the tile's first S waited for its K and V together
+                        const uint32_t uv = ubase + 2 * t + 1;
+                        const int vslot = uv % NS;
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            if (defer[h] >= 0 && defer[h] <= t + 2) {
+                                if (!issue_s(h, defer[h])) {
+                                    ok = false;
+                                    break;
+                                }
+                                defer[h] = -1;
+                            }
+                        }
+                        if (!ok) break;
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {  // unrolled: per-half counters stay in registers
+                            const Half &x = it.half(h);
+                            if (!half_uses(x, it.Tc, t)) continue;
+                            if (!wwait(bar(B_PFULL + h), pf_cnt[h] & 1)) {
+                                ok = false;
+                                break;
+                            }
+                            ++pf_cnt[h];
+                            if (first_pv[h]) {
+                                // the epilogue of this half's previous item must have read O_h
+                                if (!wwait(bar(B_OFREE + h), (n_half[h] & 1) ^ 1)) {
+                                    ok = false;
+                                    break;
+                                }
+                            }
+                            ptx::tc_fence_after();
+                            ptx::mma_ts_k128_warp(tmem + TM_O + h * HD, tmem + TM_S + h * BN,
+                                             dv0 + static_cast<uint64_t>(vslot) * (TILE_BYTES >> 4), IDESC_PV,
+                                             first_pv[h] ? 0u : 1u);
+                            first_pv[h] = false;
+                            const int tn = half_next(x, it.Tc, t);
+                            if (tn > t + 2) {
+                                defer[h] = tn;
+                            } else if (tn >= 0) {
+                                if (!issue_s(h, tn)) {
+                                    ok = false;
+                                    break;
+                                }
+                            } else {
+                                ptx::tc_commit_warp(bar(B_PVDONE + h));
+                            }
+                        }
+                        if (!ok) break;
+                        ptx::tc_commit_warp(bar(B_EMPTY + vslot));
+                    }
                 }
                 ubase += 2 * it.T;
                 n_half[0] += it.hA.valid ? 1 : 0;
