@@ -77,7 +77,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -88,9 +88,12 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.monotonic(), line.strip()))
 
-    def stop(self):
+    def stop(self, window=None):
+        """Clock summary over the samples taken inside `window` (host monotonic times
+        bracketing the timed region).  When the region is shorter than the sampling
+        interval and no sample falls inside it, the two samples around it are used."""
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         time.sleep(0.15)
@@ -99,23 +102,32 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        sm, smax, reasons = [], [], set()
+        rows = []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for t, ln in self.lines:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 8:
                 continue
             try:
-                sm.append(float(parts[0]))
-                smax.append(float(parts[1]))
+                rows.append((t, float(parts[0]), float(parts[1]),
+                             {n for n, v in zip(names, parts[4:8]) if v.lower().startswith("active")}))
             except ValueError:
                 continue
-            for n, v in zip(names, parts[4:8]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
+        where = "whole measurement"
+        if window is not None and rows:
+            lo, hi = window
+            inside = [r for r in rows if lo <= r[0] <= hi]
+            if inside:
+                rows, where = inside, "timed region"
+            else:
+                before = [r for r in rows if r[0] < lo][-1:]
+                after = [r for r in rows if r[0] > hi][:1]
+                rows, where = before + after, "samples bracketing the timed region"
+        sm = [r[1] for r in rows]
+        reasons = set().union(*[r[3] for r in rows]) if rows else set()
         return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "sm_max_mhz": max(r[2] for r in rows) if rows else None,
+                "reasons": sorted(reasons), "samples": len(sm), "window": where}
 
 
 def kernel_sha(path):
@@ -203,11 +215,14 @@ def run_cca(args, rank, world, local):
         torch.cuda.synchronize()
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
+        h0 = time.monotonic()
         t0.record(stream)
         for k in range(steps):
             step(ev[k])
         t1.record(stream)
         torch.cuda.synchronize()
+        h1 = time.monotonic()
+        window[:] = [h0, h1]
         if world > 1:
             torch.distributed.barrier()
         total_ms = t0.elapsed_time(t1)
@@ -218,10 +233,11 @@ def run_cca(args, rank, world, local):
         torch.cuda.empty_cache()
         return total_ms, statistics.mean(pool_ms), statistics.mean(attn_ms)
 
+    window = []  # host times around the timed region, set by measure()
     sampler = ClockSampler(local)
     sampler.start()
     total_ms, pool_ms, attn_ms = measure(wl, args.steps, args.warmup)
-    clocks = sampler.stop()
+    clocks = sampler.stop(tuple(window) if window else None)
     total_ms = max_over_ranks(total_ms, world, dev)
     ms_per_step, value = job_throughput(total_ms, args.steps, wl.B * wl.N, world)
     flops = W.attn_flops(wl)
@@ -478,7 +494,7 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="mha32k")
     ap.add_argument("--impl", choices=["cca", "reference"], default="cca")

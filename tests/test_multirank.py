@@ -52,3 +52,29 @@ def test_two_rank_timing_and_throughput():
 def test_single_rank_is_identity():
     assert bench.max_over_ranks(12.5, 1, torch.device("cpu")) == 12.5
     assert bench.job_throughput(100.0, 10, 1000, 1) == (10.0, pytest.approx(1000 / 0.01))
+
+
+def test_clock_summary_uses_the_timed_region(monkeypatch):
+    """The clock record covers the samples taken inside the timed region, or the two around
+    it when the region is shorter than the sampling interval; throttle reasons are the union."""
+    s = bench.ClockSampler(0)
+
+    class FakeProc:
+        def terminate(self):
+            pass
+
+        def wait(self, timeout=None):
+            pass
+
+    s.proc = FakeProc()
+    monkeypatch.setattr(bench.time, "sleep", lambda _: None)
+    row = "{}, 2070, 900.0, 0x0, Not Active, Not Active, {}, Not Active"
+    s.lines = [(1.00, row.format(1500, "Not Active")), (1.05, row.format(2070, "Active")),
+               (1.10, row.format(2060, "Not Active")), (1.20, row.format(1400, "Not Active"))]
+    inside = s.stop((1.04, 1.11))
+    assert inside["samples"] == 2 and inside["window"] == "timed region"
+    assert inside["sm_mhz"] == 2065.0 and inside["reasons"] == ["sw_thermal_slowdown"]
+    short = s.stop((1.06, 1.07))
+    assert short["samples"] == 2 and short["window"] == "samples bracketing the timed region"
+    assert short["sm_mhz"] == 2065.0
+    assert s.stop(None)["samples"] == 4
