@@ -133,7 +133,9 @@ int cca_attn_fwd(const void *Q, const void *K, const void *V, const void *Kc, co
  *   cca_decode_workspace_size(params) bytes (per-split partial results); it
  *   needs no initialisation and is fully rewritten by every call.
  * The keys are split across CTAs (flash-decoding) and the partial results are
- * merged by a second kernel on the same stream.
+ * merged by a second kernel on the same stream, launched as a programmatic
+ * dependent of the first (it starts as the first drains and waits for its
+ * completion on the device).
  * Supported: bf16 or f32, d in {64, 128}, Hq/Hkv <= 8.
  */
 int cca_decode_fwd(const void *Q, const void *K, const void *V, const void *Kc, const void *Vc, void *O,

@@ -88,6 +88,8 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, R == 1 ? 4 : 1) decode_split_k
     __shared__ float sm_m[DEC_WARPS][R], sm_l[DEC_WARPS][R];
     __shared__ float sm_o[DEC_WARPS][R][D];
 
+    // The merge kernel may be scheduled now: it waits for this grid's completion itself.
+    asm volatile("griddepcontrol.launch_dependents;");
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int sub = lane / LPR, cl = lane % LPR;
     const int s = blockIdx.x;
@@ -247,6 +249,10 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const float *__restri
     constexpr int NW = D / 32;
     __shared__ float sh_f[MAX_SPLITS];
     __shared__ float sh_wm[NW], sh_wl[NW];
+    // Launched as a programmatic dependent of the split kernel, so its CTAs can start while
+    // the split grid drains; this waits until that grid has completed and its partials are
+    // visible.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int bh = blockIdx.x;
     const int c = threadIdx.x, lane = c & 31, warp = c >> 5;
     const float *base = ws + static_cast<int64_t>(bh) * MAX_SPLITS * (D + 2);
@@ -413,8 +419,20 @@ cudaError_t launch_decode_typed(const void *Q, const void *K, const void *V, con
         static_cast<const T *>(Vc), ws, a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    decode_combine_kernel<T, D><<<s.B * s.Hq, D, 0, stream>>>(ws, static_cast<T *>(O), LSE, a.splits);
-    return cudaGetLastError();
+    // The merge kernel is a programmatic dependent launch: it is scheduled as the split
+    // grid drains instead of after it, and orders itself with griddepcontrol.wait.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(s.B * s.Hq);
+    cfg.blockDim = dim3(D);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_combine_kernel<T, D>, static_cast<const float *>(ws), static_cast<T *>(O),
+                              LSE, a.splits);
 }
 
 template <typename T, int D>
