@@ -78,3 +78,11 @@ def test_clock_summary_uses_the_timed_region(monkeypatch):
     assert short["samples"] == 2 and short["window"] == "samples bracketing the timed region"
     assert short["sm_mhz"] == 2065.0
     assert s.stop(None)["samples"] == 4
+
+
+def test_tensor_peak_follows_the_power_cap():
+    peaks = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+    p, src = bench.tensor_peak(peaks, "fallback", {"reasons": ["sw_power_cap"]})
+    assert p == 1700.0 and "sustained" in src
+    p, src = bench.tensor_peak(peaks, "fallback", {"reasons": []})
+    assert p == 1900.0 and "burst" in src
