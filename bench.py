@@ -465,8 +465,8 @@ def oracle_sample(wl, seconds_budget, row_frac=1.0):
     small = wl.small(B=1, Hq=wl.Hq // wl.Hkv, Hkv=1)  # one KV head with its query heads
     Q, K, V = make_qkv(small, "cpu")
     q, k, v = oracle.widen(Q[:, :1]), oracle.widen(K), oracle.widen(V)
-    if row_frac < 1.0:
-        stride = max(1, int(round(1.0 / row_frac)))
+    stride = max(1, int(round(1.0 / row_frac))) if row_frac < 1.0 else 1
+    if stride > 1:
         rows = [(0, 0, i) for i in range(stride // 2, wl.N, stride)]
         t0 = time.perf_counter()
         Kc, Vc = oracle.pool(oracle.widen(Q), k, v, wl.g)
