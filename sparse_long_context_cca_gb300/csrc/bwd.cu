@@ -36,13 +36,58 @@ namespace {
 constexpr unsigned kFull = 0xffffffffu;
 constexpr float LOG2E = 1.4426950408889634f;
 
-__device__ __forceinline__ float to_f(float x) { return x; }
-__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
 
+// Lane `lane` owns elements lane*PL .. lane*PL+PL-1 of a d-element row.  Rows start on
+// 16-byte boundaries (the entry points require 16-byte aligned tensors and d is 64 or
+// 128), so each lane moves its PL elements with one 4-, 8- or 16-byte access and a warp
+// covers the row with one coalesced request.
 template <typename T, int PL>
 __device__ __forceinline__ void load_row(const T *__restrict__ row, int lane, float (&f)[PL]) {
+    if constexpr (std::is_same<T, __nv_bfloat16>::value && PL == 4) {
+        const uint2 v = *reinterpret_cast<const uint2 *>(row + lane * 4);
+        f[0] = __uint_as_float(v.x << 16);
+        f[1] = __uint_as_float(v.x & 0xffff0000u);
+        f[2] = __uint_as_float(v.y << 16);
+        f[3] = __uint_as_float(v.y & 0xffff0000u);
+    } else if constexpr (std::is_same<T, __nv_bfloat16>::value && PL == 2) {
+        const uint32_t v = *reinterpret_cast<const uint32_t *>(row + lane * 2);
+        f[0] = __uint_as_float(v << 16);
+        f[1] = __uint_as_float(v & 0xffff0000u);
+    } else if constexpr (std::is_same<T, float>::value && PL == 4) {
+        const float4 v = *reinterpret_cast<const float4 *>(row + lane * 4);
+        f[0] = v.x;
+        f[1] = v.y;
+        f[2] = v.z;
+        f[3] = v.w;
+    } else if constexpr (std::is_same<T, float>::value && PL == 2) {
+        const float2 v = *reinterpret_cast<const float2 *>(row + lane * 2);
+        f[0] = v.x;
+        f[1] = v.y;
+    } else {
 #pragma unroll
-    for (int e = 0; e < PL; ++e) f[e] = to_f(row[lane * PL + e]);
+        for (int e = 0; e < PL; ++e) f[e] = static_cast<float>(row[lane * PL + e]);
+    }
+}
+
+// fp32 row slice of this lane: store, or add to what is there (one vector access each way).
+template <int PL>
+__device__ __forceinline__ void store_row(float *__restrict__ row, int lane, const float (&f)[PL]) {
+    if constexpr (PL == 4) {
+        *reinterpret_cast<float4 *>(row + lane * 4) = make_float4(f[0], f[1], f[2], f[3]);
+    } else if constexpr (PL == 2) {
+        *reinterpret_cast<float2 *>(row + lane * 2) = make_float2(f[0], f[1]);
+    } else {
+#pragma unroll
+        for (int e = 0; e < PL; ++e) row[lane * PL + e] = f[e];
+    }
+}
+template <int PL>
+__device__ __forceinline__ void add_row(float *__restrict__ row, int lane, const float (&f)[PL]) {
+    float cur[PL];
+    load_row<float, PL>(row, lane, cur);
+#pragma unroll
+    for (int e = 0; e < PL; ++e) cur[e] += f[e];
+    store_row<PL>(row, lane, cur);
 }
 
 __device__ __forceinline__ float warp_sum(float x) {
@@ -103,8 +148,7 @@ __global__ void __launch_bounds__(128) bwd_dq_kernel(const T *__restrict__ Q, co
     const int nc = lo_of(i, a.w) / a.g;
     for (int j = 0; j < nc; ++j) visit(Kc + (bk * G + j) * D, Vc + (bk * G + j) * D);
     for (int m = win_of(a, i); m <= i; ++m) visit(K + (bk * a.N + m) * D, V + (bk * a.N + m) * D);
-#pragma unroll
-    for (int e = 0; e < PL; ++e) dQ[u * D + lane * PL + e] = dq[e];
+    store_row<PL>(dQ + u * D, lane, dq);
     if (lane == 0) Dbuf[u] = Di;
 }
 
@@ -159,11 +203,8 @@ __global__ void __launch_bounds__(128) bwd_dkv_raw_kernel(const T *__restrict__ 
                                          : static_cast<int64_t>(m) + a.w - 1;
     const int i1 = static_cast<int>(i_last < a.N - 1 ? i_last : a.N - 1);
     key_grad<T, D>(Q, dO, LSE, Dbuf, k, v, bk / a.Hkv, bk % a.Hkv, m, i1, a, lane, dk, dv);
-#pragma unroll
-    for (int e = 0; e < PL; ++e) {
-        dK[u * D + lane * PL + e] = dk[e];
-        dV[u * D + lane * PL + e] = dv[e];
-    }
+    store_row<PL>(dK + u * D, lane, dk);
+    store_row<PL>(dV + u * D, lane, dv);
 }
 
 template <typename T, int D>
@@ -218,12 +259,17 @@ __global__ void __launch_bounds__(128) bwd_pool_kernel(const T *__restrict__ Q, 
     const int64_t row0 = bk * a.N + static_cast<int64_t>(j) * g;  // first token of the group
     if (a.pool_mode == 1) {
         // mean pooling: every token weighs 1/g
-        for (int t = 0; t < g; ++t)
+        float ak[PL], av[PL];
 #pragma unroll
-            for (int e = 0; e < PL; ++e) {
-                dK[(row0 + t) * D + lane * PL + e] += dkc[e] / g;
-                dV[(row0 + t) * D + lane * PL + e] += dvc[e] / g;
-            }
+        for (int e = 0; e < PL; ++e) {
+            ak[e] = dkc[e] / g;
+            av[e] = dvc[e] / g;
+        }
+#pragma unroll 4
+        for (int t = 0; t < g; ++t) {
+            add_row<PL>(dK + (row0 + t) * D, lane, ak);
+            add_row<PL>(dV + (row0 + t) * D, lane, av);
+        }
         return;
     }
     if (a.pool_mode == 2) {
@@ -261,6 +307,7 @@ __global__ void __launch_bounds__(128) bwd_pool_kernel(const T *__restrict__ Q, 
     }
     // pass A: softmax normaliser of the group scores
     float mx = -INFINITY, den = 0.f;
+#pragma unroll 4
     for (int t = 0; t < g; ++t) {
         float k[PL];
         load_row<T, PL>(K + (row0 + t) * D, lane, k);
@@ -271,6 +318,7 @@ __global__ void __launch_bounds__(128) bwd_pool_kernel(const T *__restrict__ Q, 
     }
     // pass B: sum_u a_u da_u
     float sad = 0.f;
+#pragma unroll 4
     for (int t = 0; t < g; ++t) {
         float k[PL], v[PL];
         load_row<T, PL>(K + (row0 + t) * D, lane, k);
@@ -282,24 +330,24 @@ __global__ void __launch_bounds__(128) bwd_pool_kernel(const T *__restrict__ Q, 
     float dqs[PL];
 #pragma unroll
     for (int e = 0; e < PL; ++e) dqs[e] = 0.f;
+#pragma unroll 4
     for (int t = 0; t < g; ++t) {
         float k[PL], v[PL];
         load_row<T, PL>(K + (row0 + t) * D, lane, k);
         load_row<T, PL>(V + (row0 + t) * D, lane, v);
         const float at = expf(c * dot<PL>(qs, k) - mx) / den;
         const float ds = at * (dot<PL>(dkc, k) + dot<PL>(dvc, v) - sad);
+        float ak[PL], av[PL];
 #pragma unroll
         for (int e = 0; e < PL; ++e) {
-            dK[(row0 + t) * D + lane * PL + e] += at * dkc[e] + c * ds * qs[e];
-            dV[(row0 + t) * D + lane * PL + e] += at * dvc[e];
+            ak[e] = at * dkc[e] + c * ds * qs[e];
+            av[e] = at * dvc[e];
             dqs[e] = fmaf(c * ds, k[e], dqs[e]);
         }
+        add_row<PL>(dK + (row0 + t) * D, lane, ak);
+        add_row<PL>(dV + (row0 + t) * D, lane, av);
     }
-    for (int hh = 0; hh < r; ++hh) {
-        float *dst = dQ + ((b * a.Hq + kv * r + hh) * a.N + last) * D + lane * PL;
-#pragma unroll
-        for (int e = 0; e < PL; ++e) dst[e] += dqs[e];
-    }
+    for (int hh = 0; hh < r; ++hh) add_row<PL>(dQ + ((b * a.Hq + kv * r + hh) * a.N + last) * D, lane, dqs);
 }
 
 template <typename T, int D>
