@@ -86,3 +86,24 @@ def test_tensor_peak_follows_the_power_cap():
     assert p == 1700.0 and "sustained" in src
     p, src = bench.tensor_peak(peaks, "fallback", {"reasons": []})
     assert p == 1900.0 and "burst" in src
+
+
+def test_reference_arm_prints_one_contract_line():
+    """`bench.py --impl reference` (the fp64 oracle on the host cores) prints one JSON line
+    with the contract's keys, the same metric and unit as the CUDA arm, and an e2e object that
+    moves no bytes."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--steps", "1",
+                          "--warmup", "3"], capture_output=True, text=True, timeout=600, cwd=root)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [ln for ln in out.stdout.splitlines() if ln.strip()]
+    d = json.loads(lines[-1])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "tokens/s"
+    assert d["value"] > 0 and d["steps"] == 1 and d["warmup"] == 3 and d["higher_is_better"] is True
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    assert d["config"]["workload"] == bench.WORKLOADS["mha32k"].name
