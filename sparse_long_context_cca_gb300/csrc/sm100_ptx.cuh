@@ -117,82 +117,7 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
 }
-// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (bf16/f16 inputs, fp32 accumulate).
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                       uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-// D[tmem] (+)= A[tmem] * B[smem], kind::f16.
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                       uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
 
-// Eight K=16 steps of D[tmem] (+)= A[smem] * B[smem]^T over a 128-deep K with both operands
-// K-major 128-byte-swizzled tiles stored as two 64-column halves 16 KB apart.  The
-// descriptors passed are those of step 0; later steps add the start-address offset.
-// `accumulate` applies to step 0 only; steps 1..7 always accumulate.
-__device__ __forceinline__ void mma_ss_k128(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                            uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t.reg .b64 a, b;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
-        "add.s64 a, %1, 2;\n\tadd.s64 b, %2, 2;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, 1;\n\t"
-        "add.s64 a, %1, 4;\n\tadd.s64 b, %2, 4;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, 1;\n\t"
-        "add.s64 a, %1, 6;\n\tadd.s64 b, %2, 6;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, 1;\n\t"
-        "add.s64 a, %1, 1024;\n\tadd.s64 b, %2, 1024;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, 1;\n\t"
-        "add.s64 a, %1, 1026;\n\tadd.s64 b, %2, 1026;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, 1;\n\t"
-        "add.s64 a, %1, 1028;\n\tadd.s64 b, %2, 1028;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, 1;\n\t"
-        "add.s64 a, %1, 1030;\n\tadd.s64 b, %2, 1030;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, 1;\n\t"
-        "}"
-        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-// Eight K=16 steps of D[tmem] (+)= A[tmem] * B[smem] over a 128-deep K: A is bf16 in tensor
-// memory (8 columns per step), B an MN-major 128-byte-swizzled tile whose 16-row steps are
-// 2 KB apart.  `accumulate` applies to step 0 only.
-__device__ __forceinline__ void mma_ts_k128(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                            uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t.reg .b32 a;\n\t.reg .b64 b;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
-        "add.u32 a, %1, 8;\n\tadd.s64 b, %2, 128;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, 1;\n\t"
-        "add.u32 a, %1, 16;\n\tadd.s64 b, %2, 256;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, 1;\n\t"
-        "add.u32 a, %1, 24;\n\tadd.s64 b, %2, 384;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, 1;\n\t"
-        "add.u32 a, %1, 32;\n\tadd.s64 b, %2, 512;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, 1;\n\t"
-        "add.u32 a, %1, 40;\n\tadd.s64 b, %2, 640;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, 1;\n\t"
-        "add.u32 a, %1, 48;\n\tadd.s64 b, %2, 768;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, 1;\n\t"
-        "add.u32 a, %1, 56;\n\tadd.s64 b, %2, 896;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, 1;\n\t"
-        "}"
-        ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
 
 // Warp-collective forms: the whole warp executes them with warp-uniform operands and
 // elect.sync picks the one lane that issues.  Issuing from a full warp keeps the
@@ -205,6 +130,10 @@ __device__ __forceinline__ void tc_commit_warp(uint32_t bar) {
         "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
         : "memory");
 }
+// Eight K=16 steps of D[tmem] (+)= A[smem] * B[smem]^T over a 128-deep K (kind::f16: bf16
+// inputs, fp32 accumulate), both operands K-major 128-byte-swizzled tiles stored as two
+// 64-column halves 16 KB apart.  The descriptors passed are those of step 0; later steps
+// add the start-address offset.  `accumulate` applies to step 0 only.
 __device__ __forceinline__ void mma_ss_k128_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                                  uint32_t accumulate) {
     asm volatile(
@@ -230,6 +159,9 @@ __device__ __forceinline__ void mma_ss_k128_warp(uint32_t d_tmem, uint64_t a_des
         ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// Eight K=16 steps of D[tmem] (+)= A[tmem] * B[smem] over a 128-deep K: A is bf16 in
+// tensor memory (8 columns per step), B an MN-major 128-byte-swizzled tile whose 16-row
+// steps are 2 KB apart.  `accumulate` applies to step 0 only.
 __device__ __forceinline__ void mma_ts_k128_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
                                                  uint32_t accumulate) {
     asm volatile(
@@ -340,11 +272,6 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
         :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
         : "memory");
 }
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};"
-        :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-        : "memory");
-}
 __device__ __forceinline__ void tmem_wait_st() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -374,15 +301,6 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn_maj
 }
 
 
-// Warp-group register reallocation (all four warps of the warpgroup execute it).
-template <int N>
-__device__ __forceinline__ void setmaxnreg_inc() {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <int N>
-__device__ __forceinline__ void setmaxnreg_dec() {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-}
 
 
 // max(a, b, c) in one instruction.
