@@ -410,7 +410,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int bh = bh_of(it), i0 = i0_of(it);
         const uint32_t sQ = sm.tile[2 + 2 * (it & 1)], sdO = sm.tile[3 + 2 * (it & 1)];
         float *s_lse = sm.stage + (it & 1) * 2 * BT, *s_D = s_lse + BT;
-        if (t < BT) {  // stage the query tile's LSE (log2 units) and D
+        if (it == 0 && t < BT) {  // stage the first query tile's LSE (log2 units) and D
             const int iq = i0 + t;
             s_lse[t] = iq < p.N ? p.LSE[static_cast<int64_t>(bh) * p.N + iq] * LOG2E : 0.f;
             s_D[t] = iq < p.N ? p.Dbuf[static_cast<int64_t>(bh) * p.N + iq] : 0.f;
@@ -426,6 +426,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (!(ok = wait(b_mma, mma_phase++ & 1))) break;
         // in-order completion: the previous pair's MMAs are done, its Q/dO buffer is free
         if (t == 0 && it + 1 < n_it && !p.skip_loads) issue_q(it + 1);
+        // The next query tile's LSE and D: loaded now, so that they arrive during this step's
+        // element-wise work, and staged into the other buffer before this step's barrier
+        // (every wait is a CTA barrier, and a load staged at the top of the step held them all).
+        const bool pre = t < BT && it + 1 < n_it;
+        float n_lse = 0.f, n_D = 0.f;
+        if (pre) {
+            const int iq = i0_of(it + 1) + t;
+            const int64_t off = static_cast<int64_t>(bh_of(it + 1)) * p.N + iq;
+            if (iq < p.N) {
+                n_lse = p.LSE[off] * LOG2E;
+                n_D = p.Dbuf[off];
+            }
+        }
         ptx::tc_fence_after();
         // this key's visible query columns [q_lo, q_hi] of the tile
         int q_lo, q_hi;
@@ -470,6 +483,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
+        if (pre) {
+            float *n_stage = sm.stage + ((it + 1) & 1) * 2 * BT;
+            n_stage[t] = n_lse;
+            n_stage[BT + t] = n_D;
+        }
         __syncthreads();
         if (warp == 0) {
             ptx::tc_fence_after();
