@@ -113,7 +113,8 @@ def _shapes(Q, K):
 
 def pool(Q, K, V, g: int, scale: float | None = None, lib=None, pool_mode: int = 0):
     """Global-aware pooling -> (Kc, Vc), each [B, Hkv, N/g, d] fp64.
-    pool_mode 0: softmax weights of the group-last query (the method); 1: mean; 2: max."""
+    pool_mode 0: softmax weights of the group-last query (the method); 1: mean; 2: max;
+    3: each query head's own softmax weights, averaged over the heads sharing the KV head."""
     lib = lib or load()
     Q, K, V = widen(Q), widen(K), widen(V)
     B, Hq, Hkv, N, d = _shapes(Q, K)

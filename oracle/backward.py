@@ -12,7 +12,7 @@ Formulas ("Core Context Aware Transformers for Long Context Language
 Modeling", Method section, pooling and fusion equations), readings as in the C
 oracle: core j visible to query i iff (j+1)*g <= max(0, i-w+1); raw window
 [lo(i), i] (window_mode 1: [g*(lo(i)//g), i]); pool_mode 1 mean, 2 element-wise
-max.
+max, 3 per-query-head softmax weights averaged over the heads sharing a KV head.
 """
 from __future__ import annotations
 
@@ -40,6 +40,11 @@ def pool_dense(q, k, v, g: int, tau: float, pool_mode: int = 0):
         return Kg.gather(3, ik).squeeze(3), Vg.gather(3, iv).squeeze(3)
     if pool_mode == 1:
         a = torch.full((B, Hkv, G, g), 1.0 / g, dtype=q.dtype)
+    elif pool_mode == 3:
+        # one softmax per query head over its own logits, averaged over the r heads
+        qlast = q[:, :, g - 1::g].reshape(B, Hkv, r, G, d)
+        s = tau * torch.einsum("bkrjc,bkjtc->bkrjt", qlast, Kg)
+        a = torch.softmax(s, dim=-1).mean(dim=2)
     else:
         qlast = q[:, :, g - 1::g].reshape(B, Hkv, r, G, d)
         s = tau * torch.einsum("bkrjc,bkjtc->bkjt", qlast, Kg) / r

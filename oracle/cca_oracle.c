@@ -30,6 +30,12 @@
  *  - pool_mode 1, mean pooling: every token of the group weighs 1/g;
  *  - pool_mode 2, max pooling: the element-wise maximum of the group's keys
  *    and of its values (OpenReview rebuttal, pooling-ablation table);
+ *  - pool_mode 3, grouped-query pooling averaged after the softmax: every
+ *    query head sharing the KV head scores the group with its own last-token
+ *    query and takes its own softmax; the group weights are the mean of those
+ *    r weight vectors (the rebuttal leaves GQA pooling open; this is the other
+ *    plain way to let r heads share one pooled K/V, and it equals pool_mode 0
+ *    when r = 1);
  *  - window_mode 1, the window reaches back to the start of the group that
  *    holds lo(i): raw tokens [g*(lo(i)/g), i], so that together with the cores
  *    every earlier token is covered ("at least w preceding raw tokens").
@@ -73,6 +79,7 @@ void cca_oracle_pool_mode(const double *Q, const double *K, const double *V, dou
 #pragma omp parallel
     {
         double *s = (double *)malloc(sizeof(double) * (size_t)g);
+        double *wsum = (double *)malloc(sizeof(double) * (size_t)g);
 #pragma omp for schedule(static)
         for (int64_t u = 0; u < total; ++u) {
             const int64_t j = u % n_groups;
@@ -94,6 +101,35 @@ void cca_oracle_pool_mode(const double *Q, const double *K, const double *V, dou
                     acc += dot;
                 }
                 s[t] = scale * acc / (double)r;
+            }
+            if (pool_mode == 3) {
+                /* one softmax per query head over its own logits, then the mean of
+                 * the r weight vectors weights the group's keys and values */
+                for (int64_t t = 0; t < g; ++t) wsum[t] = 0.0;
+                for (int64_t hh = 0; hh < r; ++hh) {
+                    const int64_t h = kv * r + hh;
+                    const double *q = Q + ((b * Hq + h) * (int64_t)N + last) * d;
+                    for (int64_t t = 0; t < g; ++t) {
+                        const double *k = Kh + (j * g + t) * d;
+                        double dot = 0.0;
+                        for (int64_t c = 0; c < d; ++c) dot += q[c] * k[c];
+                        s[t] = scale * dot;
+                    }
+                    double hmx = s[0];
+                    for (int64_t t = 1; t < g; ++t) hmx = s[t] > hmx ? s[t] : hmx;
+                    double hden = 0.0;
+                    for (int64_t t = 0; t < g; ++t) hden += exp(s[t] - hmx);
+                    for (int64_t t = 0; t < g; ++t) wsum[t] += exp(s[t] - hmx) / hden / (double)r;
+                }
+                double *kc = Kc + (bk * n_groups + j) * d;
+                double *vc = Vc + (bk * n_groups + j) * d;
+                for (int64_t c = 0; c < d; ++c) { kc[c] = 0.0; vc[c] = 0.0; }
+                for (int64_t t = 0; t < g; ++t) {
+                    const double *k = Kh + (j * g + t) * d;
+                    const double *v = Vh + (j * g + t) * d;
+                    for (int64_t c = 0; c < d; ++c) { kc[c] += wsum[t] * k[c]; vc[c] += wsum[t] * v[c]; }
+                }
+                continue;
             }
             if (pool_mode == 1)
                 for (int64_t t = 0; t < g; ++t) s[t] = 0.0; /* mean pooling: equal weights */
@@ -130,6 +166,7 @@ void cca_oracle_pool_mode(const double *Q, const double *K, const double *V, dou
             }
         }
         free(s);
+        free(wsum);
     }
 }
 

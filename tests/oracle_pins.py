@@ -80,6 +80,56 @@ def pin_gqa_worked_example(lib):
     Kc, Vc = oracle.pool(Q, K, V, 2, lib=lib)
     np.testing.assert_allclose(Kc[0, 0, 0], gq["Kc0"], rtol=0, atol=1e-12)
     np.testing.assert_allclose(Vc[0, 0, 0], gq["Vc0"], rtol=0, atol=1e-12)
+    # the alternative GQA pooling: per-head softmax weights averaged after the softmax
+    pm = gq["post_softmax_mean"]
+    Kc, Vc = oracle.pool(Q, K, V, 2, lib=lib, pool_mode=3)
+    for j in (0, 1):
+        np.testing.assert_allclose(Kc[0, 0, j], pm["Kc%d" % j], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(Vc[0, 0, j], pm["Vc%d" % j], rtol=0, atol=1e-12)
+
+
+def pin_post_softmax_gqa_pooling(lib):
+    """pool_mode 3 against facts outside it: with one query head per KV head it is the
+    method's pooling (the worked example's hand values, and pool_mode 0 on random
+    inputs); with r heads it is the mean of r single-head poolings, each scored by one
+    head's own query (head h of KV head kv is query head kv*r + h)."""
+    ex = _golden("worked_example.json")
+    Q = np.array(ex["Q"], dtype=np.float64)[None, None]
+    K = np.array(ex["K"], dtype=np.float64)[None, None]
+    V = np.array(ex["V"], dtype=np.float64)[None, None]
+    Kc, Vc = oracle.pool(Q, K, V, ex["shape"]["g"], lib=lib, pool_mode=3)
+    np.testing.assert_allclose(Kc[0, 0], np.array(ex["pool"]["Kc"]), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(Vc[0, 0], np.array(ex["pool"]["Vc"]), rtol=0, atol=1e-12)
+    for (B, Hq, Hkv, N, d, g, seed) in [(1, 2, 2, 32, 8, 4, 80), (2, 4, 2, 36, 8, 3, 81),
+                                         (1, 8, 2, 40, 16, 5, 82), (1, 4, 1, 24, 8, 1, 83)]:
+        Q, K, V = _rand((B, Hq, N, d), seed, 2.0), _rand((B, Hkv, N, d), seed + 1), _rand((B, Hkv, N, d), seed + 2)
+        Kc, Vc = oracle.pool(Q, K, V, g, lib=lib, pool_mode=3)
+        r = Hq // Hkv
+        if r == 1:
+            Kc0, Vc0 = oracle.pool(Q, K, V, g, lib=lib, pool_mode=0)
+            np.testing.assert_allclose(Kc, Kc0, rtol=0, atol=1e-12)
+            np.testing.assert_allclose(Vc, Vc0, rtol=0, atol=1e-12)
+            continue
+        Km = np.zeros_like(Kc)
+        Vm = np.zeros_like(Vc)
+        for b in range(B):
+            for kv in range(Hkv):
+                for hh in range(r):
+                    q1 = Q[b:b + 1, kv * r + hh:kv * r + hh + 1]
+                    k1, v1 = K[b:b + 1, kv:kv + 1], V[b:b + 1, kv:kv + 1]
+                    Kh, Vh = oracle.pool(q1, k1, v1, g, lib=lib, pool_mode=0)
+                    Km[b, kv] += Kh[0, 0] / r
+                    Vm[b, kv] += Vh[0, 0] / r
+        np.testing.assert_allclose(Kc, Km, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(Vc, Vm, rtol=0, atol=1e-12)
+        Kc0, _ = oracle.pool(Q, K, V, g, lib=lib, pool_mode=0)
+        if g == 1:
+            # a one-token group pools to its token whatever the weights
+            np.testing.assert_array_equal(Kc, K)
+            np.testing.assert_array_equal(Kc0, K)
+        else:
+            # and it is not the logit mean of pool_mode 0 (the heads' queries differ)
+            assert np.abs(Kc - Kc0).max() > 1e-3
 
 
 def pin_visibility_counts(lib):
@@ -298,7 +348,8 @@ ALL_PINS = [pin_worked_example, pin_gqa_worked_example, pin_visibility_counts, p
             pin_wide_window_is_causal, pin_early_rows_are_sliding_window, pin_pool_equal_keys_mean,
             pin_pool_zero_query_mean, pin_pool_dominant_query_selects, pin_unit_values,
             pin_constant_keys_lse, pin_causality, pin_dense_mask_formulation,
-            pin_group_aligned_window_counts, pin_group_aligned_window_no_gap, pin_mean_pooling, pin_max_pooling]
+            pin_group_aligned_window_counts, pin_group_aligned_window_no_gap, pin_mean_pooling, pin_max_pooling,
+            pin_post_softmax_gqa_pooling]
 
 
 def _fd_check(Q, K, V, g, w, pool_mode, window_mode, lib, n_probe=6, seed=0, eps=1e-6):
@@ -325,7 +376,8 @@ def _fd_check(Q, K, V, g, w, pool_mode, window_mode, lib, n_probe=6, seed=0, eps
 def pin_backward_finite_differences(lib):
     B, Hq, Hkv, N, d = 1, 4, 2, 24, 8
     Q, K, V = _rand((B, Hq, N, d), 60), _rand((B, Hkv, N, d), 61), _rand((B, Hkv, N, d), 62)
-    for g, w, pm, wm, seed in ((4, 5, 0, 0, 1), (3, 7, 0, 1, 2), (4, 6, 1, 0, 3), (2, 3, 2, 0, 4)):
+    for g, w, pm, wm, seed in ((4, 5, 0, 0, 1), (3, 7, 0, 1, 2), (4, 6, 1, 0, 3), (2, 3, 2, 0, 4),
+                               (4, 5, 3, 0, 5), (3, 4, 3, 1, 6)):
         _fd_check(Q, K, V, g, w, pm, wm, lib, seed=seed)
 
 

@@ -46,6 +46,16 @@ MUTANTS = {
     "core_output_uses_keys": ("o[c] += a * Vch[j * d + c];", "o[c] += a * Kch[j * d + c];"),
     "local_keys_reversed": ("dot += q[c] * Kh[(lo + m) * d + c];", "dot += q[c] * Kh[(i - m) * d + c];"),
     "core_logit_uses_values": ("dot += q[c] * Kch[j * d + c];", "dot += q[c] * Vch[j * d + c];"),
+    "gqa_post_mean_no_1_over_r": ("wsum[t] += exp(s[t] - hmx) / hden / (double)r;",
+                                  "wsum[t] += exp(s[t] - hmx) / hden;"),
+    "gqa_post_mean_not_normalised_per_head": ("wsum[t] += exp(s[t] - hmx) / hden / (double)r;",
+                                              "wsum[t] += exp(s[t] - hmx) / (double)r;"),
+    "gqa_post_mean_is_logit_mean": ("if (pool_mode == 3) {", "if (pool_mode == 99) {"),
+    "gqa_post_mean_first_head_only": ("wsum[t] += exp(s[t] - hmx) / hden / (double)r;\n                }",
+                                      "wsum[t] += exp(s[t] - hmx) / hden / (double)r;\n                    break;\n                }"),
+    "gqa_post_mean_values_weighted_by_keys": ("vc[c] += wsum[t] * v[c];", "vc[c] += wsum[t] * k[c];"),
+    "gqa_post_mean_head_scale_dropped": ("s[t] = scale * dot;\n                    }\n                    double hmx",
+                                         "s[t] = dot;\n                    }\n                    double hmx"),
     "kv_head_interleaved": ("const int64_t bk = b * Hkv + h / r;\n            attend_row(Q + u * d",
                             "const int64_t bk = b * Hkv + h % Hkv;\n            attend_row(Q + u * d"),
 }
@@ -89,7 +99,7 @@ def test_backward_forward_matches_c_oracle():
     from oracle.backward import dense_forward
     rng = np.random.default_rng(70)
     Q, K, V = (rng.standard_normal(s) for s in ((2, 4, 32, 8), (2, 2, 32, 8), (2, 2, 32, 8)))
-    for g, w, pm, wm in ((4, 5, 0, 0), (8, 9, 1, 1), (2, 3, 2, 0)):
+    for g, w, pm, wm in ((4, 5, 0, 0), (8, 9, 1, 1), (2, 3, 2, 0), (4, 6, 3, 0), (2, 5, 3, 1)):
         O, L = dense_forward(torch.tensor(Q), torch.tensor(K), torch.tensor(V), g, w, pool_mode=pm, window_mode=wm)
         Or, Lr, _, _ = oracle.prefill(Q, K, V, g, w, pool_mode=pm, window_mode=wm)
         np.testing.assert_allclose(O.numpy(), Or, rtol=0, atol=1e-12)
