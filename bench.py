@@ -4,7 +4,12 @@ One step = one full prefill pass (cca_pool then cca_attn_fwd) over one batch
 of synthetic inputs already resident in HBM.  Prints one JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload mha32k|mha128k|gqa64k]
-                  [--impl cca|reference] [--no-e2e] [--no-cpu-baseline]
+                  [--impl cca|reference] [--no-e2e] [--no-cpu-baseline] [--no-sweep]
+
+Besides the headline workload, the default run times the 128K MHA workload, the
+GQA 64K workload (with both GQA pooling modes) and the 12 points of the g x w
+sweep, each over at least 10 timed steps and 0.3 s, each with the clock record
+of its own timed region and the tensor peak that record selects.
 
 Under torchrun (N > 1) every rank runs an independent replica of the workload
 on its own GPU (no data-path collective: batches are independent), so the
@@ -100,20 +105,28 @@ class ClockSampler:
             self.lines.append((time.monotonic(), line.strip()))
 
     def stop(self, window=None):
-        """Clock summary over the samples taken inside `window` (host monotonic times
-        bracketing the timed region).  When the region is shorter than the sampling
-        interval and no sample falls inside it, the two samples around it are used."""
+        """Stop sampling; the clock summary over `window` (see summary)."""
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+            return self.summary(window)
         time.sleep(0.15)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+        return self.summary(window)
+
+    def summary(self, window=None):
+        """Clock summary over the samples taken inside `window` (host monotonic times
+        bracketing one timed region).  When the region is shorter than the sampling
+        interval and no sample falls inside it, the two samples around it are used."""
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         rows = []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for t, ln in self.lines:
+        for t, ln in list(self.lines):
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 8:
                 continue
@@ -185,6 +198,25 @@ def time_steps(fn, steps, stream):
     return start, end
 
 
+def bench_config(wl, world):
+    """The workload description both arms print as `config`."""
+    return {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "N": wl.N, "d": wl.d,
+            "g": wl.g, "w": wl.w, "global_batch": wl.B * world, "seq_len": wl.N,
+            "parallelism": f"replicas x{world}",
+            "l2": "inputs larger than L2 (%.0f MB of Q/K/V vs 129 MB), no flush" % (
+                (wl.B * wl.Hq + 2 * wl.B * wl.Hkv) * wl.N * wl.d * 2 / 1e6)}
+
+
+MIN_ROW_STEPS = 10
+MIN_ROW_SECONDS = 0.3
+
+
+def row_steps(est_ms: float) -> int:
+    """Timed steps of a secondary row: at least MIN_ROW_STEPS and MIN_ROW_SECONDS (so that
+    the row's own clock record holds several samples), at most 300."""
+    return int(min(300, max(MIN_ROW_STEPS, -(-MIN_ROW_SECONDS * 1e3 // max(est_ms, 1e-3)))))
+
+
 def run_cca(args, rank, world, local):
     from sparse_long_context_cca_gb300 import api
     from sparse_long_context_cca_gb300.inputs import make_qkv
@@ -196,29 +228,38 @@ def run_cca(args, rank, world, local):
     peaks, peak_src = load_peaks()
     stream = torch.cuda.current_stream()
 
-    def measure(wl, steps, warmup):
+    def measure(wl, steps, warmup, pool_mode=0):
+        """Times `steps` prefill steps (cca_pool + cca_attn_fwd) after `warmup` untimed ones.
+        steps=None picks the count from the warm-up's own timing (row_steps).  Returns
+        (total ms, mean pooling ms, mean attention ms, steps, host window)."""
         Q, K, V = make_qkv(wl, dev)
         G = wl.N // wl.g
         Kc = torch.empty((wl.B, wl.Hkv, G, wl.d), dtype=Q.dtype, device=dev)
         Vc = torch.empty_like(Kc)
         O = torch.empty_like(Q)
         LSE = torch.empty((wl.B, wl.Hq, wl.N), dtype=torch.float32, device=dev)
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-               torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
 
         def step(e=None):
             if e is not None:
                 e[0].record(stream)
-            api.cca_pool(Q, K, V, wl.g, Kc, Vc, stream=stream)
+            api.cca_pool(Q, K, V, wl.g, Kc, Vc, stream=stream, pool_mode=pool_mode)
             if e is not None:
                 e[1].record(stream)
             api.cca_attn_fwd(Q, K, V, Kc, Vc, wl.g, wl.w, O, LSE, stream=stream)
             if e is not None:
                 e[2].record(stream)
 
+        w0 = torch.cuda.Event(enable_timing=True)
+        w1 = torch.cuda.Event(enable_timing=True)
+        w0.record(stream)
         for _ in range(warmup):
             step()
+        w1.record(stream)
         torch.cuda.synchronize()
+        if steps is None:
+            steps = row_steps(w0.elapsed_time(w1) / max(1, warmup))
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+               torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
         if world > 1:
             torch.distributed.barrier()
         torch.cuda.synchronize()
@@ -231,7 +272,6 @@ def run_cca(args, rank, world, local):
         t1.record(stream)
         torch.cuda.synchronize()
         h1 = time.monotonic()
-        window[:] = [h0, h1]
         if world > 1:
             torch.distributed.barrier()
         total_ms = t0.elapsed_time(t1)
@@ -240,13 +280,31 @@ def run_cca(args, rank, world, local):
         assert torch.isfinite(LSE).all()
         del Q, K, V, O, LSE, Kc, Vc
         torch.cuda.empty_cache()
-        return total_ms, statistics.mean(pool_ms), statistics.mean(attn_ms)
+        return total_ms, statistics.mean(pool_ms), statistics.mean(attn_ms), steps, (h0, h1)
 
-    window = []  # host times around the timed region, set by measure()
+    def row(wl, pool_mode=0, note=None):
+        """One secondary workload with its own clock record and peak."""
+        tot, pm, am, steps, win = measure(wl, None, 3, pool_mode)
+        ck = sampler.summary(win)
+        tp, tp_src = tensor_peak(peaks, peak_src, ck)
+        flops, pbytes = W.attn_flops(wl), W.pool_bytes(wl)
+        r = {"workload": wl.name, "steps": steps, "warmup": 3, "ms_per_step": tot / steps,
+             "tokens_per_s": wl.B * wl.N / (tot / steps / 1e3),
+             "attn_ms": am, "attn_eff_tflops": flops / (am / 1e3) / 1e12,
+             "attn_frac": flops / (am / 1e3) / 1e12 / tp, "attn_peak": tp, "attn_peak_source": tp_src,
+             "pool_ms": pm, "pool_gbs": pbytes / (pm / 1e3) / 1e9,
+             "pool_frac": pbytes / (pm / 1e3) / 1e9 / peaks["hbm_gbs"],
+             "attn_flops": flops, "pool_bytes": pbytes, "clocks": ck}
+        if pool_mode:
+            r["pool_mode"] = pool_mode
+        if note:
+            r["note"] = note
+        return r
+
     sampler = ClockSampler(local)
     sampler.start()
-    total_ms, pool_ms, attn_ms = measure(wl, args.steps, args.warmup)
-    clocks = sampler.stop(tuple(window) if window else None)
+    total_ms, pool_ms, attn_ms, _, window = measure(wl, args.steps, args.warmup)
+    clocks = sampler.summary(window)
     tpeak, tpeak_src = tensor_peak(peaks, peak_src, clocks)
     total_ms = max_over_ranks(total_ms, world, dev)
     ms_per_step, value = job_throughput(total_ms, args.steps, wl.B * wl.N, world)
@@ -260,11 +318,7 @@ def run_cca(args, rank, world, local):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded normal Q/K/V, 1% heavy-hitter keys)",
-        "config": {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "N": wl.N, "d": wl.d,
-                   "g": wl.g, "w": wl.w, "global_batch": wl.B * world, "seq_len": wl.N,
-                   "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2 (%.0f MB of Q/K/V vs 129 MB), no flush" % (
-                       3 * wl.B * wl.Hq * wl.N * wl.d * 2 / 1e6)},
+        "config": bench_config(wl, world),
         "attn_eff_tflops": attn_tflops,
         "attn_ms": attn_ms, "pool_ms": pool_ms,
         "pool_gbs": pool_gbs,
@@ -283,32 +337,17 @@ def run_cca(args, rank, world, local):
         "gpu_launches": 2 * args.steps,
     }
     if args.also_128k and wl is not W.MHA_128K:
-        window = []
-        sampler2 = ClockSampler(local)
-        sampler2.start()
-        tot, pm, am = measure(W.MHA_128K, max(3, args.steps // 4), 3)
-        clocks2 = sampler2.stop(tuple(window) if window else None)
-        tpeak2, tpeak2_src = tensor_peak(peaks, peak_src, clocks2)
-        wl2 = W.MHA_128K
-        out["mha128k"] = {"workload": wl2.name, "tokens_per_s": wl2.B * wl2.N / (tot / max(3, args.steps // 4) / 1e3),
-                          "attn_ms": am, "pool_ms": pm,
-                          "attn_eff_tflops": W.attn_flops(wl2) / (am / 1e3) / 1e12,
-                          "attn_frac": W.attn_flops(wl2) / (am / 1e3) / 1e12 / tpeak2,
-                          "attn_peak_source": tpeak2_src,
-                          "pool_gbs": W.pool_bytes(wl2) / (pm / 1e3) / 1e9,
-                          "pool_frac": W.pool_bytes(wl2) / (pm / 1e3) / 1e9 / peaks["hbm_gbs"],
-                          "clocks": clocks2}
+        r = row(W.MHA_128K)
+        r["attn_traffic"] = recorded_traffic(kfile, "mha128k")
+        r["pool_traffic"] = recorded_traffic(pfile, "mha128k")
+        out["mha128k"] = r
     if args.sweep:
-        # the other synthetic workloads (GQA 64K and the g x w sweep), same method, 3 timed steps
-        rows = []
-        for wl3 in [W.GQA_64K] + W.sweep():
-            tot, pm, am = measure(wl3, 3, 3)
-            rows.append({"workload": wl3.name, "tokens_per_s": wl3.B * wl3.N / (tot / 3 / 1e3),
-                         "attn_ms": am, "attn_eff_tflops": W.attn_flops(wl3) / (am / 1e3) / 1e12,
-                         "attn_frac": W.attn_flops(wl3) / (am / 1e3) / 1e12 / peaks["bf16_tflops"],
-                         "pool_ms": pm, "pool_gbs": W.pool_bytes(wl3) / (pm / 1e3) / 1e9,
-                         "pool_frac": W.pool_bytes(wl3) / (pm / 1e3) / 1e9 / peaks["hbm_gbs"]})
-        out["sweep"] = rows
+        # the other synthetic workloads: GQA 64K (both GQA pooling modes) and the g x w sweep
+        rows = [row(W.GQA_64K) if wl is not W.GQA_64K else None,
+                row(W.GQA_64K, pool_mode=3, note="alternative GQA pooling: per-head softmax weights "
+                                                 "averaged over the 4 heads sharing a KV head")]
+        out["gqa64k"] = [x for x in rows if x is not None]
+        out["sweep"] = [row(w3) for w3 in W.sweep()]
     if args.decode:
         out["decode"] = decode_bench(wl, dev, stream, 50, peaks)
         if args.also_128k and wl is not W.MHA_128K:
@@ -317,6 +356,7 @@ def run_cca(args, rank, world, local):
         out["backward"] = backward_bench(wl, dev, stream, 2, peaks)
     if args.comparator:
         out["full_attention_comparator"] = comparator(wl, dev, stream, max(3, args.steps // 4), ms_per_step)
+    sampler.stop()
     if not args.no_e2e:
         out["e2e"] = e2e(wl, dev, stream, max(3, args.steps // 2), world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -495,12 +535,37 @@ def oracle_sample(wl, seconds_budget, row_frac=1.0):
     return wl.B * wl.N / step_seconds, oracle.threads(), desc, step_seconds
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the platform string)."""
+    try:
+        outp = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in outp.splitlines():
+            if ln.strip().lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for ln in open("/proc/cpuinfo"):
+            if ln.lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
 def cpu_baseline(wl, seconds):
     v, cores, desc, _ = oracle_sample(wl, seconds)
-    return {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc}
+    return {"value": v, "unit": "tokens/s", "cores": cores, "cpu_model": cpu_model(), "nproc": os.cpu_count(),
+            "kind": "oracle", "sample": desc}
 
 
 def run_reference(args, rank, world):
+    """The fp64 oracle on the host cores, on the same workload as the CUDA arm.  Each step
+    times a bounded sample of the workload (whole heads, or a fraction of one head's rows
+    when the run is long) and scales it to the whole workload: `value` is that scaled
+    tokens/s, `ms_per_step` the wall time each sampled step really took, and
+    `extrapolated_ms_per_step` the time the whole workload would take."""
     if rank != 0:
         return None
     wl = WORKLOADS[args.workload]
@@ -512,17 +577,21 @@ def run_reference(args, rank, world):
     for _ in range(args.warmup):
         oracle_sample(wl, 0.0, frac)
     desc = cores = None
+    t0 = time.perf_counter()
     for _ in range(args.steps):
         v, cores, desc, _ = oracle_sample(wl, 0.0, frac)
         vals.append(v)
+    wall = time.perf_counter() - t0
     value = statistics.mean(vals)
     return {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": wl.B * wl.N / value * 1e3, "higher_is_better": True,
+            "warmup": args.warmup, "ms_per_step": wall / args.steps * 1e3,
+            "extrapolated_ms_per_step": wl.B * wl.N / value * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "impl": "reference",
-            "config": {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "N": wl.N, "d": wl.d,
-                       "g": wl.g, "w": wl.w, "parallelism": "cpu oracle, rank 0"},
-            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "config": bench_config(wl, world),
+            "runs_on": "host CPU, rank 0 (the fp64 oracle)",
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "cpu_model": cpu_model(),
+                             "nproc": os.cpu_count(), "kind": "oracle",
                              "sample": "each step: " + desc},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
@@ -541,8 +610,8 @@ def main():
     ap.add_argument("--no-comparator", dest="comparator", action="store_false")
     ap.add_argument("--no-decode", dest="decode", action="store_false")
     ap.add_argument("--no-backward", dest="backward", action="store_false")
-    ap.add_argument("--sweep", action="store_true",
-                    help="also time the GQA 64K workload and the 12 g x w sweep points")
+    ap.add_argument("--no-sweep", dest="sweep", action="store_false",
+                    help="skip the GQA 64K workload and the 12 g x w sweep points")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

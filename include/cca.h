@@ -88,8 +88,16 @@ typedef struct cca_params {
     int32_t window_mode;/* 0: raw window [lo(i), i] (the method as read here);
                            1: raw window [g*(lo(i)/g), i], reaching back to the group boundary
                               so that cores + window cover every earlier token */
-    int32_t pool_mode;  /* 0: softmax weights of the group-last query (the method);
-                           1: mean pooling; 2: element-wise max pooling (the pages' ablations) */
+    int32_t pool_mode;  /* 0: softmax weights of the group-last query (the method; with
+                              grouped-query attention the r heads' logits are averaged
+                              before the softmax);
+                           1: mean pooling; 2: element-wise max pooling (the pages' ablations);
+                           3: grouped-query pooling averaged after the softmax: each of the
+                              r = Hq/Hkv query heads takes its own softmax over the group,
+                              scored by its own group-last query, and the group weights are
+                              the mean of the r weight vectors (the OpenReview rebuttal's
+                              GQA answer leaves this choice open).  Equals 0 when r = 1.
+                              Needs r <= 8 (else CCA_ERR_UNSUPPORTED). */
 } cca_params_t;
 
 /*
@@ -165,7 +173,9 @@ uint64_t cca_decode_workspace_size(const cca_params_t *params);
  *
  * The first call on a device (with that device current) looks up the array's
  * device address with cudaGetSymbolAddress; make that first call before any
- * stream capture.  All calls share the one array: calls whose kernels may
+ * stream capture.  The address is kept together with the CUDA context that was
+ * current then; a call made under another context (after cudaDeviceReset, for
+ * instance) looks it up again, and is then such a first call.  All calls share the one array: calls whose kernels may
  * overlap on a GPU (different streams without ordering) race on it and give
  * undefined results.  Nothing in it needs to start at zero: every call
  * rewrites each partial it later reads.

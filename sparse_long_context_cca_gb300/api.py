@@ -137,7 +137,9 @@ def _dims(Q, K):
 
 def cca_pool(Q, K, V, g: int, Kc=None, Vc=None, scale: float = 0.0, stream=None, pool_mode: int = 0):
     """Global-aware pooling: returns (Kc, Vc), each [B, Hkv, N/g, d].
-    pool_mode 0: softmax weights of the group-last query; 1: mean; 2: element-wise max."""
+    pool_mode 0: softmax weights of the group-last query (GQA: the r heads' logits averaged);
+    1: mean; 2: element-wise max; 3: GQA pooling averaged after the softmax (each query head's
+    own softmax weights, averaged over the r heads sharing the KV head; r <= 8)."""
     lib = load_library()
     B, Hq, Hkv, N, d = _dims(Q, K)
     if Q.dtype not in _DTYPE:

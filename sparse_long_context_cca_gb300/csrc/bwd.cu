@@ -14,7 +14,11 @@
 //   dk_t += a_t dKc_j + (tau / r) ds_t qsum,   dv_t += a_t dVc_j
 //   dq^h_last += (tau / r) sum_t ds_t k_t      for each of the r heads.
 // Mean pooling has a_t = 1/g and no score gradient; max pooling passes each
-// element's gradient to the row that holds the maximum.
+// element's gradient to the row that holds the maximum.  pool_mode 3 has
+// a_t = (1/r) sum_h p^h_t with p^h = softmax_t(tau q^h_last . k_t) per head:
+//   ds^h_t = p^h_t (da_t - sum_u p^h_u da_u) / r
+//   dk_t += a_t dKc_j + tau sum_h ds^h_t q^h_last,   dv_t += a_t dVc_j
+//   dq^h_last += tau sum_t ds^h_t k_t.
 //
 // Four passes on CUDA cores in fp32 (one warp per row; lane l holds d/32
 // consecutive elements): per query row (dQ, D), per raw token (dK, dV), per
@@ -290,6 +294,57 @@ __global__ void __launch_bounds__(128) bwd_pool_kernel(const T *__restrict__ Q, 
         for (int e = 0; e < PL; ++e) {
             dK[(row0 + kt[e]) * D + lane * PL + e] += dkc[e];
             dV[(row0 + vt[e]) * D + lane * PL + e] += dvc[e];
+        }
+        return;
+    }
+    if (a.pool_mode == 3) {
+        // per-head softmax weights averaged over the r heads: head by head, its
+        // normaliser, sum_u p_u da_u, then its share of every row's gradient
+        const int last3 = (j + 1) * g - 1;
+        for (int hh = 0; hh < r; ++hh) {
+            const int64_t qrow = (b * a.Hq + kv * r + hh) * a.N + last3;
+            float qh[PL];
+            load_row<T, PL>(Q + qrow * D, lane, qh);
+            float mx = -INFINITY, den = 0.f;
+#pragma unroll 4
+            for (int t = 0; t < g; ++t) {
+                float k[PL];
+                load_row<T, PL>(K + (row0 + t) * D, lane, k);
+                const float s = a.tau * dot<PL>(qh, k);
+                const float mn = fmaxf(mx, s);
+                den = den * expf(mx - mn) + expf(s - mn);
+                mx = mn;
+            }
+            float sad = 0.f;
+#pragma unroll 4
+            for (int t = 0; t < g; ++t) {
+                float k[PL], v[PL];
+                load_row<T, PL>(K + (row0 + t) * D, lane, k);
+                load_row<T, PL>(V + (row0 + t) * D, lane, v);
+                const float pt = expf(a.tau * dot<PL>(qh, k) - mx) / den;
+                sad += pt * (dot<PL>(dkc, k) + dot<PL>(dvc, v));
+            }
+            float dqh[PL];
+#pragma unroll
+            for (int e = 0; e < PL; ++e) dqh[e] = 0.f;
+#pragma unroll 4
+            for (int t = 0; t < g; ++t) {
+                float k[PL], v[PL];
+                load_row<T, PL>(K + (row0 + t) * D, lane, k);
+                load_row<T, PL>(V + (row0 + t) * D, lane, v);
+                const float pt = expf(a.tau * dot<PL>(qh, k) - mx) / den;
+                const float ds = pt * (dot<PL>(dkc, k) + dot<PL>(dvc, v) - sad) / r;
+                float ak[PL], av[PL];
+#pragma unroll
+                for (int e = 0; e < PL; ++e) {
+                    ak[e] = (pt / r) * dkc[e] + a.tau * ds * qh[e];
+                    av[e] = (pt / r) * dvc[e];
+                    dqh[e] = fmaf(a.tau * ds, k[e], dqh[e]);
+                }
+                add_row<PL>(dK + (row0 + t) * D, lane, ak);
+                add_row<PL>(dV + (row0 + t) * D, lane, av);
+            }
+            add_row<PL>(dQ + qrow * D, lane, dqh);
         }
         return;
     }

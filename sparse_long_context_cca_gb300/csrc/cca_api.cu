@@ -26,8 +26,10 @@ int check_shape(const cca_params_t *p, bool need_w) {
     if (p->Hq % p->Hkv != 0 || p->N % p->g != 0) return CCA_ERR_INVALID_ARG;
     if (p->dtype != CCA_BF16 && p->dtype != CCA_F32) return CCA_ERR_INVALID_ARG;
     if (!(p->scale == p->scale) || isinf(p->scale)) return CCA_ERR_INVALID_ARG;
-    if (p->window_mode < 0 || p->window_mode > 1 || p->pool_mode < 0 || p->pool_mode > 2)
+    if (p->window_mode < 0 || p->window_mode > 1 || p->pool_mode < 0 || p->pool_mode > 3)
         return CCA_ERR_INVALID_ARG;
+    // pool_mode 3 keeps a running (max, sum) per query head of a KV head: at most 8
+    if (p->pool_mode == 3 && p->Hq / p->Hkv > 8) return CCA_ERR_UNSUPPORTED;
     // Element counts of the largest tensor must fit the kernels' 64-bit indexing and
     // row counts the 32-bit tensor-map coordinates.
     const double elems = static_cast<double>(p->B) * p->Hq * p->N * p->d;

@@ -15,6 +15,15 @@
 // copies of chunks c+1 .. c+S-1.  Within a chunk a lane holds one 16-byte
 // vector of a row; logits are reduced with shuffles and a running (max, sum)
 // carries a group across chunks, so any g works.  Outputs are 16-byte stores.
+//
+// pool_mode 3 (grouped-query pooling averaged after the softmax): each of the r
+// query heads sharing the KV head takes its own softmax over the group and the
+// group weights are the mean of the r weight vectors.  Every chunk then carries
+// the r query rows.  A group that fits one chunk is done in one pass: head by
+// head, the chunk's logits give that head's final (max, sum) and its weights add
+// into one weight per row.  A longer group is streamed twice: a first pass over
+// its K rows only gathers every head's running (max, sum); the second pass over
+// K and V recomputes the logits and sums the weighted rows.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -30,6 +39,7 @@ namespace {
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int NW_MAX = 12;                 // warps per CTA (each feeds and consumes its own ring)
 constexpr int S_MAX = 8;                   // ring stages per warp
+constexpr int HM_MAX = 8;                  // pool_mode 3: query heads per KV head
 constexpr uint32_t CHUNK_BYTES = 4096;     // bytes of K (and of V) per chunk
 constexpr uint32_t SMEM_BUDGET = 224 * 1024;
 constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;
@@ -78,8 +88,11 @@ struct PoolArgs {
     int S;                 // ring stages per warp
     uint32_t v_off;        // bytes of one chunk's K rows (V follows them, then the query rows)
     uint32_t stage_bytes;  // K chunk + V chunk + r query rows
-    float logit_scale;     // tau * log2(e) / r (0 for mean pooling: equal weights)
+    float logit_scale;     // tau * log2(e) / r (0 for mean pooling: equal weights;
+                           // tau * log2(e) for pool_mode 3, whose logits are per head)
     int pool_max;          // element-wise max pooling instead of weighted sums
+    int headmean;          // pool_mode 3: per-head softmax weights averaged over the r heads
+    int npass;             // chunk passes over a group: 2 for pool_mode 3 with more than one chunk
     int64_t n_groups;      // B * Hkv * (N / g)
     int32_t *status;
 };
@@ -104,6 +117,7 @@ __global__ void __launch_bounds__(NW_MAX * 32) pool_kernel(const T *__restrict__
 
     extern __shared__ __align__(128) uint8_t smem_raw[];
     __shared__ uint64_t bars[NW_MAX][S_MAX];
+    __shared__ float2 head_ml[NW_MAX][HM_MAX];  // pool_mode 3: per-head running (max, sum)
     __shared__ int abort_flag;
     const int lane = threadIdx.x & 31;
     const int wib = threadIdx.x >> 5;
@@ -117,12 +131,13 @@ __global__ void __launch_bounds__(NW_MAX * 32) pool_kernel(const T *__restrict__
 
     const uint32_t ring = ptx::smem_addr(smem_raw) + wib * a.S * a.stage_bytes;
     const int G = a.N / a.g;
-    const int nch = (a.g + RS - 1) / RS;  // chunks per group
+    const int nch = (a.g + RS - 1) / RS;  // chunks per group and pass
+    const int ncg = nch * a.npass;         // chunks per group
     const int nw = blockDim.x >> 5;
     const int64_t tw = static_cast<int64_t>(gridDim.x) * nw;
     const int64_t gw = static_cast<int64_t>(blockIdx.x) * nw + wib;
     const int64_t my_groups = gw < a.n_groups ? (a.n_groups - 1 - gw) / tw + 1 : 0;
-    const int64_t n_chunks = my_groups * nch;
+    const int64_t n_chunks = my_groups * ncg;
 
     // Lane 0 brings the warp's chunks into its ring in stream order.  The cursor
     // (stage, chunk of the group, group index j, (b, kv) row bk) advances by counting,
@@ -130,18 +145,20 @@ __global__ void __launch_bounds__(NW_MAX * 32) pool_kernel(const T *__restrict__
     int is = 0, ich = 0;
     int64_t ij = gw % G, ibk = gw / G;
     auto issue = [&]() {
-        const int ch = ich;
+        const int ch = ich % nch;                             // chunk within the pass
+        const bool with_v = a.npass == 1 || ich >= nch;       // the first of two passes reads K only
+        const bool with_q = ch == 0 || a.headmean;            // pool_mode 3 scores every chunk per head
         const int64_t j = ij, bk = ibk;
         const int t0 = ch * RS;
         const int rows = min(RS, a.g - t0);
         const uint32_t stage = ring + static_cast<uint32_t>(is) * a.stage_bytes;
         const uint32_t bar = ptx::smem_addr(&bars[wib][is]);
         const uint32_t kv_bytes = rows * ROW_BYTES;
-        ptx::mbar_arrive_expect_tx(bar, 2 * kv_bytes + (ch == 0 ? a.r * ROW_BYTES : 0));
+        ptx::mbar_arrive_expect_tx(bar, (with_v ? 2 : 1) * kv_bytes + (with_q ? a.r * ROW_BYTES : 0));
         const int64_t row0 = bk * a.N + j * a.g + t0;
         ptx::bulk_load(stage, K + row0 * D, kv_bytes, bar);
-        ptx::bulk_load(stage + a.v_off, V + row0 * D, kv_bytes, bar);
-        if (ch == 0) {
+        if (with_v) ptx::bulk_load(stage + a.v_off, V + row0 * D, kv_bytes, bar);
+        if (with_q) {
             const int64_t b = bk / a.Hkv, kv = bk % a.Hkv;
             const int64_t last = (j + 1) * a.g - 1;
             for (int hh = 0; hh < a.r; ++hh)
@@ -150,7 +167,7 @@ __global__ void __launch_bounds__(NW_MAX * 32) pool_kernel(const T *__restrict__
                                bar);
         }
         if (++is == a.S) is = 0;
-        if (++ich == nch) {
+        if (++ich == ncg) {
             ich = 0;
             ij += tw;  // next group of this warp: gid += tw
             if (ij >= G) {
@@ -166,7 +183,7 @@ __global__ void __launch_bounds__(NW_MAX * 32) pool_kernel(const T *__restrict__
     float q[E], ak[E], av[E];
     float m = -INFINITY, l = 0.f;
     int64_t c = 0;
-    int st = 0, ch = 0;   // consumer's stage and chunk-of-group counters
+    int st = 0, ch = 0;   // consumer's stage and chunk-of-group counters (ch < ncg)
     uint32_t ph = 0;      // parity of the stage barrier's current use
     int64_t gid = gw;     // consumer's group
     for (; c < n_chunks; ++c) {
@@ -174,9 +191,12 @@ __global__ void __launch_bounds__(NW_MAX * 32) pool_kernel(const T *__restrict__
         volatile int *af = &abort_flag;
         if (!__all_sync(kFull, ptx::wait_bounded(ptx::smem_addr(&bars[wib][st]), ph, af, WAIT_LIMIT_NS)))
             break;
-        const int t0 = ch * RS;
+        const int t0 = (ch % nch) * RS;
         const int rows = min(RS, a.g - t0);
-        if (ch == 0) {
+        if (ch == 0 && a.headmean) {
+#pragma unroll
+            for (int e = 0; e < E; ++e) ak[e] = av[e] = 0.f;
+        } else if (ch == 0) {
             // new group: sum of the r group-last queries (1/r is in logit_scale)
             const float init = a.pool_max ? -INFINITY : 0.f;
 #pragma unroll
@@ -196,17 +216,77 @@ __global__ void __launch_bounds__(NW_MAX * 32) pool_kernel(const T *__restrict__
         constexpr int PASSES = RS / RPI;
         uint4 kr[PASSES], vr[PASSES];
         float s[PASSES];
+        const bool first_pass = a.npass == 1 || ch < nch;  // gathers pool_mode 3's per-head (max, sum)
+        const bool last_pass = a.npass == 1 || ch >= nch;  // the chunk's V rows are in the stage
 #pragma unroll
         for (int it = 0; it < PASSES; ++it) {
             const int t = it * RPI + sub;
             if (t < rows) {
                 kr[it] = lds16(stage + t * ROW_BYTES + cl * 16);
-                vr[it] = lds16(stage + a.v_off + t * ROW_BYTES + cl * 16);
+                vr[it] = last_pass ? lds16(stage + a.v_off + t * ROW_BYTES + cl * 16) : make_uint4(0, 0, 0, 0);
             } else {
                 kr[it] = vr[it] = make_uint4(0, 0, 0, 0);
             }
         }
-        if (a.pool_max) {
+        if (a.headmean) {
+            // pool_mode 3: weight of row t = (1/r) sum_h 2^(s_h,t - m_h) / l_h
+            float wgt[PASSES];
+#pragma unroll
+            for (int it = 0; it < PASSES; ++it) wgt[it] = 0.f;
+#pragma unroll 1
+            for (int hh = 0; hh < a.r; ++hh) {
+                float qh[E];
+                VT::unpack(lds16(stage + 2 * a.v_off + hh * ROW_BYTES + cl * 16), qh);
+#pragma unroll
+                for (int it = 0; it < PASSES; ++it) {
+                    float f[E];
+                    VT::unpack(kr[it], f);
+                    float p = 0.f;
+#pragma unroll
+                    for (int e = 0; e < E; ++e) p = fmaf(qh[e], f[e], p);
+#pragma unroll
+                    for (int o = LPR / 2; o > 0; o >>= 1) p += __shfl_xor_sync(kFull, p, o);
+                    s[it] = (it * RPI + sub < rows) ? p * a.logit_scale : -INFINITY;  // log2 domain
+                }
+                float2 ml = (ch % nch == 0 && first_pass) ? make_float2(-INFINITY, 0.f) : head_ml[wib][hh];
+                if (first_pass) {
+                    float cm = s[0];
+#pragma unroll
+                    for (int it = 1; it < PASSES; ++it) cm = fmaxf(cm, s[it]);
+#pragma unroll
+                    for (int o = LPR; o < 32; o <<= 1) cm = fmaxf(cm, __shfl_xor_sync(kFull, cm, o));
+                    const float mn = fmaxf(ml.x, cm);  // finite: row t0 of the chunk is valid
+                    float cs = 0.f;
+#pragma unroll
+                    for (int it = 0; it < PASSES; ++it) cs += ptx::ex2(s[it] - mn);
+#pragma unroll
+                    for (int o = LPR; o < 32; o <<= 1) cs += __shfl_xor_sync(kFull, cs, o);
+                    // the reduction ran across row subgroups only: each row counted once
+                    ml = make_float2(mn, ml.y * ptx::ex2(ml.x - mn) + cs);
+                }
+                if (last_pass) {
+                    const float wsc = 1.f / (ml.y * static_cast<float>(a.r));
+#pragma unroll
+                    for (int it = 0; it < PASSES; ++it) wgt[it] = fmaf(ptx::ex2(s[it] - ml.x), wsc, wgt[it]);
+                }
+                __syncwarp();
+                if (lane == 0) head_ml[wib][hh] = ml;
+                __syncwarp();
+            }
+            if (last_pass) {
+#pragma unroll
+                for (int it = 0; it < PASSES; ++it) {
+                    float fk[E], fv[E];
+                    VT::unpack(kr[it], fk);
+                    VT::unpack(vr[it], fv);
+#pragma unroll
+                    for (int e = 0; e < E; ++e) {
+                        ak[e] = fmaf(wgt[it], fk[e], ak[e]);
+                        av[e] = fmaf(wgt[it], fv[e], av[e]);
+                    }
+                }
+            }
+        } else if (a.pool_max) {
             // element-wise maximum of the group's keys and of its values
 #pragma unroll
             for (int it = 0; it < PASSES; ++it) {
@@ -266,7 +346,7 @@ __global__ void __launch_bounds__(NW_MAX * 32) pool_kernel(const T *__restrict__
         __syncwarp();
         if (lane == 0 && c + a.S < n_chunks) issue();
 
-        if (ch == nch - 1) {
+        if (ch == ncg - 1) {
             // group done: combine the RPI row-subgroups, normalise, store
             float lt = l, kt[E], vt[E];
 #pragma unroll
@@ -284,6 +364,16 @@ __global__ void __launch_bounds__(NW_MAX * 32) pool_kernel(const T *__restrict__
                     }
                 }
                 lt = 1.f;
+            } else if (a.headmean) {
+#pragma unroll
+                for (int o = LPR; o < 32; o <<= 1) {
+#pragma unroll
+                    for (int e = 0; e < E; ++e) {
+                        kt[e] += __shfl_xor_sync(kFull, kt[e], o);
+                        vt[e] += __shfl_xor_sync(kFull, vt[e], o);
+                    }
+                }
+                lt = 1.f;  // the weights are normalised already
             } else {
 #pragma unroll
                 for (int o = LPR; o < 32; o <<= 1) {
@@ -314,7 +404,7 @@ __global__ void __launch_bounds__(NW_MAX * 32) pool_kernel(const T *__restrict__
             st = 0;
             ph ^= 1u;
         }
-        if (++ch == nch) {
+        if (++ch == ncg) {
             ch = 0;
             gid += tw;
         }
@@ -379,7 +469,11 @@ cudaError_t launch_typed(const void *Q, const void *K, const void *V, void *Kc, 
         if (nw > NW_MAX) nw = NW_MAX;
         if (nw < 1) return cudaErrorNotSupported;  // a stage would not fit (hundreds of query heads per KV head)
     }
-    a.logit_scale = s.pool_mode == 1 ? 0.f : s.scale * 1.4426950408889634f / static_cast<float>(a.r);
+    a.headmean = s.pool_mode == 3 ? 1 : 0;
+    if (a.headmean && a.r > HM_MAX) return cudaErrorNotSupported;
+    a.npass = (a.headmean && static_cast<uint32_t>(s.g) > chunk_rows) ? 2 : 1;
+    a.logit_scale = s.pool_mode == 1 ? 0.f
+                    : s.scale * 1.4426950408889634f / static_cast<float>(a.headmean ? 1 : a.r);
     a.pool_max = s.pool_mode == 2 ? 1 : 0;
     a.n_groups = static_cast<int64_t>(s.B) * s.Hkv * (s.N / s.g);
     a.status = status;

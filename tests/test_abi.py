@@ -123,10 +123,17 @@ def test_pool_group_rejects_bad_group(lib):
 
 
 def test_rejects_unknown_modes(lib):
-    for kw in (dict(window_mode=2), dict(window_mode=-1), dict(pool_mode=3), dict(pool_mode=-1)):
+    for kw in (dict(window_mode=2), dict(window_mode=-1), dict(pool_mode=4), dict(pool_mode=-1)):
         prm = api.make_params(1, 2, 2, 256, 128, 16, 32, api.CCA_BF16, **kw)
         assert lib.cca_attn_fwd(*P, ctypes.byref(prm), None) == api.CCA_ERR_INVALID_ARG
         assert lib.cca_pool(*P[:5], ctypes.byref(prm), None) == api.CCA_ERR_INVALID_ARG
+
+
+def test_post_softmax_gqa_pooling_head_limit(lib):
+    # pool_mode 3 keeps one running softmax state per query head of a KV head: at most 8
+    prm = api.make_params(1, 16, 1, 256, 128, 16, 32, api.CCA_BF16, pool_mode=3)
+    assert lib.cca_pool(*P[:5], ctypes.byref(prm), None) == api.CCA_ERR_UNSUPPORTED
+    assert lib.cca_pool_group(*P[:5], 0, ctypes.byref(prm), None) == api.CCA_ERR_UNSUPPORTED
 
 
 def test_backward_rejects_bad_arguments(lib):
