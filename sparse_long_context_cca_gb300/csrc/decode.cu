@@ -10,6 +10,7 @@
 // CTAs (flash-decoding); each CTA keeps an online-softmax state per query head
 // over its slice, and a second kernel merges the slices' (max, sum, output)
 // partials, which live in a caller-provided workspace.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -291,12 +292,16 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const float *__restri
 
 // One warp per (b, kv): pools group j with the supplied group-last queries q[B, Hq, D].
 // pool_max: element-wise maximum of the group's rows instead of the weighted sums
-// (mean pooling arrives as logit_scale = 0, i.e. equal weights).
+// (mean pooling arrives as logit_scale = 0, i.e. equal weights).  headmean (pool_mode
+// 3): every query head takes its own softmax over the group and the weights are the
+// mean of the r weight vectors; logit_scale is then per head (no 1/r).
+constexpr int POOL_GROUP_HM_MAX = 8;
+
 template <typename T, int D>
 __global__ void __launch_bounds__(128) pool_group_kernel(const T *__restrict__ q, const T *__restrict__ K,
                                                          const T *__restrict__ V, T *__restrict__ Kc,
                                                          T *__restrict__ Vc, int Hq, int Hkv, int Ncap, int g, int j,
-                                                         float logit_scale, int pool_max, int n_bk) {
+                                                         float logit_scale, int pool_max, int headmean, int n_bk) {
     using VT = Vec<T>;
     constexpr int E = VT::E;
     constexpr int LPR = D / E;
@@ -317,6 +322,83 @@ __global__ void __launch_bounds__(128) pool_group_kernel(const T *__restrict__ q
     }
     const T *kg = K + (static_cast<int64_t>(bk) * Ncap + static_cast<int64_t>(j) * g) * D + cl * E;
     const T *vg = V + (static_cast<int64_t>(bk) * Ncap + static_cast<int64_t>(j) * g) * D + cl * E;
+    if (headmean) {
+        // Pass 1, head by head: that head's softmax normaliser over the group (max m_h,
+        // sum l_h, log2 domain).  Pass 2: weight of row t = (1/r) sum_h 2^(s_h,t - m_h) / l_h.
+        __shared__ float2 hml[4][POOL_GROUP_HM_MAX];
+        const int wib = threadIdx.x >> 5;
+        auto logit = [&](int hh, const float (&kf)[E]) {
+            float qf[E];
+            VT::unpack(ldg16(q + (static_cast<int64_t>(b) * Hq + kv * r + hh) * D + cl * E), qf);
+            float dot = 0.f;
+#pragma unroll
+            for (int e = 0; e < E; ++e) dot = fmaf(qf[e], kf[e], dot);
+#pragma unroll
+            for (int off = LPR / 2; off > 0; off >>= 1) dot += __shfl_xor_sync(kFull, dot, off);
+            return dot * logit_scale;
+        };
+        for (int hh = 0; hh < r; ++hh) {
+            float m = -INFINITY, l = 0.f;
+            for (int t0 = 0; t0 < g; t0 += RPI) {
+                const int t = t0 + sub;
+                float kf[E];
+                VT::unpack(t < g ? ldg16(kg + static_cast<int64_t>(t) * D) : make_uint4(0, 0, 0, 0), kf);
+                const float xl = logit(hh, kf);
+                if (t < g) {
+                    const float mn = fmaxf(m, xl);
+                    l = l * ptx::ex2(m - mn) + ptx::ex2(xl - mn);
+                    m = mn;
+                }
+            }
+#pragma unroll
+            for (int off = LPR; off < 32; off <<= 1) {
+                const float mo = __shfl_xor_sync(kFull, m, off);
+                const float lo_ = __shfl_xor_sync(kFull, l, off);
+                const float mn = fmaxf(m, mo);
+                const float ca = (m == -INFINITY) ? 0.f : ptx::ex2(m - mn);
+                const float cb = (mo == -INFINITY) ? 0.f : ptx::ex2(mo - mn);
+                l = l * ca + lo_ * cb;
+                m = mn;
+            }
+            if (lane == 0) hml[wib][hh] = make_float2(m, 1.f / (l * static_cast<float>(r)));
+        }
+        __syncwarp();
+        float ak[E], av[E];
+#pragma unroll
+        for (int e = 0; e < E; ++e) ak[e] = av[e] = 0.f;
+        for (int t0 = 0; t0 < g; t0 += RPI) {
+            const int t = t0 + sub;
+            float kf[E], vf[E];
+            VT::unpack(t < g ? ldg16(kg + static_cast<int64_t>(t) * D) : make_uint4(0, 0, 0, 0), kf);
+            VT::unpack(t < g ? ldg16(vg + static_cast<int64_t>(t) * D) : make_uint4(0, 0, 0, 0), vf);
+            float wgt = 0.f;
+            for (int hh = 0; hh < r; ++hh) {
+                const float2 st = hml[wib][hh];
+                wgt = fmaf(ptx::ex2(logit(hh, kf) - st.x), st.y, wgt);
+            }
+            if (t < g) {
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    ak[e] = fmaf(wgt, kf[e], ak[e]);
+                    av[e] = fmaf(wgt, vf[e], av[e]);
+                }
+            }
+        }
+#pragma unroll
+        for (int off = LPR; off < 32; off <<= 1) {
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                ak[e] += __shfl_xor_sync(kFull, ak[e], off);
+                av[e] += __shfl_xor_sync(kFull, av[e], off);
+            }
+        }
+        if (sub == 0) {
+            const int64_t orow = (static_cast<int64_t>(bk) * (Ncap / g) + j) * D + cl * E;
+            *reinterpret_cast<uint4 *>(Kc + orow) = VT::pack(ak);
+            *reinterpret_cast<uint4 *>(Vc + orow) = VT::pack(av);
+        }
+        return;
+    }
     const float init = pool_max ? -INFINITY : 0.f;
     float m = -INFINITY, l = 0.f, ak[E], av[E];
 #pragma unroll
@@ -455,19 +537,45 @@ cudaError_t dispatch_r(const void *Q, const void *K, const void *V, const void *
 // address is looked up once per device with cudaGetSymbolAddress.
 static __device__ __align__(256) unsigned char g_decode_scratch[DECODE_NOALLOC_MAX_BYTES];
 
+// The address belongs to the module loaded into one context: after cudaDeviceReset (or
+// any other end of the device's primary context) the next context loads the module
+// again, possibly elsewhere.  So the cached address is kept with the context that was
+// current when it was looked up, and looked up again when another context is current.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+
+static CtxGetCurrentFn ctx_get_current() {
+    static CtxGetCurrentFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrentFn>(ptr);
+    });
+    return fn;
+}
+
 cudaError_t decode_noalloc_scratch(float **out) {
     static std::mutex mu;
     static void *ptrs[64] = {};
+    static CUcontext ctxs[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    CtxGetCurrentFn get_ctx = ctx_get_current();
+    if (get_ctx == nullptr) return cudaErrorNotSupported;
+    CUcontext ctx = nullptr;  // stays null while no context is current yet
+    if (get_ctx(&ctx) != CUDA_SUCCESS) return cudaErrorNotSupported;
     std::lock_guard<std::mutex> lock(mu);
-    if (ptrs[dev] == nullptr) {
+    if (ptrs[dev] == nullptr || ctx == nullptr || ctxs[dev] != ctx) {
         void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_decode_scratch);  // with `dev` current
+        e = cudaGetSymbolAddress(&p, g_decode_scratch);  // with `dev` current; binds its context
         if (e != cudaSuccess) return e;
+        if (get_ctx(&ctx) != CUDA_SUCCESS || ctx == nullptr) return cudaErrorNotSupported;
         ptrs[dev] = p;
+        ctxs[dev] = ctx;
     }
     *out = static_cast<float *>(ptrs[dev]);
     return cudaSuccess;
@@ -493,30 +601,33 @@ cudaError_t launch_pool_group(int dtype, const void *q, const void *K, const voi
                               const Shape &s, int j, cudaStream_t stream) {
     const int n_bk = s.B * s.Hkv;
     const unsigned blocks = static_cast<unsigned>((n_bk + 3) / 4);
-    const float ls = s.pool_mode == 1 ? 0.f : s.scale * 1.4426950408889634f / static_cast<float>(s.Hq / s.Hkv);
+    const int hmean = s.pool_mode == 3 ? 1 : 0;
+    if (hmean && s.Hq / s.Hkv > POOL_GROUP_HM_MAX) return cudaErrorNotSupported;
+    const float ls = s.pool_mode == 1 ? 0.f
+                     : s.scale * 1.4426950408889634f / static_cast<float>(hmean ? 1 : s.Hq / s.Hkv);
     const int pmax = s.pool_mode == 2 ? 1 : 0;
     if (dtype == 0) {
         if (s.d == 128)
             pool_group_kernel<__nv_bfloat16, 128><<<blocks, 128, 0, stream>>>(
                 static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(K),
                 static_cast<const __nv_bfloat16 *>(V), static_cast<__nv_bfloat16 *>(Kc),
-                static_cast<__nv_bfloat16 *>(Vc), s.Hq, s.Hkv, s.N, s.g, j, ls, pmax, n_bk);
+                static_cast<__nv_bfloat16 *>(Vc), s.Hq, s.Hkv, s.N, s.g, j, ls, pmax, hmean, n_bk);
         else if (s.d == 64)
             pool_group_kernel<__nv_bfloat16, 64><<<blocks, 128, 0, stream>>>(
                 static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(K),
                 static_cast<const __nv_bfloat16 *>(V), static_cast<__nv_bfloat16 *>(Kc),
-                static_cast<__nv_bfloat16 *>(Vc), s.Hq, s.Hkv, s.N, s.g, j, ls, pmax, n_bk);
+                static_cast<__nv_bfloat16 *>(Vc), s.Hq, s.Hkv, s.N, s.g, j, ls, pmax, hmean, n_bk);
         else
             return cudaErrorNotSupported;
     } else {
         if (s.d == 128)
             pool_group_kernel<float, 128><<<blocks, 128, 0, stream>>>(
                 static_cast<const float *>(q), static_cast<const float *>(K), static_cast<const float *>(V),
-                static_cast<float *>(Kc), static_cast<float *>(Vc), s.Hq, s.Hkv, s.N, s.g, j, ls, pmax, n_bk);
+                static_cast<float *>(Kc), static_cast<float *>(Vc), s.Hq, s.Hkv, s.N, s.g, j, ls, pmax, hmean, n_bk);
         else if (s.d == 64)
             pool_group_kernel<float, 64><<<blocks, 128, 0, stream>>>(
                 static_cast<const float *>(q), static_cast<const float *>(K), static_cast<const float *>(V),
-                static_cast<float *>(Kc), static_cast<float *>(Vc), s.Hq, s.Hkv, s.N, s.g, j, ls, pmax, n_bk);
+                static_cast<float *>(Kc), static_cast<float *>(Vc), s.Hq, s.Hkv, s.N, s.g, j, ls, pmax, hmean, n_bk);
         else
             return cudaErrorNotSupported;
     }

@@ -12,6 +12,7 @@ import ctypes
 import pytest
 import torch
 
+import oracle
 from parity import check_out
 from sparse_long_context_cca_gb300 import api
 from sparse_long_context_cca_gb300.inputs import make_qkv
@@ -41,9 +42,11 @@ CASES = [
 
 
 def test_noalloc_decode_matches_workspace_entry_point():
+    """Both entry points launch the same kernels with the same split count, so their
+    results must agree bit for bit; the first case is also checked against the oracle."""
     lib = api.load_library()
     # Two calls in a row per case, and the cases back to back, all through the same scratch.
-    for wl, positions in CASES:
+    for n, (wl, positions) in enumerate(CASES):
         Q, K, V = make_qkv(wl, "cuda")
         Kc, Vc = api.cca_pool(Q, K, V, wl.g)
         for pos in positions:
@@ -51,8 +54,33 @@ def test_noalloc_decode_matches_workspace_entry_point():
             O_ref, L_ref = api.cca_decode_fwd(q, K, V, Kc, Vc, pos, wl.g, wl.w)
             O, L = _noalloc(lib, q, K, V, Kc, Vc, pos, wl.g, wl.w)
             torch.cuda.synchronize()
-            check_out(O.reshape(-1, wl.d), L.reshape(-1), O_ref.reshape(-1, wl.d).double().cpu().numpy(),
-                      L_ref.reshape(-1).double().cpu().numpy(), q.dtype, f"{wl.name} pos {pos}")
+            assert torch.equal(O, O_ref) and torch.equal(L, L_ref), f"{wl.name} pos {pos}"
+            if n == 0:
+                rows = [(b, h, pos) for b in range(wl.B) for h in range(wl.Hq)]
+                Oe, Le = oracle.attn_rows(Q, K, V, Kc, Vc, wl.g, wl.w, rows)
+                check_out(O.reshape(-1, wl.d), L.reshape(-1), Oe, Le, q.dtype, f"{wl.name} pos {pos} vs oracle")
+
+
+def test_noalloc_decode_at_the_scratch_limit():
+    """B * Hq = 126 query rows at d = 128 with 64 splits per row fill the 4 MiB array up
+    to its last partial (126 * 64 * 130 * 4 bytes); two calls in a row must match the
+    workspace entry point bit for bit."""
+    lib = api.load_library()
+    wl = Workload("noalloc bf16 B1 Hq126 Hkv63 N16384 g16 w16384", 1, 126, 63, 16384, 128, 16, 16384, "bf16", 23,
+                  0.01)
+    prm = api.make_params(wl.B, wl.Hq, wl.Hkv, wl.N, wl.d, wl.g, wl.w, api.CCA_BF16)
+    need = lib.cca_decode_workspace_size(ctypes.byref(prm))
+    assert need == 126 * 64 * 130 * 4 and need <= (4 << 20) < need + 64 * 130 * 4
+    Q, K, V = make_qkv(wl, "cuda")
+    Kc, Vc = api.cca_pool(Q, K, V, wl.g)
+    for pos in (wl.N - 1, wl.N - 2):  # 16384 and 16383 visible keys: 64 splits of at least 256
+        q = Q[:, :, pos].contiguous()
+        O_ref, L_ref = api.cca_decode_fwd(q, K, V, Kc, Vc, pos, wl.g, wl.w)
+        O, L = _noalloc(lib, q, K, V, Kc, Vc, pos, wl.g, wl.w)
+        torch.cuda.synchronize()
+        assert torch.equal(O, O_ref) and torch.equal(L, L_ref), f"pos {pos}"
+    del Q, K, V, Kc, Vc
+    torch.cuda.empty_cache()
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
@@ -65,3 +93,10 @@ def test_noalloc_rejects_shapes_beyond_its_scratch():
     st = lib.cca_decode_fwd_noalloc(p, p, p, p, p, p, p, 5, ctypes.byref(prm), None)
     assert st == api.CCA_ERR_SCRATCH_LIMIT
     assert "scratch" in api.status_string(st)
+    # one query row past the limit at d = 128 (127 rows), and at d = 64 (249 rows)
+    for B, Hq, d in ((1, 127, 128), (1, 249, 64)):
+        prm = api.make_params(B, Hq, Hq, 1024, d, 16, 256, api.CCA_BF16)
+        assert lib.cca_decode_fwd_noalloc(p, p, p, p, p, p, p, 5, ctypes.byref(prm), None) == api.CCA_ERR_SCRATCH_LIMIT
+    for B, Hq, d in ((1, 126, 128), (2, 124, 64)):  # the largest shapes that fit are accepted
+        prm = api.make_params(B, Hq, Hq, 1024, d, 16, 256, api.CCA_BF16)
+        assert lib.cca_decode_workspace_size(ctypes.byref(prm)) <= (4 << 20)
