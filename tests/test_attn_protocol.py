@@ -12,12 +12,25 @@ seeded random order until all finish; a state in which none can move is a deadlo
 It pins the property the GPU tests can only sample: no shape deadlocks, including the
 group-aligned window with groups of more than 128 tokens, where half B's band starts
 several tiles after its last core tile."""
+import os
 import random
+import re
 
 import pytest
 
 BM = BN = 128
 NS = 5
+
+KERNEL = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "sparse_long_context_cca_gb300",
+                      "csrc", "attn_tc.cu")
+
+
+def test_model_constants_match_the_kernel():
+    """The model's tile sizes and ring depth are the kernel's: a change there must be
+    carried into the model before it can say anything about the new pipeline."""
+    src = open(KERNEL).read()
+    found = {name: int(v) for name, v in re.findall(r"constexpr int (BM|BN|NS) = (\d+);", src)}
+    assert found == {"BM": BM, "BN": BN, "NS": NS}, found
 
 
 def lo_of(i, w):
