@@ -610,11 +610,28 @@ def main():
     ap.add_argument("--no-comparator", dest="comparator", action="store_false")
     ap.add_argument("--no-decode", dest="decode", action="store_false")
     ap.add_argument("--no-backward", dest="backward", action="store_false")
+    ap.add_argument("--heads", type=int, default=0, help="query heads of the workload (a head slice)")
+    ap.add_argument("--batch", type=int, default=0, help="batch of the workload")
+    ap.add_argument("--g", type=int, default=0, help="group size of the workload")
+    ap.add_argument("--w", type=int, default=0, help="window of the workload")
     ap.add_argument("--no-sweep", dest="sweep", action="store_false",
                     help="skip the GQA 64K workload and the 12 g x w sweep points")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.heads or args.g or args.w or args.batch:
+        # a slice or variant of the named workload (e.g. a head slice for a profiler run)
+        base = WORKLOADS[args.workload]
+        r = base.Hq // base.Hkv
+        hq = args.heads or base.Hq
+        if hq % r:
+            ap.error(f"--heads must be a multiple of {r}")
+        wl = base.small(B=args.batch or base.B, Hq=hq, Hkv=hq // r, g=args.g or base.g, w=args.w or base.w)
+        wl = wl.small(name=f"{base.name.split(' ')[0]} B{wl.B} Hq{wl.Hq} Hkv{wl.Hkv} d{wl.d} N{wl.N} g{wl.g} w{wl.w}")
+        if wl.N % wl.g:
+            ap.error("N must be a multiple of g")
+        args.workload = "custom"
+        WORKLOADS["custom"] = wl
     rank, world, local = dist_env()
     if args.impl == "reference":
         out = run_reference(args, rank, world)
