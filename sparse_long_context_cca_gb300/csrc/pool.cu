@@ -422,6 +422,238 @@ __global__ void __launch_bounds__(NW_MAX * 32) pool_kernel(const T *__restrict__
     }
 }
 
+// Small groups: g = PPG * RPI tokens (PPG row passes per group) with several whole
+// groups per chunk: GPC = PASSES / PPG consecutive groups of one (batch, KV head), so
+// that no pass of a chunk runs on rows that are not there and no state crosses chunks.
+// Every chunk brings its groups' query rows (r per group).  The copies of a chunk are
+// issued by several lanes at once.  pool_mode 0, 1 and 2 (pool_mode 3 takes pool_kernel).
+// a.n_groups counts chunks here: B * Hkv * ceil(G / GPC).
+template <typename T, int D, int PPG>
+__global__ void __launch_bounds__(NW_MAX * 32) pool_small_kernel(const T *__restrict__ Q, const T *__restrict__ K,
+                                                             const T *__restrict__ V, T *__restrict__ Kc,
+                                                             T *__restrict__ Vc, const PoolArgs a) {
+    using VT = VecTraits<T>;
+    constexpr int E = VT::E;
+    constexpr int LPR = D / E;
+    constexpr int RPI = 32 / LPR;
+    constexpr uint32_t ROW_BYTES = D * sizeof(T);
+    constexpr int RS = CHUNK_BYTES / ROW_BYTES;
+    constexpr int PASSES = RS / RPI;
+    constexpr int GS = PPG * RPI;      // tokens per group
+    constexpr int GPC = PASSES / PPG;  // groups per chunk
+    static_assert(PASSES % PPG == 0 && E % 2 == 0, "unsupported small-group shape");
+
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    __shared__ uint64_t bars[NW_MAX][S_MAX];
+    __shared__ int abort_flag;
+    const int lane = threadIdx.x & 31;
+    const int wib = threadIdx.x >> 5;
+    const int sub = lane / LPR;
+    const int cl = lane % LPR;
+    if (threadIdx.x == 0) abort_flag = 0;
+    if (lane == 0)
+        for (int x = 0; x < a.S; ++x) ptx::mbar_init(ptx::smem_addr(&bars[wib][x]), 1);
+    ptx::fence_mbar_init();
+    __syncthreads();
+
+    const uint32_t ring = ptx::smem_addr(smem_raw) + wib * a.S * a.stage_bytes;
+    const int G = a.N / GS;
+    const int CPR = (G + GPC - 1) / GPC;  // chunks per (batch, KV head)
+    const int nw = blockDim.x >> 5;
+    const int64_t tw = static_cast<int64_t>(gridDim.x) * nw;
+    const int64_t gw = static_cast<int64_t>(blockIdx.x) * nw + wib;
+    const int64_t n_chunks = gw < a.n_groups ? (a.n_groups - 1 - gw) / tw + 1 : 0;
+
+    // The whole warp advances the copy cursor (chunk cr of row bk) and issues a chunk:
+    // lane 0 arms the barrier, then lane x issues copy x (K, V, then the query rows).
+    int is = 0;
+    int64_t icr = gw % CPR, ibk = gw / CPR;
+    auto issue = [&]() {
+        const int j0 = static_cast<int>(icr) * GPC;
+        const int ng = min(GPC, G - j0);
+        const uint32_t kv_bytes = static_cast<uint32_t>(ng * GS) * ROW_BYTES;
+        const uint32_t stage = ring + static_cast<uint32_t>(is) * a.stage_bytes;
+        const uint32_t bar = ptx::smem_addr(&bars[wib][is]);
+        if (lane == 0) ptx::mbar_arrive_expect_tx(bar, 2 * kv_bytes + static_cast<uint32_t>(ng * a.r) * ROW_BYTES);
+        __syncwarp();
+        const int64_t bk = ibk;
+        const int64_t row0 = bk * a.N + static_cast<int64_t>(j0) * GS;
+        const int64_t b = bk / a.Hkv, kv = bk % a.Hkv;
+        const int ncopy = 2 + ng * a.r;
+        for (int x = lane; x < ncopy; x += 32) {
+            if (x == 0) {
+                ptx::bulk_load(stage, K + row0 * D, kv_bytes, bar);
+            } else if (x == 1) {
+                ptx::bulk_load(stage + a.v_off, V + row0 * D, kv_bytes, bar);
+            } else {
+                const int gi = (x - 2) / a.r, hh = (x - 2) % a.r;
+                const int64_t last = static_cast<int64_t>(j0 + gi + 1) * GS - 1;
+                ptx::bulk_load(stage + 2 * a.v_off + static_cast<uint32_t>(x - 2) * ROW_BYTES,
+                               Q + ((b * a.Hq + kv * a.r + hh) * static_cast<int64_t>(a.N) + last) * D, ROW_BYTES,
+                               bar);
+            }
+        }
+        if (++is == a.S) is = 0;
+        icr += tw;
+        if (icr >= CPR) {
+            ibk += icr / CPR;
+            icr %= CPR;
+        }
+    };
+    for (int64_t c = 0; c < n_chunks && c < a.S; ++c) issue();
+
+    int64_t c = 0;
+    int st = 0;
+    uint32_t ph = 0;
+    int64_t ccr = gw % CPR, cbk = gw / CPR;  // consumer's chunk
+    for (; c < n_chunks; ++c) {
+        const uint32_t stage = ring + st * a.stage_bytes;
+        volatile int *af = &abort_flag;
+        if (!__all_sync(kFull, ptx::wait_bounded(ptx::smem_addr(&bars[wib][st]), ph, af, WAIT_LIMIT_NS)))
+            break;
+        const int j0 = static_cast<int>(ccr) * GPC;
+        const int ng = min(GPC, G - j0);
+        const int rows = ng * GS;
+        uint4 kr[PASSES], vr[PASSES];
+#pragma unroll
+        for (int it = 0; it < PASSES; ++it) {
+            const int t = it * RPI + sub;
+            if (t < rows) {
+                kr[it] = lds16(stage + t * ROW_BYTES + cl * 16);
+                vr[it] = lds16(stage + a.v_off + t * ROW_BYTES + cl * 16);
+            } else {
+                kr[it] = vr[it] = make_uint4(0, 0, 0, 0);
+            }
+        }
+#pragma unroll
+        for (int gi = 0; gi < GPC; ++gi) {
+            if (gi >= ng) break;  // the same for the whole warp
+            float ak[E], av[E];
+            if (a.pool_max) {
+#pragma unroll
+                for (int e = 0; e < E; ++e) ak[e] = av[e] = -INFINITY;
+#pragma unroll
+                for (int pp = 0; pp < PPG; ++pp) {
+                    float fk[E], fv[E];
+                    VT::unpack(kr[gi * PPG + pp], fk);
+                    VT::unpack(vr[gi * PPG + pp], fv);
+#pragma unroll
+                    for (int e = 0; e < E; ++e) {
+                        ak[e] = fmaxf(ak[e], fk[e]);
+                        av[e] = fmaxf(av[e], fv[e]);
+                    }
+                }
+#pragma unroll
+                for (int o = LPR; o < 32; o <<= 1) {
+#pragma unroll
+                    for (int e = 0; e < E; ++e) {
+                        ak[e] = fmaxf(ak[e], __shfl_xor_sync(kFull, ak[e], o));
+                        av[e] = fmaxf(av[e], __shfl_xor_sync(kFull, av[e], o));
+                    }
+                }
+            } else {
+                // the sum of the group's r last-token queries (1/r is in logit_scale)
+                float q[E];
+#pragma unroll
+                for (int e = 0; e < E; ++e) q[e] = 0.f;
+                for (int hh = 0; hh < a.r; ++hh) {
+                    float f[E];
+                    VT::unpack(lds16(stage + 2 * a.v_off + static_cast<uint32_t>(gi * a.r + hh) * ROW_BYTES + cl * 16), f);
+#pragma unroll
+                    for (int e = 0; e < E; ++e) q[e] += f[e];
+                }
+                float sl[PPG];
+#pragma unroll
+                for (int pp = 0; pp < PPG; ++pp) {
+                    float f[E];
+                    VT::unpack(kr[gi * PPG + pp], f);
+                    float x = 0.f;
+#pragma unroll
+                    for (int e = 0; e < E; ++e) x = fmaf(q[e], f[e], x);
+#pragma unroll
+                    for (int o = LPR / 2; o > 0; o >>= 1) x += __shfl_xor_sync(kFull, x, o);
+                    sl[pp] = x * a.logit_scale;  // log2 domain; every row of a group is present
+                }
+                float m = sl[0];
+#pragma unroll
+                for (int pp = 1; pp < PPG; ++pp) m = fmaxf(m, sl[pp]);
+#pragma unroll
+                for (int o = LPR; o < 32; o <<= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+                float l = 0.f;
+                uint64_t ak2[E / 2], av2[E / 2];
+#pragma unroll
+                for (int e = 0; e < E / 2; ++e) ak2[e] = av2[e] = 0ull;
+#pragma unroll
+                for (int pp = 0; pp < PPG; ++pp) {
+                    const float w = ptx::ex2(sl[pp] - m);
+                    l += w;
+                    const uint64_t w2 = ptx::f2(w, w);
+                    float fk[E], fv[E];
+                    VT::unpack(kr[gi * PPG + pp], fk);
+                    VT::unpack(vr[gi * PPG + pp], fv);
+#pragma unroll
+                    for (int e = 0; e < E / 2; ++e) {
+                        ak2[e] = ptx::fma2(w2, ptx::f2(fk[2 * e], fk[2 * e + 1]), ak2[e]);
+                        av2[e] = ptx::fma2(w2, ptx::f2(fv[2 * e], fv[2 * e + 1]), av2[e]);
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < E / 2; ++e) {
+                    ptx::f2_split(ak2[e], ak[2 * e], ak[2 * e + 1]);
+                    ptx::f2_split(av2[e], av[2 * e], av[2 * e + 1]);
+                }
+#pragma unroll
+                for (int o = LPR; o < 32; o <<= 1) {
+                    l += __shfl_xor_sync(kFull, l, o);
+#pragma unroll
+                    for (int e = 0; e < E; ++e) {
+                        ak[e] += __shfl_xor_sync(kFull, ak[e], o);
+                        av[e] += __shfl_xor_sync(kFull, av[e], o);
+                    }
+                }
+                const float inv = 1.f / l;
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    ak[e] *= inv;
+                    av[e] *= inv;
+                }
+            }
+            const int64_t orow = (cbk * G + j0 + gi) * static_cast<int64_t>(D) + cl * E;
+            if (RPI >= 2) {
+                if (sub == 0) *reinterpret_cast<uint4 *>(Kc + orow) = VT::pack(ak);
+                if (sub == 1) *reinterpret_cast<uint4 *>(Vc + orow) = VT::pack(av);
+            } else {
+                *reinterpret_cast<uint4 *>(Kc + orow) = VT::pack(ak);
+                *reinterpret_cast<uint4 *>(Vc + orow) = VT::pack(av);
+            }
+        }
+        // every lane has read the stage: refill it with chunk c + S
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (c + a.S < n_chunks) issue();
+        if (++st == a.S) {
+            st = 0;
+            ph ^= 1u;
+        }
+        ccr += tw;
+        if (ccr >= CPR) {
+            cbk += ccr / CPR;
+            ccr %= CPR;
+        }
+    }
+    if (c < n_chunks) {
+        // gave up: let this warp's copies in flight land before the CTA exits
+        volatile int never = 0;
+        if (lane == 0) {
+            const int64_t end = (c + a.S < n_chunks) ? c + a.S : n_chunks;
+            for (int64_t x = c; x < end; ++x)
+                ptx::wait_bounded(ptx::smem_addr(&bars[wib][x % a.S]), (x / a.S) & 1, &never, WAIT_LIMIT_NS);
+            if (a.status != nullptr) atomicCAS(a.status, 0, static_cast<int32_t>(-4));
+        }
+        __syncwarp();
+    }
+}
+
 struct DevInfo {
     bool ready = false;
     int sms = 0;
@@ -441,10 +673,72 @@ int sm_count() {
     return d.sms;
 }
 
+// Ring geometry shared by both kernels: NW_MAX warps (more warps hide the per-chunk
+// arithmetic) and as many stages as the budget allows, at least two per warp, trading
+// warps for stages when a stage is large.  Returns the warp count, 0 if a stage does not fit.
+int ring_geometry(PoolArgs &a) {
+    int nw = NW_MAX;
+    a.S = static_cast<int>(SMEM_BUDGET / (nw * a.stage_bytes));
+    if (a.S > S_MAX) a.S = S_MAX;
+    if (a.S < 2) {
+        a.S = 2;
+        nw = static_cast<int>(SMEM_BUDGET / (a.S * a.stage_bytes));
+        if (nw > NW_MAX) nw = NW_MAX;
+    }
+    return nw;
+}
+
+template <typename T, int D, int PPG>
+cudaError_t launch_small(const void *Q, const void *K, const void *V, void *Kc, void *Vc, const Shape &s,
+                         int32_t *status, cudaStream_t stream) {
+    constexpr uint32_t ROW = D * sizeof(T);
+    constexpr int RPI = 32 / (D / VecTraits<T>::E);
+    constexpr int GPC = (CHUNK_BYTES / ROW / RPI) / PPG;
+    PoolArgs a;
+    a.Hq = s.Hq;
+    a.Hkv = s.Hkv;
+    a.N = s.N;
+    a.g = s.g;
+    a.r = s.Hq / s.Hkv;
+    a.v_off = CHUNK_BYTES;
+    a.stage_bytes = 2 * CHUNK_BYTES + static_cast<uint32_t>(GPC * a.r) * ROW;
+    const int nw = ring_geometry(a);
+    if (nw < 1) return cudaErrorNotSupported;
+    a.headmean = 0;
+    a.npass = 1;
+    a.logit_scale = s.pool_mode == 1 ? 0.f : s.scale * 1.4426950408889634f / static_cast<float>(a.r);
+    a.pool_max = s.pool_mode == 2 ? 1 : 0;
+    const int64_t G = s.N / s.g;
+    a.n_groups = static_cast<int64_t>(s.B) * s.Hkv * ((G + GPC - 1) / GPC);  // chunks
+    a.status = status;
+    static std::once_flag once;
+    static cudaError_t attr = cudaSuccess;
+    std::call_once(once, [] {
+        attr = cudaFuncSetAttribute(pool_small_kernel<T, D, PPG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(SMEM_BUDGET));
+    });
+    if (attr != cudaSuccess) return attr;
+    const int sms = sm_count();
+    if (sms <= 0) return cudaErrorInvalidDevice;
+    const int64_t want = (a.n_groups + nw - 1) / nw;
+    const unsigned grid = static_cast<unsigned>(want < sms ? want : sms);
+    pool_small_kernel<T, D, PPG><<<grid, nw * 32, nw * a.S * a.stage_bytes, stream>>>(
+        static_cast<const T *>(Q), static_cast<const T *>(K), static_cast<const T *>(V), static_cast<T *>(Kc),
+        static_cast<T *>(Vc), a);
+    return cudaGetLastError();
+}
+
 template <typename T, int D>
 cudaError_t launch_typed(const void *Q, const void *K, const void *V, void *Kc, void *Vc, const Shape &s,
                          int32_t *status, cudaStream_t stream) {
     constexpr uint32_t ROW = D * sizeof(T);
+    // groups of 1, 2 or 4 row passes take the small-group kernel (not pool_mode 3)
+    constexpr int RPI = 32 / (D / VecTraits<T>::E);
+    if (s.pool_mode != 3) {
+        if (s.g == RPI) return launch_small<T, D, 1>(Q, K, V, Kc, Vc, s, status, stream);
+        if (s.g == 2 * RPI) return launch_small<T, D, 2>(Q, K, V, Kc, Vc, s, status, stream);
+        if (s.g == 4 * RPI) return launch_small<T, D, 4>(Q, K, V, Kc, Vc, s, status, stream);
+    }
     PoolArgs a;
     a.Hq = s.Hq;
     a.Hkv = s.Hkv;
@@ -460,15 +754,8 @@ cudaError_t launch_typed(const void *Q, const void *K, const void *V, void *Kc, 
                                                                                : CHUNK_BYTES / ROW;
     a.v_off = chunk_rows * ROW;
     a.stage_bytes = 2 * a.v_off + static_cast<uint32_t>(a.r) * ROW;
-    int nw = NW_MAX;
-    a.S = static_cast<int>(SMEM_BUDGET / (nw * a.stage_bytes));
-    if (a.S > S_MAX) a.S = S_MAX;
-    if (a.S < 2) {
-        a.S = 2;
-        nw = static_cast<int>(SMEM_BUDGET / (a.S * a.stage_bytes));
-        if (nw > NW_MAX) nw = NW_MAX;
-        if (nw < 1) return cudaErrorNotSupported;  // a stage would not fit (hundreds of query heads per KV head)
-    }
+    const int nw = ring_geometry(a);
+    if (nw < 1) return cudaErrorNotSupported;  // a stage would not fit (hundreds of query heads per KV head)
     a.headmean = s.pool_mode == 3 ? 1 : 0;
     if (a.headmean && a.r > HM_MAX) return cudaErrorNotSupported;
     a.npass = (a.headmean && static_cast<uint32_t>(s.g) > chunk_rows) ? 2 : 1;

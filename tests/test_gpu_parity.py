@@ -163,3 +163,33 @@ def test_output_alignment_16_bytes():
     O2, L2 = api.cca_attn_fwd(Q, K, V, Kc, Vc, w.g, w.w, O=O2)
     torch.cuda.synchronize()
     assert torch.equal(O1, O2) and torch.equal(L1, L2)
+
+
+# Pooling of small groups: g of 1, 2 or 4 row passes takes the kernel that packs several
+# whole groups into one chunk (per dtype and d: bf16 d128 g 2/4/8, bf16 d64 g 4/8/16,
+# f32 d128 g 1/2/4, f32 d64 g 2/4/8).  Group counts are not multiples of the groups per
+# chunk, so the last chunk of every (batch, KV head) is ragged.
+SMALL_GROUP_CASES = [
+    (wl(1, 2, 2, 2 * 101, 128, 2, 40), 0), (wl(2, 4, 2, 4 * 37, 128, 4, 30), 1),
+    (wl(1, 8, 2, 8 * 45, 128, 8, 60), 0), (wl(1, 4, 4, 8 * 29, 128, 8, 60), 2),
+    (wl(1, 4, 1, 4 * 50, 64, 4, 40), 0), (wl(1, 2, 2, 8 * 33, 64, 8, 50), 2),
+    (wl(2, 2, 1, 16 * 21, 64, 16, 64), 1),
+    (wl(1, 2, 2, 77, 128, 1, 20, "f32"), 0), (wl(1, 4, 2, 2 * 61, 128, 2, 20, "f32"), 2),
+    (wl(1, 2, 2, 4 * 19, 128, 4, 20, "f32"), 1),
+    (wl(1, 2, 2, 2 * 45, 64, 2, 20, "f32"), 0), (wl(1, 4, 2, 4 * 27, 64, 4, 20, "f32"), 0),
+    (wl(1, 2, 1, 8 * 23, 64, 8, 20, "f32"), 2),
+]
+
+
+@pytest.mark.parametrize("w,pool_mode", SMALL_GROUP_CASES, ids=lambda x: x.name if hasattr(x, "name") else str(x))
+def test_small_group_pooling(w, pool_mode):
+    Q, K, V = make_qkv(w, "cuda")
+    Kc, Vc = api.cca_pool(Q, K, V, w.g, pool_mode=pool_mode)
+    torch.cuda.synchronize()
+    Kr, Vr = oracle.pool(Q, K, V, w.g, pool_mode=pool_mode)
+    check_cores(Kc, Vc, Kr, Vr, Q.dtype, f"{w.name} pool {pool_mode}")
+    if pool_mode == 0 and (w.d == 128 or w.dtype == "f32"):
+        O, LSE = api.cca_attn_fwd(Q, K, V, Kc, Vc, w.g, w.w)
+        torch.cuda.synchronize()
+        Or, Lr = oracle.attn(Q, K, V, Kr, Vr, w.g, w.w)
+        check_out(O, LSE, Or, Lr, Q.dtype, f"{w.name} prefill")
