@@ -26,7 +26,7 @@ namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int DEC_WARPS = 4;
-constexpr int MIN_KEYS_PER_SPLIT = 256;
+constexpr int MIN_KEYS_PER_SPLIT = 64;
 constexpr int MAX_SPLITS = 64;
 
 template <typename T>
@@ -476,9 +476,43 @@ __global__ void __launch_bounds__(128) pool_group_kernel(const T *__restrict__ q
     }
 }
 
-int decode_splits(int L) {
-    const int sp = (L + MIN_KEYS_PER_SPLIT - 1) / MIN_KEYS_PER_SPLIT;
-    return sp < 1 ? 1 : (sp > MAX_SPLITS ? MAX_SPLITS : sp);
+// Slices per (b, kv): enough CTAs for one even wave of `occ` CTAs on every SM (a grid
+// of 2 or 3 CTAs on different SMs finishes when the SMs with 3 do), but no slice of
+// fewer than MIN_KEYS_PER_SPLIT keys and at most MAX_SPLITS slices.
+int decode_splits(int L, int n_bk, int sms, int occ) {
+    const int target = occ * sms;
+    int sp = (target + n_bk - 1) / n_bk;
+    const int by_keys = L / MIN_KEYS_PER_SPLIT;
+    if (sp > by_keys) sp = by_keys;
+    if (sp > MAX_SPLITS) sp = MAX_SPLITS;
+    return sp < 1 ? 1 : sp;
+}
+
+// SMs of the current device and resident CTAs per SM of one split-kernel instantiation
+// (queried once per device).
+template <typename T, int D, int R>
+cudaError_t split_occupancy(int &sms, int &occ) {
+    struct Info {
+        bool ready = false;
+        int sms = 0, occ = 0;
+        cudaError_t err = cudaSuccess;
+    };
+    static Info info[64];
+    static std::mutex mu;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    Info &x = info[dev & 63];
+    if (!x.ready) {
+        x.err = cudaDeviceGetAttribute(&x.sms, cudaDevAttrMultiProcessorCount, dev);
+        if (x.err == cudaSuccess)
+            x.err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&x.occ, decode_split_kernel<T, D, R>, DEC_WARPS * 32, 0);
+        x.ready = true;
+    }
+    sms = x.sms;
+    occ = x.occ < 1 ? 1 : x.occ;
+    return x.err;
 }
 
 template <typename T, int D, int R>
@@ -493,7 +527,10 @@ cudaError_t launch_decode_typed(const void *Q, const void *K, const void *V, con
     a.n_core = visible_cores(pos, s.w, s.g);
     a.lo = window_start(pos, s.w, s.g, s.window_mode);  // first raw token of the window
     a.L = a.n_core + (pos - a.lo + 1);
-    a.splits = decode_splits(a.L);
+    int sms = 0, occ = 0;
+    cudaError_t oe = split_occupancy<T, D, R>(sms, occ);
+    if (oe != cudaSuccess) return oe;
+    a.splits = decode_splits(a.L, s.B * s.Hkv, sms, occ);
     a.scale_log2 = s.scale * 1.4426950408889634f;
     dim3 grid(a.splits, s.B * s.Hkv);
     decode_split_kernel<T, D, R><<<grid, DEC_WARPS * 32, 0, stream>>>(
