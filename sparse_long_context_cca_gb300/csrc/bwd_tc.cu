@@ -337,9 +337,32 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 }
 
 // ---------------------------------------------------------------- dK, dV
-// 256 threads: rows are keys, and the two warps on a TMEM lane quarter split each query
-// tile's 128 columns, 64 each.
-__global__ void __launch_bounds__(NTHREADS, 1)
+// One 128-key tile (raw tokens or cores) of one (b, kv) per CTA, over the query tiles of
+// the r query heads that see it.  Warp-specialised, 320 threads:
+//   warp 0      producer: K and V once; per query tile, Q and dO (lane 0, TMA) into one
+//               of two stages, and the tile's LSE and D staged by the whole warp;
+//   warp 1      MMA issuer (whole warp, one elected lane):
+//                 S^T = K Q^T, dP^T = V dO^T          (SS, into TMEM)
+//                 dV += P^T dO,  dK += dS^T Q          (TS, once the element-wise step is done)
+//   warps 2..9  element-wise: P^T = 2^(S^T tau log2e - LSE) and dS^T = P^T (dP^T - D), as
+//               bf16 over S^T and dP^T; warps w and w + 4 share TMEM lanes 32*(w%4)..+31
+//               (the keys) and split each query tile's 128 columns, 64 each.
+// The hand-offs are mbarriers, so no step waits for a whole-CTA barrier.  TMEM:
+// S^T | dP^T | dK | dV; the MMAs of one thread complete in issue order, so the next
+// tile's S^T/dP^T, issued after this tile's dV/dK MMAs, never overwrite what they read.
+constexpr int DKV_THREADS = 320;
+constexpr uint32_t DKV_STAGE = 2 * TILE_BYTES;  // Q + dO of one query tile
+constexpr uint32_t DKV_OFF_STAGE = 2 * TILE_BYTES;
+constexpr uint32_t DKV_OFF_LD = DKV_OFF_STAGE + 2 * DKV_STAGE;          // LSE/D staging, 2 x 2 x 128 floats
+constexpr uint32_t DKV_OFF_BAR = DKV_OFF_LD + 2 * 2 * BT * 4;
+constexpr int DB_KV = 0, DB_FULL = 1, DB_EMPTY = 3, DB_SFULL = 5, DB_PFULL = 6, DB_DONE = 7, DB_DRAIN = 8;
+constexpr int DKV_NBARS = 9;
+constexpr uint32_t DKV_OFF_TMEM = DKV_OFF_BAR + DKV_NBARS * 8;
+constexpr uint32_t DKV_OFF_ABORT = DKV_OFF_TMEM + 4;
+constexpr uint32_t DKV_SMEM = DKV_OFF_ABORT + 4 + 1024;  // + slack for the 1024-byte alignment
+static_assert(DKV_SMEM <= 232448, "shared memory budget");
+
+__global__ void __launch_bounds__(DKV_THREADS, 1)
     bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
                       const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                       const __grid_constant__ CUtensorMap tmKc, const __grid_constant__ CUtensorMap tmVc,
@@ -347,12 +370,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                       const __grid_constant__ CUtensorMap tmdKc, const __grid_constant__ CUtensorMap tmdVc,
                       const BwdTcParams p) {
     extern __shared__ uint8_t smem_raw[];
-    const Smem sm = carve(smem_raw);
-    const uint32_t sK = sm.tile[0], sV = sm.tile[1];
-    const uint32_t b_kv = ptx::smem_addr(&sm.bars[0]), b_mma = ptx::smem_addr(&sm.bars[3]);
+    const uint32_t r0 = ptx::smem_addr(smem_raw);
+    const uint32_t base = (r0 + 1023u) & ~1023u;
+    uint8_t *const gb = smem_raw + (base - r0);
+    const uint32_t sK = base, sV = base + TILE_BYTES;
+    auto stage_q = [&](int st) { return base + DKV_OFF_STAGE + static_cast<uint32_t>(st) * DKV_STAGE; };
+    float *const ld_stage = reinterpret_cast<float *>(gb + DKV_OFF_LD);  // [stage][LSE 128 | D 128]
+    auto bar = [&](int k) { return base + DKV_OFF_BAR + 8u * k; };
+    volatile int *const abort_flag = reinterpret_cast<volatile int *>(gb + DKV_OFF_ABORT);
+    const uint64_t lim = p.wait_limit_ns;
+
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-    const int quarter = warp & 3, ch = warp >> 2;
-    const int row = quarter * 32 + lane;
     const int BK = p.B * p.Hkv;
     const int n_core_t = (p.G + BT - 1) / BT;
     // core tiles first (they are seen by the most query rows), then raw-token tiles
@@ -378,146 +406,193 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int qt_lo = r_lo / BT;
     const int nq = r_lo <= r_hi ? r_hi / BT - qt_lo + 1 : 0;
     const int n_it = nq * r;  // (head, query tile) pairs, head-major
-
-    const uint32_t tmem = tmem_setup(sm, 5);
-    const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-    Waiter wait{p.wait_limit_ns, 0};
-    const int m = y0 + row;  // this thread's key (core index or token)
-    const float c1 = p.tau * LOG2E;
-
     auto bh_of = [&](int it) { return b * p.Hq + kv * r + it / nq; };
     auto i0_of = [&](int it) { return (qt_lo + it % nq) * BT; };
-    auto issue_q = [&](int it) {
-        const uint32_t bar = ptx::smem_addr(&sm.bars[1 + (it & 1)]);
-        ptx::mbar_arrive_expect_tx(bar, 2 * TILE_BYTES);
-        load_tile(&tmQ, bar, sm.tile[2 + 2 * (it & 1)], i0_of(it), bh_of(it));
-        load_tile(&tmdO, bar, sm.tile[3 + 2 * (it & 1)], i0_of(it), bh_of(it));
-    };
-    if (t == 0 && !p.skip_loads) {
-        ptx::mbar_arrive_expect_tx(b_kv, 2 * TILE_BYTES);
-        load_tile(core ? (const void *)&tmKc : (const void *)&tmK, b_kv, sK, y0, bk);
-        load_tile(core ? (const void *)&tmVc : (const void *)&tmV, b_kv, sV, y0, bk);
-        if (n_it > 0) issue_q(0);
-    }
-    const uint64_t dKk = ptx::smem_desc_sw128(sK, 16, 1024), dVk = ptx::smem_desc_sw128(sV, 16, 1024);
-    // this key's visible query rows, as a function of the query tile's first row
-    int64_t key_last = 0;
-    if (!core) key_last = p.window_mode ? static_cast<int64_t>(m / p.g + 1) * p.g + p.w - 2 : static_cast<int64_t>(m) + p.w - 1;
 
-    bool ok = wait(b_kv, 0);
-    uint32_t mma_phase = 0;
-    for (int it = 0; ok && it < n_it; ++it) {
-        const int bh = bh_of(it), i0 = i0_of(it);
-        const uint32_t sQ = sm.tile[2 + 2 * (it & 1)], sdO = sm.tile[3 + 2 * (it & 1)];
-        float *s_lse = sm.stage + (it & 1) * 2 * BT, *s_D = s_lse + BT;
-        if (it == 0 && t < BT) {  // stage the first query tile's LSE (log2 units) and D
-            const int iq = i0 + t;
-            s_lse[t] = iq < p.N ? p.LSE[static_cast<int64_t>(bh) * p.N + iq] * LOG2E : 0.f;
-            s_D[t] = iq < p.N ? p.Dbuf[static_cast<int64_t>(bh) * p.N + iq] : 0.f;
+    if (t == 0) {
+        ptx::mbar_init(bar(DB_KV), 1);
+        for (int st = 0; st < 2; ++st) {
+            ptx::mbar_init(bar(DB_FULL + st), 2);  // the copies' arm + the LSE/D staging
+            ptx::mbar_init(bar(DB_EMPTY + st), 1);
         }
-        if (!(ok = wait(ptx::smem_addr(&sm.bars[1 + (it & 1)]), (it >> 1) & 1))) break;
-        if (warp == 0) {
-            // queued behind the previous pair's dV/dK MMAs, which still read P^T and dS^T
+        ptx::mbar_init(bar(DB_SFULL), 1);
+        ptx::mbar_init(bar(DB_PFULL), 8);  // one arrive per element-wise warp
+        ptx::mbar_init(bar(DB_DONE), 1);
+        ptx::mbar_init(bar(DB_DRAIN), 1);
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 0) {
+        ptx::tmem_alloc(base + DKV_OFF_TMEM, 512);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<uint32_t *>(gb + DKV_OFF_TMEM);
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- producer
+        int it = 0;
+        bool ok = true;
+        if (lane == 0 && !p.skip_loads) {
+            ptx::mbar_arrive_expect_tx(bar(DB_KV), 2 * TILE_BYTES);
+            load_tile(core ? (const void *)&tmKc : (const void *)&tmK, bar(DB_KV), sK, y0, bk);
+            load_tile(core ? (const void *)&tmVc : (const void *)&tmV, bar(DB_KV), sV, y0, bk);
+        }
+        for (; it < n_it; ++it) {
+            const int st = it & 1;
+            if (it >= 2 &&
+                !__all_sync(0xffffffffu, ptx::wait_bounded(bar(DB_EMPTY + st), ((it >> 1) & 1) ^ 1, abort_flag, lim))) {
+                ok = false;
+                break;
+            }
+            const int bh = bh_of(it), i0 = i0_of(it);
+            if (lane == 0 && !p.skip_loads) {
+                ptx::mbar_arrive_expect_tx(bar(DB_FULL + st), 2 * TILE_BYTES);
+                load_tile(&tmQ, bar(DB_FULL + st), stage_q(st), i0, bh);
+                load_tile(&tmdO, bar(DB_FULL + st), stage_q(st) + TILE_BYTES, i0, bh);
+            }
+            // this tile's LSE (log2 units) and D, rows past N as zeros
+            float *ls = ld_stage + st * 2 * BT;
+#pragma unroll
+            for (int k = 0; k < BT / 32; ++k) {
+                const int iq = i0 + k * 32 + lane;
+                const int64_t off = static_cast<int64_t>(bh) * p.N + iq;
+                ls[k * 32 + lane] = iq < p.N ? p.LSE[off] * LOG2E : 0.f;
+                ls[BT + k * 32 + lane] = iq < p.N ? p.Dbuf[off] : 0.f;
+            }
+            __syncwarp();
+            if (lane == 0 && !p.skip_loads) ptx::mbar_arrive(bar(DB_FULL + st));
+        }
+        if (!ok && lane == 0 && !p.skip_loads) {
+            // let the copies already issued land before the CTA exits
+            volatile int never = 0;
+            for (int x = it > 2 ? it - 2 : 0; x < it; ++x)
+                ptx::wait_bounded(bar(DB_FULL + (x & 1)), (x >> 1) & 1, &never, lim);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issuer
+        auto wwait = [&](uint32_t bb, uint32_t parity) -> bool {
+            return __all_sync(0xffffffffu, ptx::wait_bounded(bb, parity, abort_flag, lim));
+        };
+        const uint64_t dKk = ptx::smem_desc_sw128(sK, 16, 1024), dVk = ptx::smem_desc_sw128(sV, 16, 1024);
+        bool ok = n_it == 0 || wwait(bar(DB_KV), 0);
+        for (int it = 0; ok && it < n_it; ++it) {
+            const int st = it & 1;
+            const uint32_t sQ = stage_q(st), sdO = sQ + TILE_BYTES;
+            if (!(ok = wwait(bar(DB_FULL + st), (it >> 1) & 1))) break;
             ptx::tc_fence_after();
             ptx::mma_ss_k128_warp(tmem + 0, dKk, ptx::smem_desc_sw128(sQ, 16, 1024), IDESC_SS, 0u);     // S^T  = K Q^T
             ptx::mma_ss_k128_warp(tmem + 128, dVk, ptx::smem_desc_sw128(sdO, 16, 1024), IDESC_SS, 0u);  // dP^T = V dO^T
-            ptx::tc_commit_warp(b_mma);
-        }
-        if (!(ok = wait(b_mma, mma_phase++ & 1))) break;
-        // in-order completion: the previous pair's MMAs are done, its Q/dO buffer is free
-        if (t == 0 && it + 1 < n_it && !p.skip_loads) issue_q(it + 1);
-        // The next query tile's LSE and D: loaded now, so that they arrive during this step's
-        // element-wise work, and staged into the other buffer before this step's barrier
-        // (every wait is a CTA barrier, and a load staged at the top of the step held them all).
-        const bool pre = t < BT && it + 1 < n_it;
-        float n_lse = 0.f, n_D = 0.f;
-        if (pre) {
-            const int iq = i0_of(it + 1) + t;
-            const int64_t off = static_cast<int64_t>(bh_of(it + 1)) * p.N + iq;
-            if (iq < p.N) {
-                n_lse = p.LSE[off] * LOG2E;
-                n_D = p.Dbuf[off];
-            }
-        }
-        ptx::tc_fence_after();
-        // this key's visible query columns [q_lo, q_hi] of the tile
-        int q_lo, q_hi;
-        if (m >= n_keys) {
-            q_lo = 0;
-            q_hi = -1;
-        } else if (core) {
-            q_lo = max((m + 1) * p.g + p.w - 1 - i0, 0);
-            q_hi = min(p.N - 1 - i0, BT - 1);
-        } else {
-            const int last_i = static_cast<int>(key_last < p.N - 1 ? key_last : p.N - 1);
-            q_lo = max(m - i0, 0);
-            q_hi = min(last_i - i0, BT - 1);
-        }
-        // the half ch handles query columns [64ch, 64ch + 64): P^T to S^T columns
-        // [64ch, 64ch + 32), dS^T to dP^T columns [64ch, 64ch + 32), both already read
-#pragma unroll 1
-        for (int j = 0; j < 2; ++j) {
-            const int c = 2 * ch + j;
-            uint32_t s[32], dp[32];
-            ptx::tmem_ld32(tmem + lane_addr + c * 32, s);
-            ptx::tmem_ld32(tmem + lane_addr + 128 + c * 32, dp);
-            ptx::tmem_wait_ld(s);
-            ptx::reg_touch(dp);
-            uint32_t pp[16], dd[16];
-#pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                float pv[2], dv[2];
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int col = c * 32 + 2 * k + e;
-                    const bool vis = col >= q_lo && col <= q_hi;
-                    const float pr = vis ? ptx::ex2(fmaf(__uint_as_float(s[2 * k + e]), c1, -s_lse[col])) : 0.f;
-                    pv[e] = pr;
-                    dv[e] = pr * (__uint_as_float(dp[2 * k + e]) - s_D[col]);
-                }
-                pp[k] = ptx::pack_bf16x2(pv[0], pv[1]);
-                dd[k] = ptx::pack_bf16x2(dv[0], dv[1]);
-            }
-            ptx::tmem_st16(tmem + lane_addr + ch * 64 + j * 16, pp);        // P^T  over S^T
-            ptx::tmem_st16(tmem + lane_addr + 128 + ch * 64 + j * 16, dd);  // dS^T over dP^T
-        }
-        ptx::tmem_wait_st();
-        ptx::tc_fence_before();
-        if (pre) {
-            float *n_stage = sm.stage + ((it + 1) & 1) * 2 * BT;
-            n_stage[t] = n_lse;
-            n_stage[BT + t] = n_D;
-        }
-        __syncthreads();
-        if (warp == 0) {
+            ptx::tc_commit_warp(bar(DB_SFULL));
+            if (!(ok = wwait(bar(DB_PFULL), it & 1))) break;
             ptx::tc_fence_after();
             const uint32_t acc = it > 0 ? 1u : 0u;
             ptx::mma_ts_k128_split_warp(tmem + 384, tmem + 0, ptx::smem_desc_sw128(sdO, HALF_BYTES, 1024), IDESC_TS,
                                         acc);  // dV += P^T dO
             ptx::mma_ts_k128_split_warp(tmem + 256, tmem + 128, ptx::smem_desc_sw128(sQ, HALF_BYTES, 1024),
-                                        IDESC_TS, acc);  // dK += dS^T Q; completion covered by the next wait
+                                        IDESC_TS, acc);  // dK += dS^T Q
+            ptx::tc_commit_warp(bar(DB_EMPTY + st));  // the stage is free once these have read it
+        }
+        ptx::tc_commit_warp(ok ? bar(DB_DONE) : bar(DB_DRAIN));
+        if (!ok) {
+            // whatever was issued must complete before tensor memory is freed
+            volatile int never = 0;
+            ptx::wait_bounded(bar(DB_DRAIN), 0, &never, lim);
+        }
+    } else {
+        // ---------------------------------------------------------------- element-wise
+        const int ch = (warp - 2) >> 2;
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+        const int m = y0 + row;  // this thread's key (core index or token)
+        const float c1 = p.tau * LOG2E;
+        int64_t key_last = 0;
+        if (!core) key_last = p.window_mode ? static_cast<int64_t>(m / p.g + 1) * p.g + p.w - 2 : static_cast<int64_t>(m) + p.w - 1;
+        bool ok = true;
+        for (int it = 0; it < n_it; ++it) {
+            // S^T, dP^T of this tile are in TMEM; the stage's FULL barrier (already complete, and
+            // it cannot move on before this step's arrive) orders the producer's LSE/D staging
+            if (!__all_sync(0xffffffffu, ptx::wait_bounded(bar(DB_SFULL), it & 1, abort_flag, lim)) ||
+                !__all_sync(0xffffffffu, ptx::wait_bounded(bar(DB_FULL + (it & 1)), (it >> 1) & 1, abort_flag, lim))) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            const int i0 = i0_of(it);
+            const float *s_lse = ld_stage + (it & 1) * 2 * BT, *s_D = s_lse + BT;
+            // this key's visible query columns [q_lo, q_hi] of the tile
+            int q_lo, q_hi;
+            if (m >= n_keys) {
+                q_lo = 0;
+                q_hi = -1;
+            } else if (core) {
+                q_lo = max((m + 1) * p.g + p.w - 1 - i0, 0);
+                q_hi = min(p.N - 1 - i0, BT - 1);
+            } else {
+                const int last_i = static_cast<int>(key_last < p.N - 1 ? key_last : p.N - 1);
+                q_lo = max(m - i0, 0);
+                q_hi = min(last_i - i0, BT - 1);
+            }
+            // the half ch handles query columns [64ch, 64ch + 64): P^T to S^T columns
+            // [64ch, 64ch + 32), dS^T to dP^T columns [64ch, 64ch + 32), both already read
+#pragma unroll 1
+            for (int j = 0; j < 2; ++j) {
+                const int c = 2 * ch + j;
+                uint32_t sv[32], dp[32];
+                ptx::tmem_ld32(tmem + lane_addr + c * 32, sv);
+                ptx::tmem_ld32(tmem + lane_addr + 128 + c * 32, dp);
+                ptx::tmem_wait_ld(sv);
+                ptx::reg_touch(dp);
+                uint32_t pp[16], dd[16];
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    float pv[2], dv[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int col = c * 32 + 2 * k + e;
+                        const bool vis = col >= q_lo && col <= q_hi;
+                        const float pr = vis ? ptx::ex2(fmaf(__uint_as_float(sv[2 * k + e]), c1, -s_lse[col])) : 0.f;
+                        pv[e] = pr;
+                        dv[e] = pr * (__uint_as_float(dp[2 * k + e]) - s_D[col]);
+                    }
+                    pp[k] = ptx::pack_bf16x2(pv[0], pv[1]);
+                    dd[k] = ptx::pack_bf16x2(dv[0], dv[1]);
+                }
+                ptx::tmem_st16(tmem + lane_addr + ch * 64 + j * 16, pp);        // P^T  over S^T
+                ptx::tmem_st16(tmem + lane_addr + 128 + ch * 64 + j * 16, dd);  // dS^T over dP^T
+            }
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar(DB_PFULL));
+        }
+        if (ok && !__all_sync(0xffffffffu, ptx::wait_bounded(bar(DB_DONE), 0, abort_flag, lim))) ok = false;
+        if (ok) {
+            // dK * tau and dV through shared memory (the Q/dO stages, idle now) to tiled
+            // stores; a tile no query row sees stores zeros
+            ptx::tc_fence_after();
+            stage_f32_rows(tmem + lane_addr, 256, ch, row, p.tau, n_it == 0, stage_q(0));
+            stage_f32_rows(tmem + lane_addr, 384, ch, row, 1.f, n_it == 0, stage_q(1));
+            ptx::fence_proxy_async_smem();
         }
     }
-    if (ok && n_it > 0) {
-        if (warp == 0) ptx::tc_commit_warp(b_mma);
-        ok = wait(b_mma, mma_phase++ & 1);
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (*abort_flag) {
+        if (t == 0 && p.status != nullptr) atomicCAS(p.status, 0, STATUS_TIMEOUT);
+    } else if (t == 0) {
+        store_tile_f32(core ? &tmdKc : &tmdK, stage_q(0), y0, bk);
+        store_tile_f32(core ? &tmdVc : &tmdV, stage_q(1), y0, bk);
+        ptx::bulk_wait_all();
     }
-    if (ok) {
-        // dK * tau and dV through shared memory (the Q/dO buffers, idle now) to tiled stores;
-        // a tile no query row sees stores zeros
+    if (warp == 0) {
         ptx::tc_fence_after();
-        const uint32_t stk = sm.tile[2], stv = sm.tile[4];
-        stage_f32_rows(tmem + lane_addr, 256, ch, row, p.tau, n_it == 0, stk);
-        stage_f32_rows(tmem + lane_addr, 384, ch, row, 1.f, n_it == 0, stv);
-        ptx::fence_proxy_async_smem();
-        __syncthreads();
-        if (t == 0) {
-            store_tile_f32(core ? &tmdKc : &tmdK, stk, y0, bk);
-            store_tile_f32(core ? &tmdVc : &tmdV, stv, y0, bk);
-            ptx::bulk_wait_all();
-        }
+        ptx::tmem_dealloc(tmem, 512);
     }
-    tmem_teardown(sm, tmem, ok, p);
 }
 
 struct Attr {
@@ -545,7 +620,7 @@ cudaError_t launch_attn_bwd_tc(const void *Q, const void *K, const void *V, cons
             a.err = cudaFuncSetAttribute(bwd_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
             if (a.err == cudaSuccess)
                 a.err = cudaFuncSetAttribute(bwd_dkv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             SMEM_BYTES);
+                                             DKV_SMEM);
             a.done = true;
         }
         if (a.err != cudaSuccess) return a.err;
@@ -583,7 +658,7 @@ cudaError_t launch_attn_bwd_tc(const void *Q, const void *K, const void *V, cons
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const unsigned n_kt = static_cast<unsigned>((G + BT - 1) / BT + (s.N + BT - 1) / BT);
-    bwd_dkv_tc_kernel<<<n_kt * static_cast<unsigned>(kh), NTHREADS, SMEM_BYTES, stream>>>(
+    bwd_dkv_tc_kernel<<<n_kt * static_cast<unsigned>(kh), DKV_THREADS, DKV_SMEM, stream>>>(
         mQ, mdO, mK, mV, mKc, mVc, mdK, mdV, mdKc, mdVc, p);
     return cudaGetLastError();
 }
