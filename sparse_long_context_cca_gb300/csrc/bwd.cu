@@ -240,7 +240,9 @@ __global__ void __launch_bounds__(128) bwd_dkv_core_kernel(const T *__restrict__
 }
 
 // Pass 4: one warp per group -> the pooling backward, added into dK, dV and dQ.
-template <typename T, int D>
+// HM: the pool_mode 3 instantiation (its per-head loop would otherwise cost every
+// other mode registers, and this kernel wants all the warps it can get).
+template <typename T, int D, bool HM>
 __global__ void __launch_bounds__(128) bwd_pool_kernel(const T *__restrict__ Q, const T *__restrict__ K,
                                                        const T *__restrict__ V, const float *__restrict__ dKc,
                                                        const float *__restrict__ dVc, float *__restrict__ dQ,
@@ -297,7 +299,7 @@ __global__ void __launch_bounds__(128) bwd_pool_kernel(const T *__restrict__ Q, 
         }
         return;
     }
-    if (a.pool_mode == 3) {
+    if (HM) {
         // per-head softmax weights averaged over the r heads: head by head, its
         // normaliser, sum_u p_u da_u, then its share of every row's gradient
         const int last3 = (j + 1) * g - 1;
@@ -430,8 +432,12 @@ cudaError_t run(const void *Q, const void *K, const void *V, const void *Kc, con
         bwd_dkv_core_kernel<T, D><<<blocks(static_cast<int64_t>(s.B) * s.Hkv * G), 128, 0, stream>>>(
             q, kc, vc, LSE, dout, Dbuf, dKc, dVc, a);
     }
-    bwd_pool_kernel<T, D><<<blocks(static_cast<int64_t>(s.B) * s.Hkv * G), 128, 0, stream>>>(q, k, v, dKc, dVc, dQ, dK,
-                                                                                             dV, a);
+    if (s.pool_mode == 3)
+        bwd_pool_kernel<T, D, true><<<blocks(static_cast<int64_t>(s.B) * s.Hkv * G), 128, 0, stream>>>(
+            q, k, v, dKc, dVc, dQ, dK, dV, a);
+    else
+        bwd_pool_kernel<T, D, false><<<blocks(static_cast<int64_t>(s.B) * s.Hkv * G), 128, 0, stream>>>(
+            q, k, v, dKc, dVc, dQ, dK, dV, a);
     return cudaGetLastError();
 }
 

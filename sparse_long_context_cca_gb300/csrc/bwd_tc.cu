@@ -3,10 +3,12 @@
 // Context Language Modeling" (Method section), with P recomputed from the
 // forward's LSE.  Notation as in bwd.cu: dS = P (dO.v - D), D_i = dO_i . O_i.
 //
-// Two kernels, 256 threads each.  Thread 0 issues the TMA copies, warp 0 the
-// tcgen05.mma instructions (one elected lane).  For the element-wise work warps w
-// and w + 4 share TMEM lanes 32*(w%4)..+31 and split the 128 columns, 64 each.
-// The fp32 results leave through shared memory and tiled TMA stores.
+// Two kernels, both warp-specialised with 320 threads: warp 0 issues the TMA copies,
+// warp 1 the tcgen05.mma instructions (one elected lane), warps 2..9 do the
+// element-wise work; they hand off through mbarriers, never a CTA-wide barrier
+// inside the loop.  For the element-wise work warps w and w + 4 share TMEM lanes
+// 32*(w%4)..+31 and split the 128 columns, 64 each.  The fp32 results leave
+// through shared memory and tiled TMA stores.
 //
 //  dq kernel, one 128-row query tile of one (b, h) per CTA, over the same key
 //  tiles as the forward (cores, then the band):
@@ -22,9 +24,10 @@
 //  TMEM: S^T | dP^T | dK | dV.  Q/dO tiles are double-buffered.
 //
 // The pooling backward (bwd.cu) then adds the paths through the core tokens.
-// Every wait is bounded; a time-out anywhere becomes a CTA-wide exit agreed on
-// with __syncthreads_or: the copies and MMAs in flight are waited for (again
-// bounded), TMEM is freed and CCA_ERR_TIMEOUT is written to the status word.
+// Every wait is bounded and a time-out sets the CTA's abort flag, which ends every
+// other wait at once: the issuer then waits (bounded) for the MMAs it has issued,
+// the producer for its copies in flight, TMEM is freed and CCA_ERR_TIMEOUT is
+// written to the status word.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -45,7 +48,6 @@ extern int g_skip_q_load;
 namespace {
 
 constexpr int BT = 128;  // rows per tile (queries or keys)
-constexpr int NTHREADS = 256;
 constexpr int HD = 128;
 constexpr uint32_t TILE_BYTES = BT * HD * 2;
 constexpr uint32_t HALF_BYTES = TILE_BYTES / 2;
@@ -53,9 +55,6 @@ constexpr uint32_t IDESC_SS = ptx::idesc_bf16_f32(128, 128, 0, 0);  // K-major A
 constexpr uint32_t IDESC_TS = ptx::idesc_bf16_f32(128, 128, 0, 1);  // A in TMEM, B MN-major
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr int32_t STATUS_TIMEOUT = -4;
-// six tiles (two resident, two double-buffered pairs), alignment slack, barriers + TMEM slot, LSE/D staging
-constexpr uint32_t CTRL_BYTES = 128;
-constexpr uint32_t SMEM_BYTES = 6 * TILE_BYTES + 1024 + CTRL_BYTES + 2 * 2 * BT * 4;
 
 struct BwdTcParams {
     int B, Hq, Hkv, N, g, w, window_mode, G;
@@ -75,80 +74,9 @@ __device__ __forceinline__ float bf(uint32_t w, int hi) {
     return __uint_as_float(hi ? (w & 0xffff0000u) : (w << 16));
 }
 
-// Shared-memory carve-up common to both kernels: six 32 KB tiles from a
-// 1024-aligned base, then barriers, the TMEM slot and two staging arrays.
-struct Smem {
-    uint32_t tile[6];  // shared addresses
-    uint64_t *bars;    // [0] resident pair, [1..2] double buffer, [3] mma, [4] drain
-    uint32_t *tmem_slot;
-    float *stage;      // 2 x 2 x BT floats
-};
-
-__device__ __forceinline__ Smem carve(uint8_t *raw) {
-    Smem s;
-    const uint32_t r = ptx::smem_addr(raw);
-    const uint32_t base = (r + 1023u) & ~1023u;
-    uint8_t *g = raw + (base - r);
-    for (int k = 0; k < 6; ++k) s.tile[k] = base + k * TILE_BYTES;
-    s.bars = reinterpret_cast<uint64_t *>(g + 6 * TILE_BYTES);
-    s.tmem_slot = reinterpret_cast<uint32_t *>(g + 6 * TILE_BYTES + 64);
-    s.stage = reinterpret_cast<float *>(g + 6 * TILE_BYTES + CTRL_BYTES);
-    return s;
-}
-
 __device__ __forceinline__ void load_tile(const void *map, uint32_t bar, uint32_t dst, int y, int z) {
     ptx::tma_load_3d(map, bar, dst, 0, y, z);
     ptx::tma_load_3d(map, bar, dst + HALF_BYTES, 64, y, z);
-}
-
-// Block-level wait: every thread polls, the CTA agrees on the outcome.  On a
-// time-out thread 0 gives the awaited operation one more bounded wait so that
-// nothing is still writing shared memory when the CTA leaves.
-struct Waiter {
-    uint64_t limit;
-    volatile int flag;
-    __device__ __forceinline__ bool operator()(uint32_t bar, uint32_t parity) {
-        const bool mine = ptx::wait_bounded(bar, parity, &flag, limit);
-        if (!__syncthreads_or(!mine)) return true;
-        if (threadIdx.x == 0) {
-            flag = 0;
-            ptx::wait_bounded(bar, parity, &flag, limit);
-        }
-        return false;
-    }
-};
-
-__device__ __forceinline__ uint32_t tmem_setup(const Smem &sm, int nbars) {
-    if (threadIdx.x == 0) {
-        for (int k = 0; k < nbars; ++k) ptx::mbar_init(ptx::smem_addr(&sm.bars[k]), 1);
-        ptx::fence_mbar_init();
-    }
-    if (threadIdx.x < 32) {
-        ptx::tmem_alloc(ptx::smem_addr(sm.tmem_slot), 512);
-        ptx::tmem_relinquish();
-    }
-    ptx::tc_fence_before();
-    __syncthreads();
-    ptx::tc_fence_after();
-    return *sm.tmem_slot;
-}
-
-// Leaves the CTA: after an abort, waits (bounded) for every tcgen05 op issued so far;
-// then frees TMEM and reports the time-out.
-__device__ __forceinline__ void tmem_teardown(const Smem &sm, uint32_t tmem, bool ok, const BwdTcParams &p) {
-    if (!ok && threadIdx.x == 0) {
-        volatile int flag = 0;
-        const uint32_t drain = ptx::smem_addr(&sm.bars[4]);
-        ptx::tc_commit(drain);
-        ptx::wait_bounded(drain, 0, &flag, p.wait_limit_ns);
-        if (p.status != nullptr) atomicCAS(p.status, 0, STATUS_TIMEOUT);
-    }
-    ptx::tc_fence_before();
-    __syncthreads();
-    if (threadIdx.x < 32) {
-        ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem, 512);
-    }
 }
 
 // Writes this thread's 64 fp32 values (columns [64*ch, 64*ch + 64) of TMEM row `row`,
@@ -187,20 +115,42 @@ __device__ __forceinline__ void store_tile_f32(const CUtensorMap *map, uint32_t 
 }
 
 // ---------------------------------------------------------------- dQ
-// 256 threads: warps w and w + 4 share TMEM lanes 32*(w%4)..+31 (the rows) and split the
-// 128 columns, 64 each (ch = w / 4).
-__global__ void __launch_bounds__(NTHREADS, 1)
+// One 128-row query tile of one (b, h) per CTA, over the forward's key tiles (cores,
+// then the band).  Warp-specialised, 320 threads:
+//   warp 0      producer: Q and dO once, then K(t), V(t) into one of two stages (TMA);
+//   warp 1      MMA issuer: S = Q K^T, dP = dO V^T (SS), then, once the element-wise
+//               warps have written dS, dQ += dS K (TS, K read MN-major);
+//   warps 2..9  element-wise: dS = P (dP - D) as bf16 over S, P = 2^(S tau log2e - LSE);
+//               warps w and w + 4 share TMEM lanes 32*(w%4)..+31 (the query rows) and split
+//               the 128 key columns, 64 each.  Each also computes D = dO . O of its row (and
+//               the first of the pair stores it for the dK/dV kernel).
+// TMEM: S | dP | dQ.
+constexpr int DQ_THREADS = 320;
+constexpr uint32_t DQ_OFF_STAGE = 2 * TILE_BYTES;                // Q, dO resident
+constexpr uint32_t DQ_OFF_BAR = DQ_OFF_STAGE + 2 * 2 * TILE_BYTES;  // two K+V stages
+constexpr int QB_QD = 0, QB_FULL = 1, QB_EMPTY = 3, QB_SFULL = 5, QB_PFULL = 6, QB_DONE = 7, QB_DRAIN = 8;
+constexpr int DQ_NBARS = 9;
+constexpr uint32_t DQ_OFF_TMEM = DQ_OFF_BAR + DQ_NBARS * 8;
+constexpr uint32_t DQ_OFF_ABORT = DQ_OFF_TMEM + 4;
+constexpr uint32_t DQ_SMEM = DQ_OFF_ABORT + 4 + 1024;  // + slack for the 1024-byte alignment
+static_assert(DQ_SMEM <= 232448, "shared memory budget");
+
+__global__ void __launch_bounds__(DQ_THREADS, 1)
     bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
                      const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                      const __grid_constant__ CUtensorMap tmKc, const __grid_constant__ CUtensorMap tmVc,
                      const __grid_constant__ CUtensorMap tmdQ, const BwdTcParams p) {
     extern __shared__ uint8_t smem_raw[];
-    const Smem sm = carve(smem_raw);
-    const uint32_t sQ = sm.tile[0], sdO = sm.tile[1];
-    const uint32_t b_qd = ptx::smem_addr(&sm.bars[0]), b_mma = ptx::smem_addr(&sm.bars[3]);
+    const uint32_t r0 = ptx::smem_addr(smem_raw);
+    const uint32_t base = (r0 + 1023u) & ~1023u;
+    uint8_t *const gb = smem_raw + (base - r0);
+    const uint32_t sQ = base, sdO = base + TILE_BYTES;
+    auto stage_k = [&](int st) { return base + DQ_OFF_STAGE + static_cast<uint32_t>(st) * 2 * TILE_BYTES; };
+    auto bar = [&](int k) { return base + DQ_OFF_BAR + 8u * k; };
+    volatile int *const abort_flag = reinterpret_cast<volatile int *>(gb + DQ_OFF_ABORT);
+    const uint64_t lim = p.wait_limit_ns;
+
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-    const int quarter = warp & 3, ch = warp >> 2;
-    const int row = quarter * 32 + lane;
     const int BH = p.B * p.Hq, n_qt = (p.N + BT - 1) / BT;
     const int qt = n_qt - 1 - static_cast<int>(blockIdx.x / BH);  // heaviest tiles first
     const int bh = static_cast<int>(blockIdx.x % BH);
@@ -210,130 +160,176 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int Tc = (lo_of(i1, p.w) / p.g + BT - 1) / BT;  // core tiles
     const int T = Tc + (i1 - lo0) / BT + 1;               // + band tiles
 
-    const uint32_t tmem = tmem_setup(sm, 5);
-    const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-    Waiter wait{p.wait_limit_ns, 0};
-
-    auto issue_kv = [&](int tt) {
-        const bool core = tt < Tc;
-        const int y0 = core ? tt * BT : lo0 + (tt - Tc) * BT;
-        const uint32_t bar = ptx::smem_addr(&sm.bars[1 + (tt & 1)]);
-        ptx::mbar_arrive_expect_tx(bar, 2 * TILE_BYTES);
-        load_tile(core ? (const void *)&tmKc : (const void *)&tmK, bar, sm.tile[2 + 2 * (tt & 1)], y0, kvz);
-        load_tile(core ? (const void *)&tmVc : (const void *)&tmV, bar, sm.tile[3 + 2 * (tt & 1)], y0, kvz);
-    };
-    if (t == 0 && !p.skip_loads) {
-        ptx::mbar_arrive_expect_tx(b_qd, 2 * TILE_BYTES);
-        load_tile(&tmQ, b_qd, sQ, i0, bh);
-        load_tile(&tmdO, b_qd, sdO, i0, bh);
-        issue_kv(0);
-    }
-
-    // this thread's row: D = dO . O (the two column halves add their partial sums; also
-    // stored for the dkv kernel) and the LSE in log2 units
-    const int i = i0 + row;
-    const bool valid = i < p.N;
-    float Dpart = 0.f, lse2 = 0.f;
-    const int64_t u = static_cast<int64_t>(bh) * p.N + i;
-    if (valid) {
-        const uint4 *o4 = reinterpret_cast<const uint4 *>(p.O + u * HD) + ch * 8;
-        const uint4 *d4 = reinterpret_cast<const uint4 *>(p.dO + u * HD) + ch * 8;
-#pragma unroll 4
-        for (int c = 0; c < 8; ++c) {
-            const uint4 a = o4[c], b = d4[c];
-            const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-            for (int k = 0; k < 4; ++k) Dpart += bf(aw[k], 0) * bf(bw[k], 0) + bf(aw[k], 1) * bf(bw[k], 1);
+    if (t == 0) {
+        ptx::mbar_init(bar(QB_QD), 1);
+        for (int st = 0; st < 2; ++st) {
+            ptx::mbar_init(bar(QB_FULL + st), 1);
+            ptx::mbar_init(bar(QB_EMPTY + st), 1);
         }
-        lse2 = p.LSE[u] * LOG2E;
+        ptx::mbar_init(bar(QB_SFULL), 1);
+        ptx::mbar_init(bar(QB_PFULL), 8);  // one arrive per element-wise warp
+        ptx::mbar_init(bar(QB_DONE), 1);
+        ptx::mbar_init(bar(QB_DRAIN), 1);
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
     }
-    sm.stage[t] = Dpart;
+    if (warp == 0) {
+        ptx::tmem_alloc(base + DQ_OFF_TMEM, 512);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
     __syncthreads();
-    const float Di = sm.stage[row] + sm.stage[BT + row];
-    if (valid && ch == 0) p.Dbuf[u] = Di;
-    const int lo_i = win_of(p, i), nc_i = lo_of(i, p.w) / p.g;
-    const float c1 = p.tau * LOG2E;
-    const uint64_t dQd = ptx::smem_desc_sw128(sQ, 16, 1024), ddOd = ptx::smem_desc_sw128(sdO, 16, 1024);
+    ptx::tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<uint32_t *>(gb + DQ_OFF_TMEM);
 
-    bool ok = wait(b_qd, 0);
-    uint32_t mma_phase = 0;
-    for (int tt = 0; ok && tt < T; ++tt) {
-        const bool core = tt < Tc;
-        const int y0 = core ? tt * BT : lo0 + (tt - Tc) * BT;
-        const uint32_t sK = sm.tile[2 + 2 * (tt & 1)], sV = sm.tile[3 + 2 * (tt & 1)];
-        if (!(ok = wait(ptx::smem_addr(&sm.bars[1 + (tt & 1)]), (tt >> 1) & 1))) break;
-        if (warp == 0) {
-            // queued behind the previous tile's dQ MMA, which still reads dS from S
+    if (warp == 0) {
+        // ---------------------------------------------------------------- producer
+        if (lane == 0 && !p.skip_loads) {
+            ptx::mbar_arrive_expect_tx(bar(QB_QD), 2 * TILE_BYTES);
+            load_tile(&tmQ, bar(QB_QD), sQ, i0, bh);
+            load_tile(&tmdO, bar(QB_QD), sdO, i0, bh);
+            int tt = 0;
+            for (; tt < T; ++tt) {
+                const int st = tt & 1;
+                if (tt >= 2 && !ptx::wait_bounded(bar(QB_EMPTY + st), ((tt >> 1) & 1) ^ 1, abort_flag, lim)) break;
+                const bool core = tt < Tc;
+                const int y0 = core ? tt * BT : lo0 + (tt - Tc) * BT;
+                ptx::mbar_arrive_expect_tx(bar(QB_FULL + st), 2 * TILE_BYTES);
+                load_tile(core ? (const void *)&tmKc : (const void *)&tmK, bar(QB_FULL + st), stage_k(st), y0, kvz);
+                load_tile(core ? (const void *)&tmVc : (const void *)&tmV, bar(QB_FULL + st), stage_k(st) + TILE_BYTES,
+                          y0, kvz);
+            }
+            if (*abort_flag) {
+                // let the copies already issued land before the CTA exits
+                volatile int never = 0;
+                ptx::wait_bounded(bar(QB_QD), 0, &never, lim);
+                for (int x = tt > 2 ? tt - 2 : 0; x < tt; ++x)
+                    ptx::wait_bounded(bar(QB_FULL + (x & 1)), (x >> 1) & 1, &never, lim);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issuer
+        auto wwait = [&](uint32_t bb, uint32_t parity) -> bool {
+            return __all_sync(0xffffffffu, ptx::wait_bounded(bb, parity, abort_flag, lim));
+        };
+        const uint64_t dQd = ptx::smem_desc_sw128(sQ, 16, 1024), ddOd = ptx::smem_desc_sw128(sdO, 16, 1024);
+        bool ok = wwait(bar(QB_QD), 0);
+        for (int tt = 0; ok && tt < T; ++tt) {
+            const int st = tt & 1;
+            const uint32_t sK = stage_k(st), sV = sK + TILE_BYTES;
+            if (!(ok = wwait(bar(QB_FULL + st), (tt >> 1) & 1))) break;
             ptx::tc_fence_after();
             ptx::mma_ss_k128_warp(tmem + 0, dQd, ptx::smem_desc_sw128(sK, 16, 1024), IDESC_SS, 0u);     // S  = Q K^T
             ptx::mma_ss_k128_warp(tmem + 128, ddOd, ptx::smem_desc_sw128(sV, 16, 1024), IDESC_SS, 0u);  // dP = dO V^T
-            ptx::tc_commit_warp(b_mma);
-        }
-        if (!(ok = wait(b_mma, mma_phase++ & 1))) break;
-        // MMAs complete in issue order, so the previous tile's dQ MMA is done: its K/V
-        // buffer takes the next tile's copy
-        if (t == 0 && tt + 1 < T && !p.skip_loads) issue_kv(tt + 1);
-        ptx::tc_fence_after();
-        // dS = P (dP - D) on this row's visible columns.  The half ch reads S and dP
-        // columns [64ch, 64ch + 64) and writes their bf16 dS pairs to S columns
-        // [64ch, 64ch + 32), which it has already read.
-        int c_lo = 0, c_hi = BT - 1;
-        if (core) {
-            c_hi = min(nc_i - y0, BT) - 1;
-        } else {
-            c_lo = max(lo_i - y0, 0);
-            c_hi = min(i - y0, BT - 1);
-        }
-        if (!valid) c_hi = -1;
-#pragma unroll 1
-        for (int j = 0; j < 2; ++j) {
-            const int c = 2 * ch + j;
-            uint32_t s[32], dp[32];
-            ptx::tmem_ld32(tmem + lane_addr + c * 32, s);
-            ptx::tmem_ld32(tmem + lane_addr + 128 + c * 32, dp);
-            ptx::tmem_wait_ld(s);
-            ptx::reg_touch(dp);
-            uint32_t pk[16];
-#pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                float d2[2];
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int col = c * 32 + 2 * k + e;
-                    const bool vis = col >= c_lo && col <= c_hi;
-                    const float pr = vis ? ptx::ex2(fmaf(__uint_as_float(s[2 * k + e]), c1, -lse2)) : 0.f;
-                    d2[e] = pr * (__uint_as_float(dp[2 * k + e]) - Di);
-                }
-                pk[k] = ptx::pack_bf16x2(d2[0], d2[1]);
-            }
-            ptx::tmem_st16(tmem + lane_addr + ch * 64 + j * 16, pk);
-        }
-        ptx::tmem_wait_st();
-        ptx::tc_fence_before();
-        __syncthreads();
-        if (warp == 0) {
+            ptx::tc_commit_warp(bar(QB_SFULL));
+            if (!(ok = wwait(bar(QB_PFULL), tt & 1))) break;
             ptx::tc_fence_after();
             ptx::mma_ts_k128_split_warp(tmem + 256, tmem + 0, ptx::smem_desc_sw128(sK, HALF_BYTES, 1024), IDESC_TS,
-                                        tt > 0 ? 1u : 0u);  // dQ += dS K, completion covered by the next wait
+                                        tt > 0 ? 1u : 0u);  // dQ += dS K
+            ptx::tc_commit_warp(bar(QB_EMPTY + st));  // the stage is free once this has read it
+        }
+        ptx::tc_commit_warp(ok ? bar(QB_DONE) : bar(QB_DRAIN));
+        if (!ok) {
+            // whatever was issued must complete before tensor memory is freed
+            volatile int never = 0;
+            ptx::wait_bounded(bar(QB_DRAIN), 0, &never, lim);
+        }
+    } else {
+        // ---------------------------------------------------------------- element-wise
+        const int ch = (warp - 2) >> 2;
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+        // this thread's row: D = dO . O over all 128 columns (both warps of the pair compute
+        // it; the first stores it for the dK/dV kernel) and the LSE in log2 units
+        const int i = i0 + row;
+        const bool valid = i < p.N;
+        float Di = 0.f, lse2 = 0.f;
+        const int64_t u = static_cast<int64_t>(bh) * p.N + i;
+        if (valid) {
+            const uint4 *o4 = reinterpret_cast<const uint4 *>(p.O + u * HD);
+            const uint4 *d4 = reinterpret_cast<const uint4 *>(p.dO + u * HD);
+#pragma unroll 4
+            for (int c = 0; c < 16; ++c) {
+                const uint4 a = o4[c], bb = d4[c];
+                const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {bb.x, bb.y, bb.z, bb.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) Di += bf(aw[k], 0) * bf(bw[k], 0) + bf(aw[k], 1) * bf(bw[k], 1);
+            }
+            lse2 = p.LSE[u] * LOG2E;
+            if (ch == 0) p.Dbuf[u] = Di;
+        }
+        const int lo_i = win_of(p, i), nc_i = lo_of(i, p.w) / p.g;
+        const float c1 = p.tau * LOG2E;
+        bool ok = true;
+        for (int tt = 0; tt < T; ++tt) {
+            if (!__all_sync(0xffffffffu, ptx::wait_bounded(bar(QB_SFULL), tt & 1, abort_flag, lim))) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            const bool core = tt < Tc;
+            const int y0 = core ? tt * BT : lo0 + (tt - Tc) * BT;
+            // dS = P (dP - D) on this row's visible columns.  The half ch reads S and dP
+            // columns [64ch, 64ch + 64) and writes their bf16 dS pairs to S columns
+            // [64ch, 64ch + 32), which it has already read.
+            int c_lo = 0, c_hi = BT - 1;
+            if (core) {
+                c_hi = min(nc_i - y0, BT) - 1;
+            } else {
+                c_lo = max(lo_i - y0, 0);
+                c_hi = min(i - y0, BT - 1);
+            }
+            if (!valid) c_hi = -1;
+#pragma unroll 1
+            for (int j = 0; j < 2; ++j) {
+                const int c = 2 * ch + j;
+                uint32_t sv[32], dp[32];
+                ptx::tmem_ld32(tmem + lane_addr + c * 32, sv);
+                ptx::tmem_ld32(tmem + lane_addr + 128 + c * 32, dp);
+                ptx::tmem_wait_ld(sv);
+                ptx::reg_touch(dp);
+                uint32_t pk[16];
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    float d2[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int col = c * 32 + 2 * k + e;
+                        const bool vis = col >= c_lo && col <= c_hi;
+                        const float pr = vis ? ptx::ex2(fmaf(__uint_as_float(sv[2 * k + e]), c1, -lse2)) : 0.f;
+                        d2[e] = pr * (__uint_as_float(dp[2 * k + e]) - Di);
+                    }
+                    pk[k] = ptx::pack_bf16x2(d2[0], d2[1]);
+                }
+                ptx::tmem_st16(tmem + lane_addr + ch * 64 + j * 16, pk);
+            }
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar(QB_PFULL));
+        }
+        if (ok && !__all_sync(0xffffffffu, ptx::wait_bounded(bar(QB_DONE), 0, abort_flag, lim))) ok = false;
+        if (ok) {
+            // dQ * tau through shared memory (the first K/V stage, idle now) to a tiled store
+            ptx::tc_fence_after();
+            stage_f32_rows(tmem + lane_addr, 256, ch, row, p.tau, false, stage_k(0));
+            ptx::fence_proxy_async_smem();
         }
     }
-    if (ok) {
-        if (warp == 0) ptx::tc_commit_warp(b_mma);
-        ok = wait(b_mma, mma_phase++ & 1);
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (*abort_flag) {
+        if (t == 0 && p.status != nullptr) atomicCAS(p.status, 0, STATUS_TIMEOUT);
+    } else if (t == 0) {
+        store_tile_f32(&tmdQ, stage_k(0), i0, bh);
+        ptx::bulk_wait_all();
     }
-    if (ok) {
-        // dQ * tau through shared memory (the first K/V buffer, idle now) to a tiled store
+    if (warp == 0) {
         ptx::tc_fence_after();
-        const uint32_t stage = sm.tile[2];
-        stage_f32_rows(tmem + lane_addr, 256, ch, row, p.tau, false, stage);
-        ptx::fence_proxy_async_smem();
-        __syncthreads();
-        if (t == 0) {
-            store_tile_f32(&tmdQ, stage, i0, bh);
-            ptx::bulk_wait_all();
-        }
+        ptx::tmem_dealloc(tmem, 512);
     }
-    tmem_teardown(sm, tmem, ok, p);
 }
 
 // ---------------------------------------------------------------- dK, dV
@@ -617,7 +613,7 @@ cudaError_t launch_attn_bwd_tc(const void *Q, const void *K, const void *V, cons
         std::lock_guard<std::mutex> lock(mu);
         Attr &a = attr[dev & 63];
         if (!a.done) {
-            a.err = cudaFuncSetAttribute(bwd_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+            a.err = cudaFuncSetAttribute(bwd_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, DQ_SMEM);
             if (a.err == cudaSuccess)
                 a.err = cudaFuncSetAttribute(bwd_dkv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              DKV_SMEM);
@@ -653,8 +649,8 @@ cudaError_t launch_attn_bwd_tc(const void *Q, const void *K, const void *V, cons
     p.wait_limit_ns = g_wait_limit_ns;
     p.skip_loads = g_skip_q_load;
     const unsigned n_qt = static_cast<unsigned>((s.N + BT - 1) / BT);
-    bwd_dq_tc_kernel<<<n_qt * static_cast<unsigned>(qh), NTHREADS, SMEM_BYTES, stream>>>(mQ, mdO, mK, mV, mKc, mVc,
-                                                                                         mdQ, p);
+    bwd_dq_tc_kernel<<<n_qt * static_cast<unsigned>(qh), DQ_THREADS, DQ_SMEM, stream>>>(mQ, mdO, mK, mV, mKc, mVc,
+                                                                                        mdQ, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const unsigned n_kt = static_cast<unsigned>((G + BT - 1) / BT + (s.N + BT - 1) / BT);
