@@ -117,23 +117,31 @@ __device__ __forceinline__ void store_tile_f32(const CUtensorMap *map, uint32_t 
 // ---------------------------------------------------------------- dQ
 // One 128-row query tile of one (b, h) per CTA, over the forward's key tiles (cores,
 // then the band).  Warp-specialised, 320 threads:
-//   warp 0      producer: Q and dO once, then K(t), V(t) into one of two stages (TMA);
-//   warp 1      MMA issuer: S = Q K^T, dP = dO V^T (SS), then, once the element-wise
-//               warps have written dS, dQ += dS K (TS, K read MN-major);
-//   warps 2..9  element-wise: dS = P (dP - D) as bf16 over S, P = 2^(S tau log2e - LSE);
-//               warps w and w + 4 share TMEM lanes 32*(w%4)..+31 (the query rows) and split
-//               the 128 key columns, 64 each.  Each also computes D = dO . O of its row (and
-//               the first of the pair stores it for the dK/dV kernel).
-// TMEM: S | dP | dQ.
+//   warp 0      producer: Q and dO once, then K(t) into one of three stages and V(t)
+//               into one of two (TMA; K lives longer: S(t) and dQ(t) read it);
+//   warp 1      MMA issuer, per tile t:  S(t+1) = Q K(t+1)^T into the other S buffer,
+//               then (once the element-wise warps have written dS(t)) dQ += dS(t) K(t),
+//               then dP(t+1) = dO V(t+1)^T;
+//   warps 2..9  element-wise: P = 2^(S tau log2e - LSE) as soon as S(t) is there (while
+//               dP(t) is still being computed), then dS = P (dP - D) as bf16 over S.
+//               Warps w and w + 4 share TMEM lanes 32*(w%4)..+31 (the query rows) and
+//               split the 128 key columns, 64 each.  Each also computes D = dO . O of its
+//               row (the first of the pair stores it for the dK/dV kernel).
+// TMEM: S0 | S1 | dP | dQ, 128 columns each.  S is double-buffered so that the tensor
+// pipe computes the next tile's S while this tile's dS is formed.
 constexpr int DQ_THREADS = 320;
-constexpr uint32_t DQ_OFF_STAGE = 2 * TILE_BYTES;                // Q, dO resident
-constexpr uint32_t DQ_OFF_BAR = DQ_OFF_STAGE + 2 * 2 * TILE_BYTES;  // two K+V stages
-constexpr int QB_QD = 0, QB_FULL = 1, QB_EMPTY = 3, QB_SFULL = 5, QB_PFULL = 6, QB_DONE = 7, QB_DRAIN = 8;
-constexpr int DQ_NBARS = 9;
+constexpr int DQ_KST = 3, DQ_VST = 2;
+constexpr uint32_t DQ_OFF_K = 2 * TILE_BYTES;  // after Q, dO
+constexpr uint32_t DQ_OFF_V = DQ_OFF_K + DQ_KST * TILE_BYTES;
+constexpr uint32_t DQ_OFF_BAR = DQ_OFF_V + DQ_VST * TILE_BYTES;
+constexpr int QB_QD = 0, QB_FULLK = 1, QB_EMPTYK = 4, QB_FULLV = 7, QB_EMPTYV = 9, QB_SFULL = 11, QB_DPFULL = 13,
+              QB_PFULL = 14, QB_DONE = 15, QB_DRAIN = 16;
+constexpr int DQ_NBARS = 17;
 constexpr uint32_t DQ_OFF_TMEM = DQ_OFF_BAR + DQ_NBARS * 8;
 constexpr uint32_t DQ_OFF_ABORT = DQ_OFF_TMEM + 4;
 constexpr uint32_t DQ_SMEM = DQ_OFF_ABORT + 4 + 1024;  // + slack for the 1024-byte alignment
 static_assert(DQ_SMEM <= 232448, "shared memory budget");
+static_assert(DQ_KST >= 2, "the fp32 dQ tile is staged over the first two K stages");
 
 __global__ void __launch_bounds__(DQ_THREADS, 1)
     bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
@@ -145,7 +153,8 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     const uint32_t base = (r0 + 1023u) & ~1023u;
     uint8_t *const gb = smem_raw + (base - r0);
     const uint32_t sQ = base, sdO = base + TILE_BYTES;
-    auto stage_k = [&](int st) { return base + DQ_OFF_STAGE + static_cast<uint32_t>(st) * 2 * TILE_BYTES; };
+    auto stage_k = [&](int x) { return base + DQ_OFF_K + static_cast<uint32_t>(x % DQ_KST) * TILE_BYTES; };
+    auto stage_v = [&](int x) { return base + DQ_OFF_V + static_cast<uint32_t>(x % DQ_VST) * TILE_BYTES; };
     auto bar = [&](int k) { return base + DQ_OFF_BAR + 8u * k; };
     volatile int *const abort_flag = reinterpret_cast<volatile int *>(gb + DQ_OFF_ABORT);
     const uint64_t lim = p.wait_limit_ns;
@@ -159,14 +168,21 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     const int lo0 = win_of(p, i0);
     const int Tc = (lo_of(i1, p.w) / p.g + BT - 1) / BT;  // core tiles
     const int T = Tc + (i1 - lo0) / BT + 1;               // + band tiles
+    auto tile_y = [&](int x) { return x < Tc ? x * BT : lo0 + (x - Tc) * BT; };
 
     if (t == 0) {
         ptx::mbar_init(bar(QB_QD), 1);
-        for (int st = 0; st < 2; ++st) {
-            ptx::mbar_init(bar(QB_FULL + st), 1);
-            ptx::mbar_init(bar(QB_EMPTY + st), 1);
+        for (int st = 0; st < DQ_KST; ++st) {
+            ptx::mbar_init(bar(QB_FULLK + st), 1);
+            ptx::mbar_init(bar(QB_EMPTYK + st), 1);
+        }
+        for (int st = 0; st < DQ_VST; ++st) {
+            ptx::mbar_init(bar(QB_FULLV + st), 1);
+            ptx::mbar_init(bar(QB_EMPTYV + st), 1);
         }
         ptx::mbar_init(bar(QB_SFULL), 1);
+        ptx::mbar_init(bar(QB_SFULL + 1), 1);
+        ptx::mbar_init(bar(QB_DPFULL), 1);
         ptx::mbar_init(bar(QB_PFULL), 8);  // one arrive per element-wise warp
         ptx::mbar_init(bar(QB_DONE), 1);
         ptx::mbar_init(bar(QB_DRAIN), 1);
@@ -181,6 +197,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<uint32_t *>(gb + DQ_OFF_TMEM);
+    constexpr uint32_t T_DP = 256, T_DQ = 384;  // TMEM columns; S(t) at 128 * (t & 1)
 
     if (warp == 0) {
         // ---------------------------------------------------------------- producer
@@ -188,23 +205,34 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
             ptx::mbar_arrive_expect_tx(bar(QB_QD), 2 * TILE_BYTES);
             load_tile(&tmQ, bar(QB_QD), sQ, i0, bh);
             load_tile(&tmdO, bar(QB_QD), sdO, i0, bh);
-            int tt = 0;
-            for (; tt < T; ++tt) {
-                const int st = tt & 1;
-                if (tt >= 2 && !ptx::wait_bounded(bar(QB_EMPTY + st), ((tt >> 1) & 1) ^ 1, abort_flag, lim)) break;
-                const bool core = tt < Tc;
-                const int y0 = core ? tt * BT : lo0 + (tt - Tc) * BT;
-                ptx::mbar_arrive_expect_tx(bar(QB_FULL + st), 2 * TILE_BYTES);
-                load_tile(core ? (const void *)&tmKc : (const void *)&tmK, bar(QB_FULL + st), stage_k(st), y0, kvz);
-                load_tile(core ? (const void *)&tmVc : (const void *)&tmV, bar(QB_FULL + st), stage_k(st) + TILE_BYTES,
-                          y0, kvz);
+            int nk = 0, nv = 0;  // tiles whose K / V copies have been issued
+            for (int x = 0; x < T; ++x) {
+                const bool core = x < Tc;
+                // K(x) reuses the stage of K(x - 3) once dQ(x - 3) has read it
+                if (x >= DQ_KST &&
+                    !ptx::wait_bounded(bar(QB_EMPTYK + x % DQ_KST), (x / DQ_KST - 1) & 1, abort_flag, lim))
+                    break;
+                ptx::mbar_arrive_expect_tx(bar(QB_FULLK + x % DQ_KST), TILE_BYTES);
+                load_tile(core ? (const void *)&tmKc : (const void *)&tmK, bar(QB_FULLK + x % DQ_KST), stage_k(x),
+                          tile_y(x), kvz);
+                nk = x + 1;
+                // V(x) reuses the stage of V(x - 2) once dP(x - 2) has read it
+                if (x >= DQ_VST &&
+                    !ptx::wait_bounded(bar(QB_EMPTYV + x % DQ_VST), (x / DQ_VST - 1) & 1, abort_flag, lim))
+                    break;
+                ptx::mbar_arrive_expect_tx(bar(QB_FULLV + x % DQ_VST), TILE_BYTES);
+                load_tile(core ? (const void *)&tmVc : (const void *)&tmV, bar(QB_FULLV + x % DQ_VST), stage_v(x),
+                          tile_y(x), kvz);
+                nv = x + 1;
             }
             if (*abort_flag) {
                 // let the copies already issued land before the CTA exits
                 volatile int never = 0;
                 ptx::wait_bounded(bar(QB_QD), 0, &never, lim);
-                for (int x = tt > 2 ? tt - 2 : 0; x < tt; ++x)
-                    ptx::wait_bounded(bar(QB_FULL + (x & 1)), (x >> 1) & 1, &never, lim);
+                for (int x = nk > DQ_KST ? nk - DQ_KST : 0; x < nk; ++x)
+                    ptx::wait_bounded(bar(QB_FULLK + x % DQ_KST), (x / DQ_KST) & 1, &never, lim);
+                for (int x = nv > DQ_VST ? nv - DQ_VST : 0; x < nv; ++x)
+                    ptx::wait_bounded(bar(QB_FULLV + x % DQ_VST), (x / DQ_VST) & 1, &never, lim);
             }
         }
         __syncwarp();
@@ -214,20 +242,37 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
             return __all_sync(0xffffffffu, ptx::wait_bounded(bb, parity, abort_flag, lim));
         };
         const uint64_t dQd = ptx::smem_desc_sw128(sQ, 16, 1024), ddOd = ptx::smem_desc_sw128(sdO, 16, 1024);
-        bool ok = wwait(bar(QB_QD), 0);
-        for (int tt = 0; ok && tt < T; ++tt) {
-            const int st = tt & 1;
-            const uint32_t sK = stage_k(st), sV = sK + TILE_BYTES;
-            if (!(ok = wwait(bar(QB_FULL + st), (tt >> 1) & 1))) break;
+        auto issue_s = [&](int x) {  // S(x) = Q K(x)^T
             ptx::tc_fence_after();
-            ptx::mma_ss_k128_warp(tmem + 0, dQd, ptx::smem_desc_sw128(sK, 16, 1024), IDESC_SS, 0u);     // S  = Q K^T
-            ptx::mma_ss_k128_warp(tmem + 128, ddOd, ptx::smem_desc_sw128(sV, 16, 1024), IDESC_SS, 0u);  // dP = dO V^T
-            ptx::tc_commit_warp(bar(QB_SFULL));
+            ptx::mma_ss_k128_warp(tmem + 128u * (x & 1), dQd, ptx::smem_desc_sw128(stage_k(x), 16, 1024), IDESC_SS,
+                                  0u);
+            ptx::tc_commit_warp(bar(QB_SFULL + (x & 1)));
+        };
+        auto issue_dp = [&](int x) {  // dP(x) = dO V(x)^T
+            ptx::tc_fence_after();
+            ptx::mma_ss_k128_warp(tmem + T_DP, ddOd, ptx::smem_desc_sw128(stage_v(x), 16, 1024), IDESC_SS, 0u);
+            ptx::tc_commit_warp(bar(QB_DPFULL));
+            ptx::tc_commit_warp(bar(QB_EMPTYV + x % DQ_VST));
+        };
+        bool ok = wwait(bar(QB_QD), 0) && wwait(bar(QB_FULLK), 0);
+        if (ok) issue_s(0);
+        if (ok && (ok = wwait(bar(QB_FULLV), 0))) issue_dp(0);
+        for (int tt = 0; ok && tt < T; ++tt) {
+            const int x = tt + 1;
+            if (x < T) {
+                if (!(ok = wwait(bar(QB_FULLK + x % DQ_KST), (x / DQ_KST) & 1))) break;
+                issue_s(x);
+            }
             if (!(ok = wwait(bar(QB_PFULL), tt & 1))) break;
             ptx::tc_fence_after();
-            ptx::mma_ts_k128_split_warp(tmem + 256, tmem + 0, ptx::smem_desc_sw128(sK, HALF_BYTES, 1024), IDESC_TS,
+            ptx::mma_ts_k128_split_warp(tmem + T_DQ, tmem + 128u * (tt & 1),
+                                        ptx::smem_desc_sw128(stage_k(tt), HALF_BYTES, 1024), IDESC_TS,
                                         tt > 0 ? 1u : 0u);  // dQ += dS K
-            ptx::tc_commit_warp(bar(QB_EMPTY + st));  // the stage is free once this has read it
+            ptx::tc_commit_warp(bar(QB_EMPTYK + tt % DQ_KST));  // K(tt)'s stage is free once this has read it
+            if (x < T) {
+                if (!(ok = wwait(bar(QB_FULLV + x % DQ_VST), (x / DQ_VST) & 1))) break;
+                issue_dp(x);
+            }
         }
         ptx::tc_commit_warp(ok ? bar(QB_DONE) : bar(QB_DRAIN));
         if (!ok) {
@@ -240,6 +285,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
         const int ch = (warp - 2) >> 2;
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
+        const int h0 = ch * 64;  // this warp's 64 key columns of the tile
         const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
         // this thread's row: D = dO . O over all 128 columns (both warps of the pair compute
         // it; the first stores it for the dK/dV kernel) and the LSE in log2 units
@@ -264,47 +310,66 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
         const float c1 = p.tau * LOG2E;
         bool ok = true;
         for (int tt = 0; tt < T; ++tt) {
-            if (!__all_sync(0xffffffffu, ptx::wait_bounded(bar(QB_SFULL), tt & 1, abort_flag, lim))) {
+            if (!__all_sync(0xffffffffu, ptx::wait_bounded(bar(QB_SFULL + (tt & 1)), (tt >> 1) & 1, abort_flag, lim))) {
                 ok = false;
                 break;
             }
             ptx::tc_fence_after();
-            const bool core = tt < Tc;
-            const int y0 = core ? tt * BT : lo0 + (tt - Tc) * BT;
-            // dS = P (dP - D) on this row's visible columns.  The half ch reads S and dP
-            // columns [64ch, 64ch + 64) and writes their bf16 dS pairs to S columns
-            // [64ch, 64ch + 32), which it has already read.
+            const uint32_t sS = tmem + lane_addr + 128u * (tt & 1) + h0;
+            uint32_t pa[32], pb[32];
+            ptx::tmem_ld32(sS, pa);
+            ptx::tmem_ld32(sS + 32, pb);
+            // the row's visible key columns of this tile
+            const int y0 = tile_y(tt);
             int c_lo = 0, c_hi = BT - 1;
-            if (core) {
+            if (tt < Tc) {
                 c_hi = min(nc_i - y0, BT) - 1;
             } else {
                 c_lo = max(lo_i - y0, 0);
                 c_hi = min(i - y0, BT - 1);
             }
             if (!valid) c_hi = -1;
-#pragma unroll 1
-            for (int j = 0; j < 2; ++j) {
-                const int c = 2 * ch + j;
-                uint32_t sv[32], dp[32];
-                ptx::tmem_ld32(tmem + lane_addr + c * 32, sv);
-                ptx::tmem_ld32(tmem + lane_addr + 128 + c * 32, dp);
-                ptx::tmem_wait_ld(sv);
-                ptx::reg_touch(dp);
-                uint32_t pk[16];
+            ptx::tmem_wait_ld(pa);
+            ptx::reg_touch(pb);
+            // P = 2^(S tau log2e - LSE), zero off the visible columns
+            if (__all_sync(0xffffffffu, c_lo <= h0 && c_hi >= h0 + 63)) {
 #pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    float d2[2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int col = c * 32 + 2 * k + e;
-                        const bool vis = col >= c_lo && col <= c_hi;
-                        const float pr = vis ? ptx::ex2(fmaf(__uint_as_float(sv[2 * k + e]), c1, -lse2)) : 0.f;
-                        d2[e] = pr * (__uint_as_float(dp[2 * k + e]) - Di);
-                    }
-                    pk[k] = ptx::pack_bf16x2(d2[0], d2[1]);
+                for (int k = 0; k < 32; ++k) {
+                    pa[k] = __float_as_uint(ptx::ex2(fmaf(__uint_as_float(pa[k]), c1, -lse2)));
+                    pb[k] = __float_as_uint(ptx::ex2(fmaf(__uint_as_float(pb[k]), c1, -lse2)));
                 }
-                ptx::tmem_st16(tmem + lane_addr + ch * 64 + j * 16, pk);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    const int ca = h0 + k, cb = h0 + 32 + k;
+                    pa[k] = (ca >= c_lo && ca <= c_hi)
+                                ? __float_as_uint(ptx::ex2(fmaf(__uint_as_float(pa[k]), c1, -lse2))) : 0u;
+                    pb[k] = (cb >= c_lo && cb <= c_hi)
+                                ? __float_as_uint(ptx::ex2(fmaf(__uint_as_float(pb[k]), c1, -lse2))) : 0u;
+                }
             }
+            if (!__all_sync(0xffffffffu, ptx::wait_bounded(bar(QB_DPFULL), tt & 1, abort_flag, lim))) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            // dS = P (dP - D), bf16 pairs written over the S columns [h0, h0 + 32), which
+            // this warp has already read
+            uint32_t dp[32], pk[16];
+            ptx::tmem_ld32(tmem + lane_addr + T_DP + h0, dp);
+            ptx::tmem_wait_ld(dp);
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+                pk[k] = ptx::pack_bf16x2(__uint_as_float(pa[2 * k]) * (__uint_as_float(dp[2 * k]) - Di),
+                                         __uint_as_float(pa[2 * k + 1]) * (__uint_as_float(dp[2 * k + 1]) - Di));
+            ptx::tmem_st16(sS, pk);
+            ptx::tmem_ld32(tmem + lane_addr + T_DP + h0 + 32, dp);
+            ptx::tmem_wait_ld(dp);
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+                pk[k] = ptx::pack_bf16x2(__uint_as_float(pb[2 * k]) * (__uint_as_float(dp[2 * k]) - Di),
+                                         __uint_as_float(pb[2 * k + 1]) * (__uint_as_float(dp[2 * k + 1]) - Di));
+            ptx::tmem_st16(sS + 16, pk);
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
             __syncwarp();
@@ -312,9 +377,9 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
         }
         if (ok && !__all_sync(0xffffffffu, ptx::wait_bounded(bar(QB_DONE), 0, abort_flag, lim))) ok = false;
         if (ok) {
-            // dQ * tau through shared memory (the first K/V stage, idle now) to a tiled store
+            // dQ * tau through shared memory (the first two K stages, idle now) to a tiled store
             ptx::tc_fence_after();
-            stage_f32_rows(tmem + lane_addr, 256, ch, row, p.tau, false, stage_k(0));
+            stage_f32_rows(tmem + lane_addr, T_DQ, ch, row, p.tau, false, base + DQ_OFF_K);
             ptx::fence_proxy_async_smem();
         }
     }
@@ -323,7 +388,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     if (*abort_flag) {
         if (t == 0 && p.status != nullptr) atomicCAS(p.status, 0, STATUS_TIMEOUT);
     } else if (t == 0) {
-        store_tile_f32(&tmdQ, stage_k(0), i0, bh);
+        store_tile_f32(&tmdQ, base + DQ_OFF_K, i0, bh);
         ptx::bulk_wait_all();
     }
     if (warp == 0) {
