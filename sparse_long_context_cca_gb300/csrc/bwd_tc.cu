@@ -139,7 +139,9 @@ constexpr int QB_QD = 0, QB_FULLK = 1, QB_EMPTYK = 4, QB_FULLV = 7, QB_EMPTYV = 
 constexpr int DQ_NBARS = 17;
 constexpr uint32_t DQ_OFF_TMEM = DQ_OFF_BAR + DQ_NBARS * 8;
 constexpr uint32_t DQ_OFF_ABORT = DQ_OFF_TMEM + 4;
-constexpr uint32_t DQ_SMEM = DQ_OFF_ABORT + 4 + 1024;  // + slack for the 1024-byte alignment
+constexpr uint32_t DQ_OFF_DPART = DQ_OFF_BAR + 256;                // 2 x 128 partial sums of D
+constexpr uint32_t DQ_SMEM = DQ_OFF_DPART + 2 * BT * 4 + 1024;  // + slack for the 1024-byte alignment
+static_assert(DQ_OFF_ABORT + 4 <= DQ_OFF_DPART, "control words overlap the D staging");
 static_assert(DQ_SMEM <= 232448, "shared memory budget");
 static_assert(DQ_KST >= 2, "the fp32 dQ tile is staged over the first two K stages");
 
@@ -171,6 +173,14 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     auto tile_y = [&](int x) { return x < Tc ? x * BT : lo0 + (x - Tc) * BT; };
 
     if (t == 0) {
+        // the first use of each descriptor would otherwise wait for its fetch
+        ptx::prefetch_tmap(&tmQ);
+        ptx::prefetch_tmap(&tmdO);
+        ptx::prefetch_tmap(&tmKc);
+        ptx::prefetch_tmap(&tmVc);
+        ptx::prefetch_tmap(&tmK);
+        ptx::prefetch_tmap(&tmV);
+        ptx::prefetch_tmap(&tmdQ);
         ptx::mbar_init(bar(QB_QD), 1);
         for (int st = 0; st < DQ_KST; ++st) {
             ptx::mbar_init(bar(QB_FULLK + st), 1);
@@ -287,25 +297,37 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
         const int row = quarter * 32 + lane;
         const int h0 = ch * 64;  // this warp's 64 key columns of the tile
         const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-        // this thread's row: D = dO . O over all 128 columns (both warps of the pair compute
-        // it; the first stores it for the dK/dV kernel) and the LSE in log2 units
+        // this thread's row: D = dO . O (the pair's two halves of 64 columns each add their
+        // partial sums through shared memory; the first stores D for the dK/dV kernel) and
+        // the LSE in log2 units.  O comes from global memory (all eight 16-byte loads in
+        // flight at once), dO from the swizzled tile already copied for the MMAs.
         const int i = i0 + row;
         const bool valid = i < p.N;
-        float Di = 0.f, lse2 = 0.f;
         const int64_t u = static_cast<int64_t>(bh) * p.N + i;
+        uint4 o4[8];
+        float lse2 = 0.f;
         if (valid) {
-            const uint4 *o4 = reinterpret_cast<const uint4 *>(p.O + u * HD);
-            const uint4 *d4 = reinterpret_cast<const uint4 *>(p.dO + u * HD);
-#pragma unroll 4
-            for (int c = 0; c < 16; ++c) {
-                const uint4 a = o4[c], bb = d4[c];
-                const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {bb.x, bb.y, bb.z, bb.w};
+            const uint4 *src = reinterpret_cast<const uint4 *>(p.O + u * HD) + ch * 8;
 #pragma unroll
-                for (int k = 0; k < 4; ++k) Di += bf(aw[k], 0) * bf(bw[k], 0) + bf(aw[k], 1) * bf(bw[k], 1);
-            }
+            for (int c = 0; c < 8; ++c) o4[c] = src[c];
             lse2 = p.LSE[u] * LOG2E;
-            if (ch == 0) p.Dbuf[u] = Di;
         }
+        float Dpart = 0.f;
+        if (__all_sync(0xffffffffu, ptx::wait_bounded(bar(QB_QD), 0, abort_flag, lim)) && valid) {
+            const uint32_t rbase = sdO + ch * HALF_BYTES + row * 128;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const uint4 d = ptx::ld_shared_v4(rbase + ((c ^ (row & 7)) << 4));
+                const uint32_t aw[4] = {o4[c].x, o4[c].y, o4[c].z, o4[c].w}, bw[4] = {d.x, d.y, d.z, d.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) Dpart += bf(aw[k], 0) * bf(bw[k], 0) + bf(aw[k], 1) * bf(bw[k], 1);
+            }
+        }
+        float *const dpart = reinterpret_cast<float *>(gb + DQ_OFF_DPART);
+        dpart[ch * BT + row] = Dpart;
+        ptx::named_bar_sync(1, 256);  // the eight element-wise warps, every one of them, always
+        const float Di = dpart[row] + dpart[BT + row];
+        if (valid && ch == 0) p.Dbuf[u] = Di;
         const int lo_i = win_of(p, i), nc_i = lo_of(i, p.w) / p.g;
         const float c1 = p.tau * LOG2E;
         bool ok = true;
@@ -389,7 +411,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
         if (t == 0 && p.status != nullptr) atomicCAS(p.status, 0, STATUS_TIMEOUT);
     } else if (t == 0) {
         store_tile_f32(&tmdQ, base + DQ_OFF_K, i0, bh);
-        ptx::bulk_wait_all();
+        ptx::bulk_wait_read();
     }
     if (warp == 0) {
         ptx::tc_fence_after();
