@@ -422,28 +422,36 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
 // ---------------------------------------------------------------- dK, dV
 // One 128-key tile (raw tokens or cores) of one (b, kv) per CTA, over the query tiles of
 // the r query heads that see it.  Warp-specialised, 320 threads:
-//   warp 0      producer: K and V once; per query tile, Q and dO (lane 0, TMA) into one
-//               of two stages, and the tile's LSE and D staged by the whole warp;
-//   warp 1      MMA issuer (whole warp, one elected lane):
-//                 S^T = K Q^T, dP^T = V dO^T          (SS, into TMEM)
-//                 dV += P^T dO,  dK += dS^T Q          (TS, once the element-wise step is done)
-//   warps 2..9  element-wise: P^T = 2^(S^T tau log2e - LSE) and dS^T = P^T (dP^T - D), as
-//               bf16 over S^T and dP^T; warps w and w + 4 share TMEM lanes 32*(w%4)..+31
-//               (the keys) and split each query tile's 128 columns, 64 each.
-// The hand-offs are mbarriers, so no step waits for a whole-CTA barrier.  TMEM:
-// S^T | dP^T | dK | dV; the MMAs of one thread complete in issue order, so the next
-// tile's S^T/dP^T, issued after this tile's dV/dK MMAs, never overwrite what they read.
+//   warp 0      producer: K and V once; per query tile x, Q(x) into one of three stages
+//               and dO(x) into one of two (TMA; Q lives longer: S^T(x) and dK(x) read it);
+//   warp 1      MMA issuer (whole warp, one elected lane), per query tile x:
+//                 dV += P^T dO(x)            once P^T(x) is written,
+//                 S^T(x+1) = K Q(x+1)^T      (the S^T buffer is free again),
+//                 dK += dS^T Q(x)            once dS^T(x) is written,
+//                 dP^T(x+1) = V dO(x+1)^T    (the dP^T buffer is free again);
+//   warps 2..9  element-wise, in two phases per tile: P^T = 2^(S^T tau log2e - LSE) as
+//               bf16 over S^T (kept in fp32 registers), then dS^T = P^T (dP^T - D) as bf16
+//               over dP^T.  Warps w and w + 4 share TMEM lanes 32*(w%4)..+31 (the keys)
+//               and split each query tile's 128 columns, 64 each.  They also keep the
+//               tile's LSE and D in one shared-memory slot: each of the 256 threads loads
+//               one value of the next tile early and writes it between two named barriers.
+// The hand-offs are mbarriers.  TMEM: S^T | dP^T | dK | dV; the MMAs of one thread
+// complete in issue order, so S^T(x+1) and dP^T(x+1), issued after dV(x) and dK(x),
+// never overwrite what those read.
 constexpr int DKV_THREADS = 320;
-constexpr uint32_t DKV_STAGE = 2 * TILE_BYTES;  // Q + dO of one query tile
-constexpr uint32_t DKV_OFF_STAGE = 2 * TILE_BYTES;
-constexpr uint32_t DKV_OFF_LD = DKV_OFF_STAGE + 2 * DKV_STAGE;          // LSE/D staging, 2 x 2 x 128 floats
-constexpr uint32_t DKV_OFF_BAR = DKV_OFF_LD + 2 * 2 * BT * 4;
-constexpr int DB_KV = 0, DB_FULL = 1, DB_EMPTY = 3, DB_SFULL = 5, DB_PFULL = 6, DB_DONE = 7, DB_DRAIN = 8;
-constexpr int DKV_NBARS = 9;
+constexpr int DKV_QST = 3, DKV_OST = 2;
+constexpr uint32_t DKV_OFF_Q = 2 * TILE_BYTES;  // after K, V
+constexpr uint32_t DKV_OFF_O = DKV_OFF_Q + DKV_QST * TILE_BYTES;
+constexpr uint32_t DKV_OFF_SLOT = DKV_OFF_O + DKV_OST * TILE_BYTES;  // LSE (log2 units) 128 | D 128
+constexpr uint32_t DKV_OFF_BAR = DKV_OFF_SLOT + 2 * BT * 4;
+constexpr int DB_KV = 0, DB_FULLQ = 1, DB_EMPTYQ = 4, DB_FULLO = 7, DB_EMPTYO = 9, DB_SFULL = 11, DB_DPFULL = 12,
+              DB_PFULL = 13, DB_DSFULL = 14, DB_DONE = 15, DB_DRAIN = 16;
+constexpr int DKV_NBARS = 17;
 constexpr uint32_t DKV_OFF_TMEM = DKV_OFF_BAR + DKV_NBARS * 8;
 constexpr uint32_t DKV_OFF_ABORT = DKV_OFF_TMEM + 4;
 constexpr uint32_t DKV_SMEM = DKV_OFF_ABORT + 4 + 1024;  // + slack for the 1024-byte alignment
 static_assert(DKV_SMEM <= 232448, "shared memory budget");
+static_assert(DKV_QST + DKV_OST >= 4, "the fp32 dK and dV tiles are staged over the Q and dO stages");
 
 __global__ void __launch_bounds__(DKV_THREADS, 1)
     bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
@@ -457,8 +465,9 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
     const uint32_t base = (r0 + 1023u) & ~1023u;
     uint8_t *const gb = smem_raw + (base - r0);
     const uint32_t sK = base, sV = base + TILE_BYTES;
-    auto stage_q = [&](int st) { return base + DKV_OFF_STAGE + static_cast<uint32_t>(st) * DKV_STAGE; };
-    float *const ld_stage = reinterpret_cast<float *>(gb + DKV_OFF_LD);  // [stage][LSE 128 | D 128]
+    auto stage_q = [&](int x) { return base + DKV_OFF_Q + static_cast<uint32_t>(x % DKV_QST) * TILE_BYTES; };
+    auto stage_o = [&](int x) { return base + DKV_OFF_O + static_cast<uint32_t>(x % DKV_OST) * TILE_BYTES; };
+    const uint32_t slot = base + DKV_OFF_SLOT;
     auto bar = [&](int k) { return base + DKV_OFF_BAR + 8u * k; };
     volatile int *const abort_flag = reinterpret_cast<volatile int *>(gb + DKV_OFF_ABORT);
     const uint64_t lim = p.wait_limit_ns;
@@ -493,13 +502,26 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
     auto i0_of = [&](int it) { return (qt_lo + it % nq) * BT; };
 
     if (t == 0) {
+        // the first use of each descriptor would otherwise wait for its fetch
+        ptx::prefetch_tmap(core ? (const void *)&tmKc : (const void *)&tmK);
+        ptx::prefetch_tmap(core ? (const void *)&tmVc : (const void *)&tmV);
+        ptx::prefetch_tmap(&tmQ);
+        ptx::prefetch_tmap(&tmdO);
+        ptx::prefetch_tmap(core ? (const void *)&tmdKc : (const void *)&tmdK);
+        ptx::prefetch_tmap(core ? (const void *)&tmdVc : (const void *)&tmdV);
         ptx::mbar_init(bar(DB_KV), 1);
-        for (int st = 0; st < 2; ++st) {
-            ptx::mbar_init(bar(DB_FULL + st), 2);  // the copies' arm + the LSE/D staging
-            ptx::mbar_init(bar(DB_EMPTY + st), 1);
+        for (int st = 0; st < DKV_QST; ++st) {
+            ptx::mbar_init(bar(DB_FULLQ + st), 1);
+            ptx::mbar_init(bar(DB_EMPTYQ + st), 1);
+        }
+        for (int st = 0; st < DKV_OST; ++st) {
+            ptx::mbar_init(bar(DB_FULLO + st), 1);
+            ptx::mbar_init(bar(DB_EMPTYO + st), 1);
         }
         ptx::mbar_init(bar(DB_SFULL), 1);
-        ptx::mbar_init(bar(DB_PFULL), 8);  // one arrive per element-wise warp
+        ptx::mbar_init(bar(DB_DPFULL), 1);
+        ptx::mbar_init(bar(DB_PFULL), 8);   // one arrive per element-wise warp
+        ptx::mbar_init(bar(DB_DSFULL), 8);  // one arrive per element-wise warp
         ptx::mbar_init(bar(DB_DONE), 1);
         ptx::mbar_init(bar(DB_DRAIN), 1);
         *abort_flag = 0;
@@ -513,46 +535,41 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<uint32_t *>(gb + DKV_OFF_TMEM);
+    constexpr uint32_t T_DP = 128, T_DK = 256, T_DV = 384;  // TMEM columns; S^T at 0
 
     if (warp == 0) {
         // ---------------------------------------------------------------- producer
-        int it = 0;
-        bool ok = true;
-        if (lane == 0 && !p.skip_loads) {
+        if (lane == 0 && !p.skip_loads && n_it > 0) {
             ptx::mbar_arrive_expect_tx(bar(DB_KV), 2 * TILE_BYTES);
             load_tile(core ? (const void *)&tmKc : (const void *)&tmK, bar(DB_KV), sK, y0, bk);
             load_tile(core ? (const void *)&tmVc : (const void *)&tmV, bar(DB_KV), sV, y0, bk);
-        }
-        for (; it < n_it; ++it) {
-            const int st = it & 1;
-            if (it >= 2 &&
-                !__all_sync(0xffffffffu, ptx::wait_bounded(bar(DB_EMPTY + st), ((it >> 1) & 1) ^ 1, abort_flag, lim))) {
-                ok = false;
-                break;
+            int nqd = 0, nod = 0;  // tiles whose Q / dO copies have been issued
+            for (int x = 0; x < n_it; ++x) {
+                const int bh = bh_of(x), i0 = i0_of(x);
+                // Q(x) reuses the stage of Q(x - 3) once dK(x - 3) has read it
+                if (x >= DKV_QST &&
+                    !ptx::wait_bounded(bar(DB_EMPTYQ + x % DKV_QST), (x / DKV_QST - 1) & 1, abort_flag, lim))
+                    break;
+                ptx::mbar_arrive_expect_tx(bar(DB_FULLQ + x % DKV_QST), TILE_BYTES);
+                load_tile(&tmQ, bar(DB_FULLQ + x % DKV_QST), stage_q(x), i0, bh);
+                nqd = x + 1;
+                // dO(x) reuses the stage of dO(x - 2) once dV(x - 2) has read it
+                if (x >= DKV_OST &&
+                    !ptx::wait_bounded(bar(DB_EMPTYO + x % DKV_OST), (x / DKV_OST - 1) & 1, abort_flag, lim))
+                    break;
+                ptx::mbar_arrive_expect_tx(bar(DB_FULLO + x % DKV_OST), TILE_BYTES);
+                load_tile(&tmdO, bar(DB_FULLO + x % DKV_OST), stage_o(x), i0, bh);
+                nod = x + 1;
             }
-            const int bh = bh_of(it), i0 = i0_of(it);
-            if (lane == 0 && !p.skip_loads) {
-                ptx::mbar_arrive_expect_tx(bar(DB_FULL + st), 2 * TILE_BYTES);
-                load_tile(&tmQ, bar(DB_FULL + st), stage_q(st), i0, bh);
-                load_tile(&tmdO, bar(DB_FULL + st), stage_q(st) + TILE_BYTES, i0, bh);
+            if (*abort_flag) {
+                // let the copies already issued land before the CTA exits
+                volatile int never = 0;
+                ptx::wait_bounded(bar(DB_KV), 0, &never, lim);
+                for (int x = nqd > DKV_QST ? nqd - DKV_QST : 0; x < nqd; ++x)
+                    ptx::wait_bounded(bar(DB_FULLQ + x % DKV_QST), (x / DKV_QST) & 1, &never, lim);
+                for (int x = nod > DKV_OST ? nod - DKV_OST : 0; x < nod; ++x)
+                    ptx::wait_bounded(bar(DB_FULLO + x % DKV_OST), (x / DKV_OST) & 1, &never, lim);
             }
-            // this tile's LSE (log2 units) and D, rows past N as zeros
-            float *ls = ld_stage + st * 2 * BT;
-#pragma unroll
-            for (int k = 0; k < BT / 32; ++k) {
-                const int iq = i0 + k * 32 + lane;
-                const int64_t off = static_cast<int64_t>(bh) * p.N + iq;
-                ls[k * 32 + lane] = iq < p.N ? p.LSE[off] * LOG2E : 0.f;
-                ls[BT + k * 32 + lane] = iq < p.N ? p.Dbuf[off] : 0.f;
-            }
-            __syncwarp();
-            if (lane == 0 && !p.skip_loads) ptx::mbar_arrive(bar(DB_FULL + st));
-        }
-        if (!ok && lane == 0 && !p.skip_loads) {
-            // let the copies already issued land before the CTA exits
-            volatile int never = 0;
-            for (int x = it > 2 ? it - 2 : 0; x < it; ++x)
-                ptx::wait_bounded(bar(DB_FULL + (x & 1)), (x >> 1) & 1, &never, lim);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -561,23 +578,41 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
             return __all_sync(0xffffffffu, ptx::wait_bounded(bb, parity, abort_flag, lim));
         };
         const uint64_t dKk = ptx::smem_desc_sw128(sK, 16, 1024), dVk = ptx::smem_desc_sw128(sV, 16, 1024);
-        bool ok = n_it == 0 || wwait(bar(DB_KV), 0);
-        for (int it = 0; ok && it < n_it; ++it) {
-            const int st = it & 1;
-            const uint32_t sQ = stage_q(st), sdO = sQ + TILE_BYTES;
-            if (!(ok = wwait(bar(DB_FULL + st), (it >> 1) & 1))) break;
+        auto issue_s = [&](int x) {  // S^T(x) = K Q(x)^T
             ptx::tc_fence_after();
-            ptx::mma_ss_k128_warp(tmem + 0, dKk, ptx::smem_desc_sw128(sQ, 16, 1024), IDESC_SS, 0u);     // S^T  = K Q^T
-            ptx::mma_ss_k128_warp(tmem + 128, dVk, ptx::smem_desc_sw128(sdO, 16, 1024), IDESC_SS, 0u);  // dP^T = V dO^T
+            ptx::mma_ss_k128_warp(tmem + 0, dKk, ptx::smem_desc_sw128(stage_q(x), 16, 1024), IDESC_SS, 0u);
             ptx::tc_commit_warp(bar(DB_SFULL));
+        };
+        auto issue_dp = [&](int x) {  // dP^T(x) = V dO(x)^T
+            ptx::tc_fence_after();
+            ptx::mma_ss_k128_warp(tmem + T_DP, dVk, ptx::smem_desc_sw128(stage_o(x), 16, 1024), IDESC_SS, 0u);
+            ptx::tc_commit_warp(bar(DB_DPFULL));
+        };
+        bool ok = n_it == 0 || (wwait(bar(DB_KV), 0) && wwait(bar(DB_FULLQ), 0));
+        if (ok && n_it > 0) issue_s(0);
+        if (ok && n_it > 0 && (ok = wwait(bar(DB_FULLO), 0))) issue_dp(0);
+        for (int it = 0; ok && it < n_it; ++it) {
+            const int x = it + 1;
+            const uint32_t acc = it > 0 ? 1u : 0u;
             if (!(ok = wwait(bar(DB_PFULL), it & 1))) break;
             ptx::tc_fence_after();
-            const uint32_t acc = it > 0 ? 1u : 0u;
-            ptx::mma_ts_k128_split_warp(tmem + 384, tmem + 0, ptx::smem_desc_sw128(sdO, HALF_BYTES, 1024), IDESC_TS,
-                                        acc);  // dV += P^T dO
-            ptx::mma_ts_k128_split_warp(tmem + 256, tmem + 128, ptx::smem_desc_sw128(sQ, HALF_BYTES, 1024),
-                                        IDESC_TS, acc);  // dK += dS^T Q
-            ptx::tc_commit_warp(bar(DB_EMPTY + st));  // the stage is free once these have read it
+            ptx::mma_ts_k128_split_warp(tmem + T_DV, tmem + 0, ptx::smem_desc_sw128(stage_o(it), HALF_BYTES, 1024),
+                                        IDESC_TS, acc);  // dV += P^T dO
+            ptx::tc_commit_warp(bar(DB_EMPTYO + it % DKV_OST));
+            if (x < n_it) {
+                if (!(ok = wwait(bar(DB_FULLQ + x % DKV_QST), (x / DKV_QST) & 1))) break;
+                issue_s(x);
+            }
+            if (!(ok = wwait(bar(DB_DSFULL), it & 1))) break;
+            ptx::tc_fence_after();
+            ptx::mma_ts_k128_split_warp(tmem + T_DK, tmem + T_DP,
+                                        ptx::smem_desc_sw128(stage_q(it), HALF_BYTES, 1024), IDESC_TS,
+                                        acc);  // dK += dS^T Q
+            ptx::tc_commit_warp(bar(DB_EMPTYQ + it % DKV_QST));
+            if (x < n_it) {
+                if (!(ok = wwait(bar(DB_FULLO + x % DKV_OST), (x / DKV_OST) & 1))) break;
+                issue_dp(x);
+            }
         }
         ptx::tc_commit_warp(ok ? bar(DB_DONE) : bar(DB_DRAIN));
         if (!ok) {
@@ -590,76 +625,127 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
         const int ch = (warp - 2) >> 2;
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
+        const int h0 = ch * 64;  // this warp's 64 query columns of the tile
         const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
         const int m = y0 + row;  // this thread's key (core index or token)
         const float c1 = p.tau * LOG2E;
         int64_t key_last = 0;
         if (!core) key_last = p.window_mode ? static_cast<int64_t>(m / p.g + 1) * p.g + p.w - 2 : static_cast<int64_t>(m) + p.w - 1;
+        // this thread's value of the LSE/D slot: LSE (log2 units) of query e, or D of query e - 128
+        const int e = (warp - 2) * 32 + lane;
+        auto slot_value = [&](int x) -> float {
+            const int iq = i0_of(x) + (e & (BT - 1));
+            if (iq >= p.N) return 0.f;
+            const int64_t off = static_cast<int64_t>(bh_of(x)) * p.N + iq;
+            return e < BT ? p.LSE[off] * LOG2E : p.Dbuf[off];
+        };
+        float *const slot_f = reinterpret_cast<float *>(gb + DKV_OFF_SLOT);
+        if (n_it > 0) slot_f[e] = slot_value(0);
+        ptx::named_bar_sync(1, 256);
         bool ok = true;
+        // Every element-wise thread runs every iteration and both named barriers of it, so
+        // that a time-out (which skips the work) cannot leave a barrier short of threads.
         for (int it = 0; it < n_it; ++it) {
-            // S^T, dP^T of this tile are in TMEM; the stage's FULL barrier (already complete, and
-            // it cannot move on before this step's arrive) orders the producer's LSE/D staging
-            if (!__all_sync(0xffffffffu, ptx::wait_bounded(bar(DB_SFULL), it & 1, abort_flag, lim)) ||
-                !__all_sync(0xffffffffu, ptx::wait_bounded(bar(DB_FULL + (it & 1)), (it >> 1) & 1, abort_flag, lim))) {
-                ok = false;
-                break;
-            }
-            ptx::tc_fence_after();
-            const int i0 = i0_of(it);
-            const float *s_lse = ld_stage + (it & 1) * 2 * BT, *s_D = s_lse + BT;
-            // this key's visible query columns [q_lo, q_hi] of the tile
-            int q_lo, q_hi;
-            if (m >= n_keys) {
-                q_lo = 0;
-                q_hi = -1;
-            } else if (core) {
-                q_lo = max((m + 1) * p.g + p.w - 1 - i0, 0);
-                q_hi = min(p.N - 1 - i0, BT - 1);
-            } else {
-                const int last_i = static_cast<int>(key_last < p.N - 1 ? key_last : p.N - 1);
-                q_lo = max(m - i0, 0);
-                q_hi = min(last_i - i0, BT - 1);
-            }
-            // the half ch handles query columns [64ch, 64ch + 64): P^T to S^T columns
-            // [64ch, 64ch + 32), dS^T to dP^T columns [64ch, 64ch + 32), both already read
-#pragma unroll 1
-            for (int j = 0; j < 2; ++j) {
-                const int c = 2 * ch + j;
-                uint32_t sv[32], dp[32];
-                ptx::tmem_ld32(tmem + lane_addr + c * 32, sv);
-                ptx::tmem_ld32(tmem + lane_addr + 128 + c * 32, dp);
-                ptx::tmem_wait_ld(sv);
-                ptx::reg_touch(dp);
-                uint32_t pp[16], dd[16];
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    float pv[2], dv[2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int col = c * 32 + 2 * k + e;
-                        const bool vis = col >= q_lo && col <= q_hi;
-                        const float pr = vis ? ptx::ex2(fmaf(__uint_as_float(sv[2 * k + e]), c1, -s_lse[col])) : 0.f;
-                        pv[e] = pr;
-                        dv[e] = pr * (__uint_as_float(dp[2 * k + e]) - s_D[col]);
-                    }
-                    pp[k] = ptx::pack_bf16x2(pv[0], pv[1]);
-                    dd[k] = ptx::pack_bf16x2(dv[0], dv[1]);
+            const float v_next = it + 1 < n_it ? slot_value(it + 1) : 0.f;
+            if (ok) ok = __all_sync(0xffffffffu, ptx::wait_bounded(bar(DB_SFULL), it & 1, abort_flag, lim));
+            uint32_t pa[32], pb[32];
+            if (ok) {
+                ptx::tc_fence_after();
+                const uint32_t sS = tmem + lane_addr + h0;
+                ptx::tmem_ld32(sS, pa);
+                ptx::tmem_ld32(sS + 32, pb);
+                // this key's visible query columns [q_lo, q_hi] of the tile
+                const int i0 = i0_of(it);
+                int q_lo, q_hi;
+                if (m >= n_keys) {
+                    q_lo = 0;
+                    q_hi = -1;
+                } else if (core) {
+                    q_lo = max((m + 1) * p.g + p.w - 1 - i0, 0);
+                    q_hi = min(p.N - 1 - i0, BT - 1);
+                } else {
+                    const int last_i = static_cast<int>(key_last < p.N - 1 ? key_last : p.N - 1);
+                    q_lo = max(m - i0, 0);
+                    q_hi = min(last_i - i0, BT - 1);
                 }
-                ptx::tmem_st16(tmem + lane_addr + ch * 64 + j * 16, pp);        // P^T  over S^T
-                ptx::tmem_st16(tmem + lane_addr + 128 + ch * 64 + j * 16, dd);  // dS^T over dP^T
+                ptx::tmem_wait_ld(pa);
+                ptx::reg_touch(pb);
+                // P^T = 2^(S^T tau log2e - LSE), zero off the visible columns
+                const bool full = __all_sync(0xffffffffu, q_lo <= h0 && q_hi >= h0 + 63);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const uint4 la = ptx::ld_shared_v4(slot + (h0 + 4 * q) * 4);
+                    const uint4 lb = ptx::ld_shared_v4(slot + (h0 + 32 + 4 * q) * 4);
+                    const float lsa[4] = {__uint_as_float(la.x), __uint_as_float(la.y), __uint_as_float(la.z),
+                                          __uint_as_float(la.w)};
+                    const float lsb[4] = {__uint_as_float(lb.x), __uint_as_float(lb.y), __uint_as_float(lb.z),
+                                          __uint_as_float(lb.w)};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int ka = 4 * q + k;
+                        const float xa = ptx::ex2(fmaf(__uint_as_float(pa[ka]), c1, -lsa[k]));
+                        const float xb = ptx::ex2(fmaf(__uint_as_float(pb[ka]), c1, -lsb[k]));
+                        const int ca = h0 + ka, cb = h0 + 32 + ka;
+                        pa[ka] = __float_as_uint(full || (ca >= q_lo && ca <= q_hi) ? xa : 0.f);
+                        pb[ka] = __float_as_uint(full || (cb >= q_lo && cb <= q_hi) ? xb : 0.f);
+                    }
+                }
+                uint32_t pk[16];
+#pragma unroll
+                for (int k = 0; k < 16; ++k) pk[k] = ptx::pack_bf16x2(__uint_as_float(pa[2 * k]), __uint_as_float(pa[2 * k + 1]));
+                ptx::tmem_st16(sS, pk);  // P^T over S^T columns [h0, h0 + 16), already read
+#pragma unroll
+                for (int k = 0; k < 16; ++k) pk[k] = ptx::pack_bf16x2(__uint_as_float(pb[2 * k]), __uint_as_float(pb[2 * k + 1]));
+                ptx::tmem_st16(sS + 16, pk);
+                ptx::tmem_wait_st();
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar(DB_PFULL));
             }
-            ptx::tmem_wait_st();
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(bar(DB_PFULL));
+            if (ok) ok = __all_sync(0xffffffffu, ptx::wait_bounded(bar(DB_DPFULL), it & 1, abort_flag, lim));
+            if (ok) {
+                ptx::tc_fence_after();
+                // dS^T = P^T (dP^T - D), bf16 pairs over dP^T columns [h0, h0 + 32), which this
+                // warp has already read
+                const uint32_t sD = tmem + lane_addr + T_DP + h0;
+                uint32_t dp[32], dd[16];
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    ptx::tmem_ld32(sD + 32 * j, dp);
+                    ptx::tmem_wait_ld(dp);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const uint4 dv = ptx::ld_shared_v4(slot + (BT + h0 + 32 * j + 4 * q) * 4);
+                        const float Dv[4] = {__uint_as_float(dv.x), __uint_as_float(dv.y), __uint_as_float(dv.z),
+                                             __uint_as_float(dv.w)};
+                        const uint32_t *pp = j ? pb : pa;
+#pragma unroll
+                        for (int k = 0; k < 2; ++k) {
+                            const int c = 4 * q + 2 * k;
+                            dd[2 * q + k] = ptx::pack_bf16x2(
+                                __uint_as_float(pp[c]) * (__uint_as_float(dp[c]) - Dv[2 * k]),
+                                __uint_as_float(pp[c + 1]) * (__uint_as_float(dp[c + 1]) - Dv[2 * k + 1]));
+                        }
+                    }
+                    ptx::tmem_st16(sD + 16 * j, dd);
+                }
+                ptx::tmem_wait_st();
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar(DB_DSFULL));
+            }
+            // the slot moves on to the next tile once every warp is done with this one
+            ptx::named_bar_sync(1, 256);
+            slot_f[e] = v_next;
+            ptx::named_bar_sync(1, 256);
         }
         if (ok && !__all_sync(0xffffffffu, ptx::wait_bounded(bar(DB_DONE), 0, abort_flag, lim))) ok = false;
         if (ok) {
-            // dK * tau and dV through shared memory (the Q/dO stages, idle now) to tiled
+            // dK * tau and dV through shared memory (the Q and dO stages, idle now) to tiled
             // stores; a tile no query row sees stores zeros
             ptx::tc_fence_after();
-            stage_f32_rows(tmem + lane_addr, 256, ch, row, p.tau, n_it == 0, stage_q(0));
-            stage_f32_rows(tmem + lane_addr, 384, ch, row, 1.f, n_it == 0, stage_q(1));
+            stage_f32_rows(tmem + lane_addr, T_DK, ch, row, p.tau, n_it == 0, base + DKV_OFF_Q);
+            stage_f32_rows(tmem + lane_addr, T_DV, ch, row, 1.f, n_it == 0, base + DKV_OFF_Q + 2 * TILE_BYTES);
             ptx::fence_proxy_async_smem();
         }
     }
@@ -668,9 +754,9 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
     if (*abort_flag) {
         if (t == 0 && p.status != nullptr) atomicCAS(p.status, 0, STATUS_TIMEOUT);
     } else if (t == 0) {
-        store_tile_f32(core ? &tmdKc : &tmdK, stage_q(0), y0, bk);
-        store_tile_f32(core ? &tmdVc : &tmdV, stage_q(1), y0, bk);
-        ptx::bulk_wait_all();
+        store_tile_f32(core ? &tmdKc : &tmdK, base + DKV_OFF_Q, y0, bk);
+        store_tile_f32(core ? &tmdVc : &tmdV, base + DKV_OFF_Q + 2 * TILE_BYTES, y0, bk);
+        ptx::bulk_wait_read();
     }
     if (warp == 0) {
         ptx::tc_fence_after();
