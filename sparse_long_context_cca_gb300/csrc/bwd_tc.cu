@@ -467,7 +467,6 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
     const uint32_t sK = base, sV = base + TILE_BYTES;
     auto stage_q = [&](int x) { return base + DKV_OFF_Q + static_cast<uint32_t>(x % DKV_QST) * TILE_BYTES; };
     auto stage_o = [&](int x) { return base + DKV_OFF_O + static_cast<uint32_t>(x % DKV_OST) * TILE_BYTES; };
-    const uint32_t slot = base + DKV_OFF_SLOT;
     auto bar = [&](int k) { return base + DKV_OFF_BAR + 8u * k; };
     volatile int *const abort_flag = reinterpret_cast<volatile int *>(gb + DKV_OFF_ABORT);
     const uint64_t lim = p.wait_limit_ns;
@@ -640,6 +639,7 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
             return e < BT ? p.LSE[off] * LOG2E : p.Dbuf[off];
         };
         float *const slot_f = reinterpret_cast<float *>(gb + DKV_OFF_SLOT);
+        const float4 *const slot4 = reinterpret_cast<const float4 *>(slot_f);
         if (n_it > 0) slot_f[e] = slot_value(0);
         ptx::named_bar_sync(1, 256);
         bool ok = true;
@@ -670,24 +670,32 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
                 }
                 ptx::tmem_wait_ld(pa);
                 ptx::reg_touch(pb);
-                // P^T = 2^(S^T tau log2e - LSE), zero off the visible columns
-                const bool full = __all_sync(0xffffffffu, q_lo <= h0 && q_hi >= h0 + 63);
+                // P^T = 2^(S^T tau log2e - LSE), zero off the visible columns (the LSE of four
+                // columns per shared-memory load, the same address across the warp)
+                if (__all_sync(0xffffffffu, q_lo <= h0 && q_hi >= h0 + 63)) {
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const uint4 la = ptx::ld_shared_v4(slot + (h0 + 4 * q) * 4);
-                    const uint4 lb = ptx::ld_shared_v4(slot + (h0 + 32 + 4 * q) * 4);
-                    const float lsa[4] = {__uint_as_float(la.x), __uint_as_float(la.y), __uint_as_float(la.z),
-                                          __uint_as_float(la.w)};
-                    const float lsb[4] = {__uint_as_float(lb.x), __uint_as_float(lb.y), __uint_as_float(lb.z),
-                                          __uint_as_float(lb.w)};
+                    for (int q = 0; q < 8; ++q) {
+                        const float4 la = slot4[h0 / 4 + q], lb = slot4[h0 / 4 + 8 + q];
+                        const float lsa[4] = {la.x, la.y, la.z, la.w}, lsb[4] = {lb.x, lb.y, lb.z, lb.w};
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int ka = 4 * q + k;
-                        const float xa = ptx::ex2(fmaf(__uint_as_float(pa[ka]), c1, -lsa[k]));
-                        const float xb = ptx::ex2(fmaf(__uint_as_float(pb[ka]), c1, -lsb[k]));
-                        const int ca = h0 + ka, cb = h0 + 32 + ka;
-                        pa[ka] = __float_as_uint(full || (ca >= q_lo && ca <= q_hi) ? xa : 0.f);
-                        pb[ka] = __float_as_uint(full || (cb >= q_lo && cb <= q_hi) ? xb : 0.f);
+                        for (int k = 0; k < 4; ++k) {
+                            pa[4 * q + k] = __float_as_uint(ptx::ex2(fmaf(__uint_as_float(pa[4 * q + k]), c1, -lsa[k])));
+                            pb[4 * q + k] = __float_as_uint(ptx::ex2(fmaf(__uint_as_float(pb[4 * q + k]), c1, -lsb[k])));
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const float4 la = slot4[h0 / 4 + q], lb = slot4[h0 / 4 + 8 + q];
+                        const float lsa[4] = {la.x, la.y, la.z, la.w}, lsb[4] = {lb.x, lb.y, lb.z, lb.w};
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const int ka = 4 * q + k, ca = h0 + ka, cb = h0 + 32 + ka;
+                            const float xa = ptx::ex2(fmaf(__uint_as_float(pa[ka]), c1, -lsa[k]));
+                            const float xb = ptx::ex2(fmaf(__uint_as_float(pb[ka]), c1, -lsb[k]));
+                            pa[ka] = __float_as_uint(ca >= q_lo && ca <= q_hi ? xa : 0.f);
+                            pb[ka] = __float_as_uint(cb >= q_lo && cb <= q_hi ? xb : 0.f);
+                        }
                     }
                 }
                 uint32_t pk[16];
@@ -715,9 +723,8 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
                     ptx::tmem_wait_ld(dp);
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
-                        const uint4 dv = ptx::ld_shared_v4(slot + (BT + h0 + 32 * j + 4 * q) * 4);
-                        const float Dv[4] = {__uint_as_float(dv.x), __uint_as_float(dv.y), __uint_as_float(dv.z),
-                                             __uint_as_float(dv.w)};
+                        const float4 dv = slot4[(BT + h0) / 4 + 8 * j + q];
+                        const float Dv[4] = {dv.x, dv.y, dv.z, dv.w};
                         const uint32_t *pp = j ? pb : pa;
 #pragma unroll
                         for (int k = 0; k < 2; ++k) {
