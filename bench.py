@@ -422,11 +422,14 @@ def backward_bench(wl, dev, stream, iters, peaks):
     flops = 2.5 * W.attn_flops(wl)
     del Q, K, V, O, LSE, Kc, Vc, dO, grads
     torch.cuda.empty_cache()
-    return {"what": "backward of pooling + fused attention (tcgen05 dQ and dK/dV kernels, "
-                    "fp32 CUDA-core pooling backward)", "ms": ms,
-            "eff_tflops": flops / (ms / 1e3) / 1e12,
+    eff = flops / (ms / 1e3) / 1e12
+    return {"what": "backward of pooling + fused attention: tcgen05 dQ kernel, tcgen05 dK/dV kernel over the "
+                    "core tiles, the pooling backward as per-token scalars (CUDA cores, fp32), then the "
+                    "dK/dV kernel over the raw-token tiles adding the pooling terms as it writes each row",
+            "ms": ms, "eff_tflops": eff,
+            "frac_of_bf16_burst": eff / peaks["bf16_tflops"] if peaks.get("bf16_tflops") else None,
             "algorithmic_unit": "10*d FLOP per (query, visible key, head): q.k, dO.v, dQ, dK, dV",
-            "kernel_launches": 3}
+            "kernel_launches": 4}
 
 
 def comparator(wl, dev, stream, steps, cca_ms_per_step):

@@ -214,7 +214,9 @@ int cca_pool_group(const void *q, const void *K, const void *V, void *Kc, void *
  * maximum.  bf16 with d = 128 computes the attention gradients on the tensor
  * cores (bf16 operands, fp32 accumulation, P and dS rounded to bf16 before
  * their products); every other case, and the pooling backward, runs on CUDA
- * cores in fp32.  A kernel that gives up waiting writes CCA_ERR_TIMEOUT into
+ * cores in fp32 (with softmax or mean pooling at bf16, d = 128, the pooling
+ * backward's share of each raw token's row is added as the tensor-core kernel
+ * writes that row).  A kernel that gives up waiting writes CCA_ERR_TIMEOUT into
  * *params.dev_status when that pointer is set (4-byte aligned); the gradients
  * are then undefined.
  */

@@ -24,6 +24,11 @@
 // consecutive elements): per query row (dQ, D), per raw token (dK, dV), per
 // core (dKc, dVc into the workspace), per group (pooling backward, added into
 // dK, dV and the group-last rows of dQ).  P is recomputed from the forward's LSE.
+// bf16 with d = 128 runs the attention part on the tensor cores (bwd_tc.cu); with
+// softmax or mean pooling it then computes the cores' gradients first, reduces the
+// pooling backward to per-token scalars (a_t, (tau/r) ds_t) and per-group qsum_j, and
+// lets the raw tokens' dK/dV kernel add a_t dKc_j + (tau/r) ds_t qsum_j and a_t dVc_j
+// to each row as it writes it, instead of a second fp32 pass over dK and dV.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -407,22 +412,196 @@ __global__ void __launch_bounds__(128) bwd_pool_kernel(const T *__restrict__ Q, 
     for (int hh = 0; hh < r; ++hh) add_row<PL>(dQ + ((b * a.Hq + kv * r + hh) * a.N + last) * D, lane, dqs);
 }
 
+// Sums each of the 32 values v[0..31] over the warp in 31 shuffles (a halving butterfly:
+// at each step a lane keeps the half of its values whose index bit matches its own lane
+// bit and receives the partner's share of it); lane l returns the total of v[l].
+__device__ __forceinline__ float warp_transpose_sum32(float (&v)[32], int lane) {
+#pragma unroll
+    for (int o = 16, n = 16; o > 0; o >>= 1, n >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < n; ++i) {
+            const float keep = up ? v[i + n] : v[i];
+            const float send = up ? v[i] : v[i + n];
+            v[i] = keep + __shfl_xor_sync(kFull, send, o);
+        }
+    }
+    return v[0];
+}
+
+// The method's pooling backward, reduced to what the dK/dV kernel needs to fold it into
+// the raw tokens' rows (BwdPoolFuse mode 2): per token a_t and (tau/r) ds_t, per group
+// qsum_j in fp32; the group-last queries' term (tau/r) sum_t ds_t k_t goes into dQ here.
+// One warp per group, keys in chunks of 16: each lane forms its partial dot products for
+// the chunk's 16 scores s_t and 16 values da_t = dKc_j . k_t + dVc_j . v_t, one
+// transposed reduction finishes all 32, and an online softmax carries the normaliser and
+// sum_u exp(s_u) da_u across chunks.  A second pass (reusing the one chunk of a group of
+// at most 16 tokens, else recomputing) writes a_t, (tau/r) ds_t and sums the dQ term.
+template <typename T, int D>
+__global__ void __launch_bounds__(128) bwd_pool_scalars_kernel(const T *__restrict__ Q, const T *__restrict__ K,
+                                                               const T *__restrict__ V, const float *__restrict__ dKc,
+                                                               const float *__restrict__ dVc, float *__restrict__ dQ,
+                                                               float *__restrict__ pa, float *__restrict__ pcds,
+                                                               float *__restrict__ pqs, const BwdArgs a) {
+    constexpr int PL = D / 32;
+    const int lane = threadIdx.x & 31;
+    const int G = a.N / a.g;
+    const int64_t u = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (u >= static_cast<int64_t>(a.B) * a.Hkv * G) return;
+    const int j = static_cast<int>(u % G);
+    const int64_t bk = u / G;
+    const int64_t b = bk / a.Hkv, kv = bk % a.Hkv;
+    const int r = a.Hq / a.Hkv, g = a.g;
+    float dkc[PL], dvc[PL];
+    load_row<float, PL>(dKc + u * D, lane, dkc);
+    load_row<float, PL>(dVc + u * D, lane, dvc);
+    const int64_t row0 = bk * a.N + static_cast<int64_t>(j) * g;  // first token of the group
+    const float c = a.tau / r;
+    const int last = (j + 1) * g - 1;
+    float qs[PL];
+#pragma unroll
+    for (int e = 0; e < PL; ++e) qs[e] = 0.f;
+    for (int hh = 0; hh < r; ++hh) {
+        float f[PL];
+        load_row<T, PL>(Q + ((b * a.Hq + kv * r + hh) * a.N + last) * D, lane, f);
+#pragma unroll
+        for (int e = 0; e < PL; ++e) qs[e] += f[e];
+    }
+    store_row<PL>(pqs + u * D, lane, qs);
+    const int nch = (g + 15) / 16;
+    const int t16 = lane & 15;
+    // this lane's key of chunk ch: its score s and its da (lanes l and l + 16 both get key l)
+    auto chunk = [&](int ch, float &sv, float &ev) {
+        float val[32];
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+            float k[PL], v[PL];
+            if (ch * 16 + t < g) {
+                load_row<T, PL>(K + (row0 + ch * 16 + t) * D, lane, k);
+                load_row<T, PL>(V + (row0 + ch * 16 + t) * D, lane, v);
+            } else {
+#pragma unroll
+                for (int e = 0; e < PL; ++e) k[e] = v[e] = 0.f;
+            }
+            float ps = 0.f, pe = 0.f;
+#pragma unroll
+            for (int e = 0; e < PL; ++e) {
+                ps = fmaf(qs[e], k[e], ps);
+                pe = fmaf(dkc[e], k[e], fmaf(dvc[e], v[e], pe));
+            }
+            val[t] = c * ps;
+            val[16 + t] = pe;
+        }
+        const float x = warp_transpose_sum32(val, lane);  // lane t: s of key t; lane 16 + t: its da
+        sv = __shfl_sync(kFull, x, t16);
+        ev = __shfl_sync(kFull, x, 16 + t16);
+    };
+    // pass 1: max, normaliser and sum_u exp(s_u - max) da_u, online over the chunks
+    float mx = -INFINITY, den = 0.f, num = 0.f, s_keep = 0.f, e_keep = 0.f;
+    for (int ch = 0; ch < nch; ++ch) {
+        float sv, ev;
+        chunk(ch, sv, ev);
+        const bool valid = ch * 16 + t16 < g;
+        float cm = valid ? sv : -INFINITY;
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) cm = fmaxf(cm, __shfl_xor_sync(kFull, cm, o));
+        const float mn = fmaxf(mx, cm);
+        const float pk = valid ? expf(sv - mn) : 0.f;
+        float ps = pk, pe = pk * ev;
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) {
+            ps += __shfl_xor_sync(kFull, ps, o);
+            pe += __shfl_xor_sync(kFull, pe, o);
+        }
+        const float f = expf(mx - mn);
+        den = den * f + ps;
+        num = num * f + pe;
+        mx = mn;
+        s_keep = sv;
+        e_keep = ev;
+    }
+    const float sad = num / den;  // sum_u a_u da_u
+    // pass 2: the per-token scalars and the query-side term
+    float dqs[PL];
+#pragma unroll
+    for (int e = 0; e < PL; ++e) dqs[e] = 0.f;
+    for (int ch = 0; ch < nch; ++ch) {
+        float sv = s_keep, ev = e_keep;
+        if (nch > 1) chunk(ch, sv, ev);
+        const int key = ch * 16 + t16;
+        const bool valid = key < g;
+        const float at = valid ? expf(sv - mx) / den : 0.f;
+        const float cds = c * at * (ev - sad);
+        if (lane < 16 && valid) {
+            pa[row0 + key] = at;
+            pcds[row0 + key] = cds;
+        }
+        const int nt = min(16, g - ch * 16);
+        for (int t = 0; t < nt; ++t) {
+            const float w = __shfl_sync(kFull, cds, t);
+            float k[PL];
+            load_row<T, PL>(K + (row0 + ch * 16 + t) * D, lane, k);
+#pragma unroll
+            for (int e = 0; e < PL; ++e) dqs[e] = fmaf(w, k[e], dqs[e]);
+        }
+    }
+    for (int hh = 0; hh < r; ++hh) add_row<PL>(dQ + ((b * a.Hq + kv * r + hh) * a.N + last) * D, lane, dqs);
+}
+
+// Workspace layout (fp32, every part 256-byte aligned): D [B*Hq*N], dKc and dVc
+// [B*Hkv*G*d] each, then for the folded pooling backward a and cds [B*Hkv*N] each and
+// qs [B*Hkv*G*d].
+struct BwdWorkspace {
+    float *Dbuf, *dKc, *dVc, *pa, *pcds, *pqs;
+};
+inline int64_t round64(int64_t n) { return (n + 63) / 64 * 64; }
+inline int64_t bwd_workspace_floats(const Shape &s, float *base, BwdWorkspace *w) {
+    const int64_t G = s.N / s.g;
+    const int64_t nD = round64(static_cast<int64_t>(s.B) * s.Hq * s.N);
+    const int64_t nc = round64(static_cast<int64_t>(s.B) * s.Hkv * G * s.d);
+    const int64_t nt = round64(static_cast<int64_t>(s.B) * s.Hkv * s.N);
+    if (w != nullptr) {
+        w->Dbuf = base;
+        w->dKc = w->Dbuf + nD;
+        w->dVc = w->dKc + nc;
+        w->pa = w->dVc + nc;
+        w->pcds = w->pa + nt;
+        w->pqs = w->pcds + nt;
+    }
+    return nD + 3 * nc + 2 * nt;
+}
+
 template <typename T, int D>
 cudaError_t run(const void *Q, const void *K, const void *V, const void *Kc, const void *Vc, const void *O,
                 const float *LSE, const void *dO, float *dQ, float *dK, float *dV, const Shape &s, float *ws,
                 int32_t *status, cudaStream_t stream) {
     BwdArgs a{s.B, s.Hq, s.Hkv, s.N, s.g, s.w, s.window_mode, s.pool_mode, s.scale};
     const int64_t G = s.N / s.g;
-    float *Dbuf = ws;
-    float *dKc = Dbuf + ((static_cast<int64_t>(s.B) * s.Hq * s.N + 63) / 64) * 64;
-    float *dVc = dKc + static_cast<int64_t>(s.B) * s.Hkv * G * D;
+    BwdWorkspace W;
+    bwd_workspace_floats(s, ws, &W);
+    float *const Dbuf = W.Dbuf, *const dKc = W.dKc, *const dVc = W.dVc;
     auto blocks = [](int64_t rows) { return static_cast<unsigned>((rows + 3) / 4); };
     const T *q = static_cast<const T *>(Q), *k = static_cast<const T *>(K), *v = static_cast<const T *>(V);
     const T *kc = static_cast<const T *>(Kc), *vc = static_cast<const T *>(Vc);
     const T *o = static_cast<const T *>(O), *dout = static_cast<const T *>(dO);
-    if (std::is_same<T, __nv_bfloat16>::value && D == 128) {
+    if constexpr (std::is_same<T, __nv_bfloat16>::value && D == 128) {
+        if (s.pool_mode == 0 || s.pool_mode == 1) {
+            // cores first, then the raw tokens with the pooling backward folded into their rows
+            cudaError_t e = launch_attn_bwd_tc(Q, K, V, Kc, Vc, O, LSE, dO, dQ, dK, dV, Dbuf, dKc, dVc, s, status, 1,
+                                               BwdPoolFuse{0, nullptr, nullptr, nullptr}, stream);
+            if (e != cudaSuccess) return e;
+            BwdPoolFuse pf{1, nullptr, nullptr, nullptr};
+            if (s.pool_mode == 0) {
+                bwd_pool_scalars_kernel<T, D><<<blocks(static_cast<int64_t>(s.B) * s.Hkv * G), 128, 0, stream>>>(
+                    q, k, v, dKc, dVc, dQ, W.pa, W.pcds, W.pqs, a);
+                if ((e = cudaGetLastError()) != cudaSuccess) return e;
+                pf = BwdPoolFuse{2, W.pa, W.pcds, W.pqs};
+            }
+            return launch_attn_bwd_tc(Q, K, V, Kc, Vc, O, LSE, dO, dQ, dK, dV, Dbuf, dKc, dVc, s, status, 2, pf,
+                                      stream);
+        }
         const cudaError_t e = launch_attn_bwd_tc(Q, K, V, Kc, Vc, O, LSE, dO, dQ, dK, dV, Dbuf, dKc, dVc, s, status,
-                                                 stream);
+                                                 0, BwdPoolFuse{0, nullptr, nullptr, nullptr}, stream);
         if (e != cudaSuccess) return e;
     } else {
         bwd_dq_kernel<T, D><<<blocks(static_cast<int64_t>(s.B) * s.Hq * s.N), 128, 0, stream>>>(
@@ -443,10 +622,7 @@ cudaError_t run(const void *Q, const void *K, const void *V, const void *Kc, con
 
 }  // namespace
 
-uint64_t prefill_bwd_workspace_bytes(const Shape &s) {
-    const uint64_t rows = ((static_cast<uint64_t>(s.B) * s.Hq * s.N + 63) / 64) * 64;
-    return 4ull * (rows + 2ull * s.B * s.Hkv * (s.N / s.g) * s.d);
-}
+uint64_t prefill_bwd_workspace_bytes(const Shape &s) { return 4ull * bwd_workspace_floats(s, nullptr, nullptr); }
 
 cudaError_t launch_prefill_bwd(int dtype, const void *Q, const void *K, const void *V, const void *Kc, const void *Vc,
                                const void *O, const float *LSE, const void *dO, float *dQ, float *dK, float *dV,

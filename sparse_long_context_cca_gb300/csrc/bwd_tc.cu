@@ -62,6 +62,10 @@ struct BwdTcParams {
     const float *LSE;
     const __nv_bfloat16 *O, *dO;
     float *Dbuf;  // written by the dq kernel, read by the dkv kernel
+    int tile0;    // first key tile of this dkv launch (core tiles come first)
+    // pooling backward folded into the raw-token tiles' epilogue (BwdPoolFuse)
+    int pool_fuse;
+    const float *pool_a, *pool_cds, *pool_qs, *pool_dkc, *pool_dvc;
     int32_t *status;
     unsigned long long wait_limit_ns;
     int skip_loads;  // test hook: issue no copies, so the first wait runs out
@@ -103,6 +107,41 @@ __device__ __forceinline__ void stage_f32_rows(uint32_t tmem_row_addr, int tcol,
             ptx::st_shared_v4(rbase + ((q ^ (row & 7)) << 4), __uint_as_float(v[4 * q]) * scale,
                               __uint_as_float(v[4 * q + 1]) * scale, __uint_as_float(v[4 * q + 2]) * scale,
                               __uint_as_float(v[4 * q + 3]) * scale);
+    }
+}
+// As stage_f32_rows, adding xs * x + ys * y (x, y: fp32 rows of 128 in global memory;
+// y may be nullptr) to every element: the pooling backward's share of a raw token's
+// gradient.
+__device__ __forceinline__ void stage_f32_rows_plus(uint32_t tmem_row_addr, int tcol, int ch, int row, float scale,
+                                                    bool zero, uint32_t stage, const float *x, float xs,
+                                                    const float *y, float ys) {
+#pragma unroll 1
+    for (int j = 0; j < 2; ++j) {
+        const int c = 2 * ch + j;  // 32-column box
+        uint32_t v[32];
+        if (!zero) {
+            ptx::tmem_ld32(tmem_row_addr + tcol + c * 32, v);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) v[k] = 0u;
+        }
+        float4 xv[8], yv[8];
+        const float4 *x4 = reinterpret_cast<const float4 *>(x + c * 32);
+        const float4 *y4 = reinterpret_cast<const float4 *>(y + c * 32);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            xv[q] = x4[q];
+            yv[q] = y != nullptr ? y4[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        if (!zero) ptx::tmem_wait_ld(v);
+        const uint32_t rbase = stage + c * (BT * 128) + row * 128;
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            ptx::st_shared_v4(rbase + ((q ^ (row & 7)) << 4),
+                              fmaf(ys, yv[q].x, fmaf(xs, xv[q].x, __uint_as_float(v[4 * q]) * scale)),
+                              fmaf(ys, yv[q].y, fmaf(xs, xv[q].y, __uint_as_float(v[4 * q + 1]) * scale)),
+                              fmaf(ys, yv[q].z, fmaf(xs, xv[q].z, __uint_as_float(v[4 * q + 2]) * scale)),
+                              fmaf(ys, yv[q].w, fmaf(xs, xv[q].w, __uint_as_float(v[4 * q + 3]) * scale)));
     }
 }
 
@@ -475,7 +514,7 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
     const int BK = p.B * p.Hkv;
     const int n_core_t = (p.G + BT - 1) / BT;
     // core tiles first (they are seen by the most query rows), then raw-token tiles
-    const int idx = static_cast<int>(blockIdx.x / BK);
+    const int idx = p.tile0 + static_cast<int>(blockIdx.x / BK);
     const int bk = static_cast<int>(blockIdx.x % BK);
     const bool core = idx < n_core_t;
     const int y0 = core ? idx * BT : (idx - n_core_t) * BT;
@@ -643,10 +682,29 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
         if (n_it > 0) slot_f[e] = slot_value(0);
         ptx::named_bar_sync(1, 256);
         bool ok = true;
+        // the pooling backward's terms for this key's row (raw tiles, folded pooling backward)
+        const bool fuse = !core && p.pool_fuse != 0;
+        const int mm = m < p.N ? m : p.N - 1;  // rows past N only take part in collective loads
+        const int64_t uj = static_cast<int64_t>(bk) * p.G + mm / p.g;
+        float am = 0.f, cm = 0.f;
+        if (fuse) {
+            const int64_t um = static_cast<int64_t>(bk) * p.N + mm;
+            am = p.pool_fuse == 1 ? 1.f / p.g : p.pool_a[um];
+            cm = p.pool_fuse == 1 ? 0.f : p.pool_cds[um];
+        }
         // Every element-wise thread runs every iteration and both named barriers of it, so
         // that a time-out (which skips the work) cannot leave a barrier short of threads.
         for (int it = 0; it < n_it; ++it) {
             const float v_next = it + 1 < n_it ? slot_value(it + 1) : 0.f;
+            if (fuse && it == n_it - 1) {
+                // bring this row's half of dKc_j, dVc_j (and qsum_j) into L1 for the epilogue
+#pragma unroll
+                for (int l = 0; l < 2; ++l) {
+                    ptx::prefetch_l1(p.pool_dkc + uj * HD + h0 + 32 * l);
+                    ptx::prefetch_l1(p.pool_dvc + uj * HD + h0 + 32 * l);
+                    if (p.pool_fuse == 2) ptx::prefetch_l1(p.pool_qs + uj * HD + h0 + 32 * l);
+                }
+            }
             if (ok) ok = __all_sync(0xffffffffu, ptx::wait_bounded(bar(DB_SFULL), it & 1, abort_flag, lim));
             uint32_t pa[32], pb[32];
             if (ok) {
@@ -751,8 +809,18 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
             // dK * tau and dV through shared memory (the Q and dO stages, idle now) to tiled
             // stores; a tile no query row sees stores zeros
             ptx::tc_fence_after();
-            stage_f32_rows(tmem + lane_addr, T_DK, ch, row, p.tau, n_it == 0, base + DKV_OFF_Q);
-            stage_f32_rows(tmem + lane_addr, T_DV, ch, row, 1.f, n_it == 0, base + DKV_OFF_Q + 2 * TILE_BYTES);
+            if (fuse) {
+                // + the pooling backward: a_m dKc_j + (tau/r) ds_m qsum_j and a_m dVc_j, j = m / g
+                // (the store drops rows past N)
+                const float *qs = p.pool_fuse == 1 ? nullptr : p.pool_qs + uj * HD;
+                stage_f32_rows_plus(tmem + lane_addr, T_DK, ch, row, p.tau, n_it == 0, base + DKV_OFF_Q,
+                                    p.pool_dkc + uj * HD, am, qs, cm);
+                stage_f32_rows_plus(tmem + lane_addr, T_DV, ch, row, 1.f, n_it == 0,
+                                    base + DKV_OFF_Q + 2 * TILE_BYTES, p.pool_dvc + uj * HD, am, nullptr, 0.f);
+            } else {
+                stage_f32_rows(tmem + lane_addr, T_DK, ch, row, p.tau, n_it == 0, base + DKV_OFF_Q);
+                stage_f32_rows(tmem + lane_addr, T_DV, ch, row, 1.f, n_it == 0, base + DKV_OFF_Q + 2 * TILE_BYTES);
+            }
             ptx::fence_proxy_async_smem();
         }
     }
@@ -780,8 +848,8 @@ struct Attr {
 
 cudaError_t launch_attn_bwd_tc(const void *Q, const void *K, const void *V, const void *Kc, const void *Vc,
                                const void *O, const float *LSE, const void *dO, float *dQ, float *dK, float *dV,
-                               float *Dbuf, float *dKc, float *dVc, const Shape &s, int32_t *status,
-                               cudaStream_t stream) {
+                               float *Dbuf, float *dKc, float *dVc, const Shape &s, int32_t *status, int part,
+                               const BwdPoolFuse &pf, cudaStream_t stream) {
     EncodeTiledFn enc = get_encoder();
     if (enc == nullptr) return cudaErrorNotSupported;
     static std::mutex mu;
@@ -825,15 +893,34 @@ cudaError_t launch_attn_bwd_tc(const void *Q, const void *K, const void *V, cons
     p.O = static_cast<const __nv_bfloat16 *>(O);
     p.dO = static_cast<const __nv_bfloat16 *>(dO);
     p.Dbuf = Dbuf;
+    p.tile0 = 0;
+    p.pool_fuse = 0;
+    p.pool_a = p.pool_cds = p.pool_qs = nullptr;
+    p.pool_dkc = dKc;
+    p.pool_dvc = dVc;
     p.status = status;
     p.wait_limit_ns = g_wait_limit_ns;
     p.skip_loads = g_skip_q_load;
-    const unsigned n_qt = static_cast<unsigned>((s.N + BT - 1) / BT);
-    bwd_dq_tc_kernel<<<n_qt * static_cast<unsigned>(qh), DQ_THREADS, DQ_SMEM, stream>>>(mQ, mdO, mK, mV, mKc, mVc,
-                                                                                        mdQ, p);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    const unsigned n_kt = static_cast<unsigned>((G + BT - 1) / BT + (s.N + BT - 1) / BT);
+    if (part != 2) {
+        const unsigned n_qt = static_cast<unsigned>((s.N + BT - 1) / BT);
+        bwd_dq_tc_kernel<<<n_qt * static_cast<unsigned>(qh), DQ_THREADS, DQ_SMEM, stream>>>(mQ, mdO, mK, mV, mKc,
+                                                                                            mVc, mdQ, p);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    const unsigned n_ct = static_cast<unsigned>((G + BT - 1) / BT), n_rt = static_cast<unsigned>((s.N + BT - 1) / BT);
+    unsigned n_kt = n_ct + n_rt;
+    if (part == 1) {
+        n_kt = n_ct;
+    } else if (part == 2) {
+        p.tile0 = static_cast<int>(n_ct);
+        n_kt = n_rt;
+        p.pool_fuse = pf.mode;
+        p.pool_a = pf.a;
+        p.pool_cds = pf.cds;
+        p.pool_qs = pf.qs;
+    }
+    if (n_kt == 0) return cudaSuccess;
     bwd_dkv_tc_kernel<<<n_kt * static_cast<unsigned>(kh), DKV_THREADS, DKV_SMEM, stream>>>(
         mQ, mdO, mK, mV, mKc, mVc, mdK, mdV, mdKc, mdVc, p);
     return cudaGetLastError();

@@ -47,12 +47,22 @@ uint64_t prefill_bwd_workspace_bytes(const Shape &s);
 cudaError_t launch_prefill_bwd(int dtype, const void *Q, const void *K, const void *V, const void *Kc, const void *Vc,
                                const void *O, const float *LSE, const void *dO, float *dQ, float *dK, float *dV,
                                const Shape &s, float *ws, int32_t *status, cudaStream_t stream);
-// Tensor-core attention backward (bf16, d = 128): writes dQ (all rows), D = dO.O into Dbuf,
-// dK/dV of the raw tokens and dKc/dVc of the cores; the pooling backward is not included.
+// The pooling backward's share of a raw token's gradient, added by the dK/dV kernel
+// while it writes the token's row: dK_t += a_t dKc_j + cds_t qs_j, dV_t += a_t dVc_j
+// (j the token's group).  mode 0: nothing added; 1: mean pooling (a_t = 1/g, cds_t = 0,
+// no arrays); 2: a, cds ([B, Hkv, N]) and qs ([B, Hkv, N/g, 128], fp32) as given.
+struct BwdPoolFuse {
+    int mode;
+    const float *a, *cds, *qs;
+};
+// Tensor-core attention backward (bf16, d = 128).  part 0: dQ (all rows), D = dO.O into
+// Dbuf, dK/dV of the raw tokens and dKc/dVc of the cores, no pooling backward; part 1:
+// dQ, D and the cores' dKc/dVc only; part 2: the raw tokens' dK/dV only, with the
+// pooling backward pf folded in (dKc/dVc already complete).
 cudaError_t launch_attn_bwd_tc(const void *Q, const void *K, const void *V, const void *Kc, const void *Vc,
                                const void *O, const float *LSE, const void *dO, float *dQ, float *dK, float *dV,
-                               float *Dbuf, float *dKc, float *dVc, const Shape &s, int32_t *status,
-                               cudaStream_t stream);
+                               float *Dbuf, float *dKc, float *dVc, const Shape &s, int32_t *status, int part,
+                               const BwdPoolFuse &pf, cudaStream_t stream);
 
 // Prefill on host buffers, pipelined over slices of (batch, KV head) pairs (host_pipeline.cu).
 uint64_t prefill_host_workspace_bytes(const Shape &s, int dtype);

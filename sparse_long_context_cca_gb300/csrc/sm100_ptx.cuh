@@ -64,6 +64,9 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
 }
 
 // ---------------------------------------------------------------- TMA
+__device__ __forceinline__ void prefetch_l1(const void *addr) {
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(reinterpret_cast<uint64_t>(addr)));
+}
 __device__ __forceinline__ void prefetch_tmap(const void *tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }

@@ -30,6 +30,12 @@ CASES = [
     (wl(1, 2, 2, 384, 128, 16, 300), 2, 0),
     # window covers the whole sequence: no core is ever visible
     (wl(1, 2, 2, 256, 128, 16, 512), 0, 0),
+    # the pooling backward folded into the raw-token rows: groups that straddle
+    # 128-key tiles, groups longer than a tile, ragged N with GQA
+    (wl(1, 2, 2, 768, 128, 24, 100), 0, 0),
+    (wl(1, 4, 2, 768, 128, 192, 200), 0, 0),
+    (wl(1, 2, 1, 1000, 128, 40, 150), 1, 1),
+    (wl(1, 8, 2, 520, 128, 8, 60), 0, 1),
 ]
 
 
