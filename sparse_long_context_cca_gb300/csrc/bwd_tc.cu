@@ -533,11 +533,14 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
         r_lo = y0;
         r_hi = static_cast<int>(last < p.N - 1 ? last : p.N - 1);
     }
-    const int qt_lo = r_lo / BT;
-    const int nq = r_lo <= r_hi ? r_hi / BT - qt_lo + 1 : 0;
-    const int n_it = nq * r;  // (head, query tile) pairs, head-major
-    auto bh_of = [&](int it) { return b * p.Hq + kv * r + it / nq; };
-    auto i0_of = [&](int it) { return (qt_lo + it % nq) * BT; };
+    const int qt_hi = r_hi / BT;
+    const int nq = r_lo <= r_hi ? qt_hi - r_lo / BT + 1 : 0;
+    // (query tile, head) pairs from the last query tile down, heads fastest: every CTA of a
+    // KV head (their ranges all end at the last tile, or overlap their neighbours') then
+    // reads the same Q/dO tiles at about the same time, so they come from L2
+    const int n_it = nq * r;
+    auto bh_of = [&](int it) { return b * p.Hq + kv * r + it % r; };
+    auto i0_of = [&](int it) { return (qt_hi - it / r) * BT; };
 
     if (t == 0) {
         // the first use of each descriptor would otherwise wait for its fetch
