@@ -379,10 +379,15 @@ def decode_bench(wl, dev, stream, iters, peaks):
     ws = torch.empty(api.decode_workspace_size(wl.B, wl.Hq, wl.Hkv, wl.N, wl.d, wl.g, wl.w, q.dtype),
                      dtype=torch.uint8, device=dev)
     # The caches of one step (49 MB at 32K) fit in the 129 MB L2, so every timed step
-    # starts from a flushed L2: a 256 MB write on the same stream just before it.  Each step
-    # has its own pair of events; the flush keeps the GPU busy while the host enqueues the
-    # step, so the pair measures the step on the device, not the host's launch overhead.
+    # starts from a flushed L2: a 256 MB write on the same stream just before it, then a
+    # read of another 256 MB, so that the L2 holds clean lines (as between two decode steps
+    # of a model, which mostly read other layers' caches and weights) and the step's reads
+    # do not also pay for writing back the flush's dirty lines.  Each step has its own pair
+    # of events; the flush keeps the GPU busy while the host enqueues the step, so the pair
+    # measures the step on the device, not the host's launch overhead.
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    sweep = torch.ones(64 << 20, dtype=torch.float32, device=dev)
+    sink = torch.empty((), dtype=torch.float32, device=dev)
     for _ in range(5):
         api.cca_decode_fwd(q, K, V, Kc, Vc, pos, wl.g, wl.w, O, LSE, ws, stream=stream)
     torch.cuda.synchronize()
@@ -390,13 +395,14 @@ def decode_bench(wl, dev, stream, iters, peaks):
     with torch.cuda.stream(stream):
         for e0, e1 in ev:
             flush.fill_(1)
+            torch.sum(sweep, 0, out=sink)
             e0.record(stream)
             api.cca_decode_fwd(q, K, V, Kc, Vc, pos, wl.g, wl.w, O, LSE, ws, stream=stream)
             e1.record(stream)
     torch.cuda.synchronize()
     step_us = sorted(e0.elapsed_time(e1) * 1e3 for e0, e1 in ev)
     us = sum(step_us) / len(step_us)
-    del flush
+    del flush, sweep, sink
     lo = max(0, pos - wl.w + 1)
     keys = lo // wl.g + (pos - lo + 1)
     e = 2 if wl.dtype == "bf16" else 4
@@ -405,7 +411,8 @@ def decode_bench(wl, dev, stream, iters, peaks):
     torch.cuda.empty_cache()
     return {"what": f"one decode step at position {pos} ({keys} visible keys per head), split-KV + combine",
             "us_per_step": us, "us_median": step_us[len(step_us) // 2], "steps": iters,
-            "l2": "flushed before every step (256 MB write); per-step CUDA events",
+            "l2": "flushed before every step (256 MB write, then a 256 MB read so the L2 holds clean lines); "
+                  "per-step CUDA events",
             "tokens_per_s": wl.B / (us * 1e-6),
             "gbs": nbytes / (us * 1e-6) / 1e9, "hbm_frac": nbytes / (us * 1e-6) / 1e9 / peaks["hbm_gbs"],
             "algorithmic_bytes": nbytes, "kernel_launches_per_step": 2}

@@ -21,7 +21,9 @@ def wl(B, Hq, Hkv, N, d, g, w, dtype="bf16", seed=11):
 
 
 CASES = [wl(1, 4, 4, 4096, 128, 16, 1024), wl(2, 8, 2, 2048, 128, 16, 256), wl(1, 4, 1, 3000, 128, 8, 500),
-         wl(1, 2, 2, 1024, 64, 4, 100), wl(1, 4, 2, 1024, 128, 16, 200, "f32"), wl(1, 2, 2, 512, 64, 32, 64, "f32")]
+         wl(1, 2, 2, 1024, 64, 4, 100), wl(1, 4, 2, 1024, 128, 16, 200, "f32"), wl(1, 2, 2, 512, 64, 32, 64, "f32"),
+         # eight query heads per KV head (bf16 d = 128 and d = 64, f32 d = 128)
+         wl(1, 8, 1, 2048, 128, 16, 300), wl(2, 16, 2, 1024, 64, 8, 200), wl(1, 8, 1, 768, 128, 16, 100, "f32")]
 
 
 @pytest.mark.parametrize("w", CASES, ids=lambda w: w.name)
