@@ -63,6 +63,7 @@ struct BwdTcParams {
     const __nv_bfloat16 *O, *dO;
     float *Dbuf;  // written by the dq kernel, read by the dkv kernel
     int tile0;    // first key tile of this dkv launch (core tiles come first)
+    int core_chunk;  // > 0: core tiles in items of this many query tiles, summed into dKc/dVc
     // pooling backward folded into the raw-token tiles' epilogue (BwdPoolFuse)
     int pool_fuse;
     const float *pool_a, *pool_cds, *pool_qs, *pool_dkc, *pool_dvc;
@@ -145,11 +146,15 @@ __device__ __forceinline__ void stage_f32_rows_plus(uint32_t tmem_row_addr, int 
     }
 }
 
-// Thread 0 stores a staged 128 x 128 fp32 tile (four boxes) at rows [y, y + 128) of head z;
-// rows past the tensor's end are not written.
-__device__ __forceinline__ void store_tile_f32(const CUtensorMap *map, uint32_t stage, int y, int z) {
+// Thread 0 stores a staged 128 x 128 fp32 tile (four boxes) at rows [y, y + 128) of head z
+// (or adds it to what is there); rows past the tensor's end are not written.
+__device__ __forceinline__ void store_tile_f32(const CUtensorMap *map, uint32_t stage, int y, int z,
+                                               bool add = false) {
 #pragma unroll
-    for (int c = 0; c < 4; ++c) ptx::tma_store_3d(map, stage + c * (BT * 128), c * 32, y, z);
+    for (int c = 0; c < 4; ++c) {
+        if (add) ptx::tma_reduce_add_3d(map, stage + c * (BT * 128), c * 32, y, z);
+        else ptx::tma_store_3d(map, stage + c * (BT * 128), c * 32, y, z);
+    }
     ptx::bulk_commit_group();
 }
 
@@ -478,6 +483,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
 // complete in issue order, so S^T(x+1) and dP^T(x+1), issued after dV(x) and dK(x),
 // never overwrite what those read.
 constexpr int DKV_THREADS = 320;
+constexpr int BWD_CORE_CHUNK = 64;  // query tiles per core-tile item
 constexpr int DKV_QST = 3, DKV_OST = 2;
 constexpr uint32_t DKV_OFF_Q = 2 * TILE_BYTES;  // after K, V
 constexpr uint32_t DKV_OFF_O = DKV_OFF_Q + DKV_QST * TILE_BYTES;
@@ -513,9 +519,24 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     const int BK = p.B * p.Hkv;
     const int n_core_t = (p.G + BT - 1) / BT;
-    // core tiles first (they are seen by the most query rows), then raw-token tiles
-    const int idx = p.tile0 + static_cast<int>(blockIdx.x / BK);
-    const int bk = static_cast<int>(blockIdx.x % BK);
+    const int n_qt = (p.N + BT - 1) / BT;
+    // core tiles first (they are seen by the most query rows), then raw-token tiles.  With
+    // core_chunk > 0 (core tiles only) an item is one core tile over one chunk of query
+    // tiles, [c * core_chunk, (c + 1) * core_chunk); items run top chunk first, each chunk
+    // head by head, a head's core tiles side by side, so the CTAs that run together stream
+    // the same Q/dO tiles.
+    int idx, bk, chunk = -1;
+    if (p.core_chunk > 0) {
+        const int per_chunk = BK * n_core_t;
+        const int n_chunks = (n_qt + p.core_chunk - 1) / p.core_chunk;
+        chunk = n_chunks - 1 - static_cast<int>(blockIdx.x / per_chunk);
+        const int rem = static_cast<int>(blockIdx.x % per_chunk);
+        bk = rem / n_core_t;
+        idx = rem % n_core_t;
+    } else {
+        idx = p.tile0 + static_cast<int>(blockIdx.x / BK);
+        bk = static_cast<int>(blockIdx.x % BK);
+    }
     const bool core = idx < n_core_t;
     const int y0 = core ? idx * BT : (idx - n_core_t) * BT;
     const int n_keys = core ? p.G : p.N;
@@ -533,8 +554,14 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
         r_lo = y0;
         r_hi = static_cast<int>(last < p.N - 1 ? last : p.N - 1);
     }
-    const int qt_hi = r_hi / BT;
-    const int nq = r_lo <= r_hi ? qt_hi - r_lo / BT + 1 : 0;
+    int qt_hi = r_hi / BT, qt_lo = r_lo / BT;
+    if (chunk >= 0) {
+        // this item's part of the range; an item with nothing to do leaves before any setup
+        qt_hi = min(qt_hi, (chunk + 1) * p.core_chunk - 1);
+        qt_lo = max(qt_lo, chunk * p.core_chunk);
+        if (r_lo > r_hi || qt_lo > qt_hi) return;
+    }
+    const int nq = r_lo <= r_hi ? qt_hi - qt_lo + 1 : 0;
     // (query tile, head) pairs from the last query tile down, heads fastest: every CTA of a
     // KV head (their ranges all end at the last tile, or overlap their neighbours') then
     // reads the same Q/dO tiles at about the same time, so they come from L2
@@ -832,8 +859,9 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
     if (*abort_flag) {
         if (t == 0 && p.status != nullptr) atomicCAS(p.status, 0, STATUS_TIMEOUT);
     } else if (t == 0) {
-        store_tile_f32(core ? &tmdKc : &tmdK, base + DKV_OFF_Q, y0, bk);
-        store_tile_f32(core ? &tmdVc : &tmdV, base + DKV_OFF_Q + 2 * TILE_BYTES, y0, bk);
+        // a chunked core item adds its share to dKc/dVc (zeroed before the launch)
+        store_tile_f32(core ? &tmdKc : &tmdK, base + DKV_OFF_Q, y0, bk, chunk >= 0);
+        store_tile_f32(core ? &tmdVc : &tmdV, base + DKV_OFF_Q + 2 * TILE_BYTES, y0, bk, chunk >= 0);
         ptx::bulk_wait_read();
     }
     if (warp == 0) {
@@ -897,6 +925,7 @@ cudaError_t launch_attn_bwd_tc(const void *Q, const void *K, const void *V, cons
     p.dO = static_cast<const __nv_bfloat16 *>(dO);
     p.Dbuf = Dbuf;
     p.tile0 = 0;
+    p.core_chunk = 0;
     p.pool_fuse = 0;
     p.pool_a = p.pool_cds = p.pool_qs = nullptr;
     p.pool_dkc = dKc;
@@ -913,8 +942,19 @@ cudaError_t launch_attn_bwd_tc(const void *Q, const void *K, const void *V, cons
     }
     const unsigned n_ct = static_cast<unsigned>((G + BT - 1) / BT), n_rt = static_cast<unsigned>((s.N + BT - 1) / BT);
     unsigned n_kt = n_ct + n_rt;
+    unsigned grid = 0;
     if (part == 1) {
+        // core tiles in chunks of query tiles, added into zeroed dKc/dVc
+        const int n_qt = static_cast<int>((s.N + BT - 1) / BT);
+        p.core_chunk = BWD_CORE_CHUNK;
+        const unsigned n_chunks = static_cast<unsigned>((n_qt + p.core_chunk - 1) / p.core_chunk);
+        const size_t core_bytes = static_cast<size_t>(G) * static_cast<size_t>(kh) * 128 * sizeof(float);
+        if (n_ct > 0) {
+            if ((e = cudaMemsetAsync(dKc, 0, core_bytes, stream)) != cudaSuccess) return e;
+            if ((e = cudaMemsetAsync(dVc, 0, core_bytes, stream)) != cudaSuccess) return e;
+        }
         n_kt = n_ct;
+        grid = n_chunks * n_ct * static_cast<unsigned>(kh);
     } else if (part == 2) {
         p.tile0 = static_cast<int>(n_ct);
         n_kt = n_rt;
@@ -924,7 +964,8 @@ cudaError_t launch_attn_bwd_tc(const void *Q, const void *K, const void *V, cons
         p.pool_qs = pf.qs;
     }
     if (n_kt == 0) return cudaSuccess;
-    bwd_dkv_tc_kernel<<<n_kt * static_cast<unsigned>(kh), DKV_THREADS, DKV_SMEM, stream>>>(
+    if (grid == 0) grid = n_kt * static_cast<unsigned>(kh);
+    bwd_dkv_tc_kernel<<<grid, DKV_THREADS, DKV_SMEM, stream>>>(
         mQ, mdO, mK, mV, mKc, mVc, mdK, mdV, mdKc, mdVc, p);
     return cudaGetLastError();
 }
