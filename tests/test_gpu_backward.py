@@ -59,3 +59,27 @@ def test_backward_parity(w, pool_mode, window_mode):
         else:
             assert err.max() <= 2e-2 * scale, (name, err.max(), scale)
             assert err.mean() <= 2e-3 * scale, (name, err.mean(), scale)
+
+
+@pytest.mark.parametrize("w,pool_mode", [(wl(1, 2, 1, 8448, 128, 16, 256, seed=41), 0),
+                                         (wl(1, 1, 1, 8448, 128, 24, 300, seed=42), 1)],
+                         ids=lambda x: x.name if hasattr(x, "name") else str(x))
+def test_backward_core_tiles_over_several_query_chunks(w, pool_mode):
+    """The tensor-core backward splits each core tile's query range into chunks of 64 query
+    tiles and adds the chunks' dKc/dVc shares together; at N = 8448 (66 query tiles) the
+    first core tiles are seen from both chunks, the last core tile is ragged, and r = 2 in
+    the first case."""
+    Q, K, V = make_qkv(w, "cuda")
+    gen = torch.Generator(device="cuda").manual_seed(w.seed + 100)
+    dO = torch.randn(Q.shape, generator=gen, device="cuda").to(Q.dtype)
+    O, LSE, Kc, Vc = api.cca_prefill(Q, K, V, w.g, w.w, pool_mode=pool_mode)
+    dQ, dK, dV = api.cca_prefill_bwd(Q, K, V, Kc, Vc, O, LSE, dO, w.g, w.w, pool_mode=pool_mode)
+    torch.cuda.synchronize()
+    rQ, rK, rV = prefill_grads(Q, K, V, dO, w.g, w.w, pool_mode=pool_mode)
+    for name, got, ref in (("dQ", dQ, rQ), ("dK", dK, rK), ("dV", dV, rV)):
+        g = got.double().cpu().numpy()
+        assert np.isfinite(g).all(), name
+        err = np.abs(g - ref)
+        scale = np.abs(ref).max()
+        assert err.max() <= 2e-2 * scale, (name, err.max(), scale)
+        assert err.mean() <= 2e-3 * scale, (name, err.mean(), scale)
