@@ -103,7 +103,10 @@ __device__ __forceinline__ uint4 lds16(uint32_t addr) {
     return v;
 }
 
-template <typename T, int D>
+// HM4: the instantiation for pool_mode 3 with four query heads per KV head and one chunk per
+// group, which takes the specialised scoring path below (kept out of the other
+// instantiations, whose registers it would otherwise raise).
+template <typename T, int D, bool HM4>
 __global__ void __launch_bounds__(NW_MAX * 32) pool_kernel(const T *__restrict__ Q, const T *__restrict__ K,
                                                        const T *__restrict__ V, T *__restrict__ Kc,
                                                        T *__restrict__ Vc, const PoolArgs a) {
@@ -228,7 +231,81 @@ __global__ void __launch_bounds__(NW_MAX * 32) pool_kernel(const T *__restrict__
                 kr[it] = vr[it] = make_uint4(0, 0, 0, 0);
             }
         }
-        if (a.headmean) {
+        bool scored = false;  // the chunk was taken by a specialised path below
+        if constexpr (HM4 && PASSES == 8 && LPR == 16) {
+            if (a.headmean && a.npass == 1 && a.r == 4) {
+                scored = true;
+                // pool_mode 3, four query heads, the whole group in this one chunk: all 32
+                // partial dot products (head hh, pass it at index 8 hh + it) first, then one
+                // transposed butterfly inside each 16-lane row subgroup (31 -> 30 shuffles
+                // for 32 sums), after which lane j of a subgroup holds the scores of head j/4
+                // for passes 2 (j%4) and 2 (j%4) + 1 and does that head's softmax for them.
+                float val[32];
+#pragma unroll
+                for (int hh = 0; hh < 4; ++hh) {
+                    float qh[E];
+                    VT::unpack(lds16(stage + 2 * a.v_off + hh * ROW_BYTES + cl * 16), qh);
+#pragma unroll
+                    for (int it = 0; it < PASSES; ++it) {
+                        float f[E];
+                        VT::unpack(kr[it], f);
+                        float d = qh[0] * f[0];
+#pragma unroll
+                        for (int e = 1; e < E; ++e) d = fmaf(qh[e], f[e], d);
+                        val[hh * PASSES + it] = d;
+                    }
+                }
+#pragma unroll
+                for (int o = 8, n = 16; o > 0; o >>= 1, n >>= 1) {
+                    const bool up = (lane & o) != 0;
+#pragma unroll
+                    for (int i = 0; i < n; ++i) {
+                        const float keep = up ? val[i + n] : val[i];
+                        const float send = up ? val[i] : val[i + n];
+                        val[i] = keep + __shfl_xor_sync(kFull, send, o);
+                    }
+                }
+                const int j = lane & 15;
+                const int p0 = 2 * (j & 3);  // this lane's passes p0, p0 + 1 of head j / 4
+                const float s0 = p0 * RPI + sub < rows ? val[0] * a.logit_scale : -INFINITY;
+                const float s1 = (p0 + 1) * RPI + sub < rows ? val[1] * a.logit_scale : -INFINITY;
+                // the head's max and sum over its 16 rows: lanes j ^ 1, j ^ 2 and the other subgroup
+                float mx = fmaxf(s0, s1);
+                mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
+                mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+                mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));  // finite: row 0 is valid
+                const float e0 = ptx::ex2(s0 - mx), e1 = ptx::ex2(s1 - mx);
+                float sm = e0 + e1;
+                sm += __shfl_xor_sync(kFull, sm, 1);
+                sm += __shfl_xor_sync(kFull, sm, 2);
+                sm += __shfl_xor_sync(kFull, sm, 16);
+                const float inv = 1.f / (sm * 4.f);
+                // average over the heads: lanes j ^ 4, j ^ 8 hold the same passes of the others
+                float w0 = e0 * inv, w1 = e1 * inv;
+                w0 += __shfl_xor_sync(kFull, w0, 4);
+                w1 += __shfl_xor_sync(kFull, w1, 4);
+                w0 += __shfl_xor_sync(kFull, w0, 8);
+                w1 += __shfl_xor_sync(kFull, w1, 8);
+                // row weights of this subgroup's passes, from lane it / 2 of the subgroup
+                float wgt[PASSES];
+#pragma unroll
+                for (int it = 0; it < PASSES; ++it)
+                    wgt[it] = __shfl_sync(kFull, (it & 1) ? w1 : w0, (lane & 16) + (it >> 1));
+#pragma unroll
+                for (int it = 0; it < PASSES; ++it) {
+                    float fk[E], fv[E];
+                    VT::unpack(kr[it], fk);
+                    VT::unpack(vr[it], fv);
+#pragma unroll
+                    for (int e = 0; e < E; ++e) {
+                        ak[e] = fmaf(wgt[it], fk[e], ak[e]);
+                        av[e] = fmaf(wgt[it], fv[e], av[e]);
+                    }
+                }
+            }
+        }
+        if (scored) {
+        } else if (a.headmean) {
             // pool_mode 3: weight of row t = (1/r) sum_h 2^(s_h,t - m_h) / l_h
             float wgt[PASSES];
 #pragma unroll
@@ -768,17 +845,27 @@ cudaError_t launch_typed(const void *Q, const void *K, const void *V, void *Kc, 
     static std::once_flag once;
     static cudaError_t attr = cudaSuccess;
     std::call_once(once, [] {
-        attr = cudaFuncSetAttribute(pool_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        attr = cudaFuncSetAttribute(pool_kernel<T, D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(SMEM_BUDGET));
+        if (attr == cudaSuccess)
+            attr = cudaFuncSetAttribute(pool_kernel<T, D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        static_cast<int>(SMEM_BUDGET));
     });
     if (attr != cudaSuccess) return attr;
     const int sms = sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
     const int64_t want = (a.n_groups + nw - 1) / nw;
     const unsigned grid = static_cast<unsigned>(want < sms ? want : sms);
-    pool_kernel<T, D><<<grid, nw * 32, smem, stream>>>(static_cast<const T *>(Q), static_cast<const T *>(K),
-                                                       static_cast<const T *>(V), static_cast<T *>(Kc),
-                                                       static_cast<T *>(Vc), a);
+    const bool hm4 = a.headmean && a.npass == 1 && a.r == 4;
+    if (hm4)
+        pool_kernel<T, D, true><<<grid, nw * 32, smem, stream>>>(static_cast<const T *>(Q), static_cast<const T *>(K),
+                                                                 static_cast<const T *>(V), static_cast<T *>(Kc),
+                                                                 static_cast<T *>(Vc), a);
+    else
+        pool_kernel<T, D, false><<<grid, nw * 32, smem, stream>>>(static_cast<const T *>(Q),
+                                                                  static_cast<const T *>(K),
+                                                                  static_cast<const T *>(V), static_cast<T *>(Kc),
+                                                                  static_cast<T *>(Vc), a);
     return cudaGetLastError();
 }
 
