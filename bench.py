@@ -379,14 +379,14 @@ def decode_bench(wl, dev, stream, iters, peaks):
     ws = torch.empty(api.decode_workspace_size(wl.B, wl.Hq, wl.Hkv, wl.N, wl.d, wl.g, wl.w, q.dtype),
                      dtype=torch.uint8, device=dev)
     # The caches of one step (49 MB at 32K) fit in the 129 MB L2, so every timed step
-    # starts from a flushed L2: a 256 MB write on the same stream just before it, then a
-    # read of another 256 MB, so that the L2 holds clean lines (as between two decode steps
+    # starts from a flushed L2: a 512 MB write on the same stream just before it, then a
+    # read of another 512 MB, so that the L2 holds clean lines (as between two decode steps
     # of a model, which mostly read other layers' caches and weights) and the step's reads
     # do not also pay for writing back the flush's dirty lines.  Each step has its own pair
-    # of events; the flush keeps the GPU busy while the host enqueues the step, so the pair
-    # measures the step on the device, not the host's launch overhead.
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    sweep = torch.ones(64 << 20, dtype=torch.float32, device=dev)
+    # of events; the flush (about 0.16 ms) keeps the GPU busy while the host enqueues the
+    # next step, so the pair measures the step on the device, not the host's launch overhead.
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    sweep = torch.ones(128 << 20, dtype=torch.float32, device=dev)
     sink = torch.empty((), dtype=torch.float32, device=dev)
     for _ in range(5):
         api.cca_decode_fwd(q, K, V, Kc, Vc, pos, wl.g, wl.w, O, LSE, ws, stream=stream)
@@ -411,8 +411,8 @@ def decode_bench(wl, dev, stream, iters, peaks):
     torch.cuda.empty_cache()
     return {"what": f"one decode step at position {pos} ({keys} visible keys per head), split-KV + combine",
             "us_per_step": us, "us_median": step_us[len(step_us) // 2], "steps": iters,
-            "l2": "flushed before every step (256 MB write, then a 256 MB read so the L2 holds clean lines); "
-                  "per-step CUDA events",
+            "l2": "flushed before every step (512 MB write, then a 512 MB read so the L2 holds clean lines); "
+                  "per-step CUDA events (1.024 us ticks)",
             "tokens_per_s": wl.B / (us * 1e-6),
             "gbs": nbytes / (us * 1e-6) / 1e9, "hbm_frac": nbytes / (us * 1e-6) / 1e9 / peaks["hbm_gbs"],
             "algorithmic_bytes": nbytes, "kernel_launches_per_step": 2}
