@@ -257,7 +257,11 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const float *__restri
     const int bh = blockIdx.x;
     const int c = threadIdx.x, lane = c & 31, warp = c >> 5;
     const float *base = ws + static_cast<int64_t>(bh) * MAX_SPLITS * (D + 2);
-    // split weights in parallel: thread s reads split s's (max, sum)
+    // Every load is issued here, at once: column c of each split's partial (they do not
+    // depend on the weights) and, in thread s, split s's (max, sum).
+    float v[MAX_SPLITS];
+#pragma unroll
+    for (int s = 0; s < MAX_SPLITS; ++s) v[s] = s < splits ? base[s * (D + 2) + c] : 0.f;
     const float ms = c < splits ? base[c * (D + 2) + D] : -INFINITY;
     const float ls = c < splits ? base[c * (D + 2) + D + 1] : 0.f;
     float mx = ms;
@@ -277,10 +281,10 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const float *__restri
     float lsum = 0.f;
 #pragma unroll
     for (int w = 0; w < NW; ++w) lsum += sh_wl[w];
-    // column c: independent loads of every split's partial, unrolled so they overlap
+    // column c: the splits' values weighed (sh_f is zero past the last split)
     float acc = 0.f;
-#pragma unroll 8
-    for (int s = 0; s < splits; ++s) acc = fmaf(base[s * (D + 2) + c], sh_f[s], acc);
+#pragma unroll
+    for (int s = 0; s < MAX_SPLITS; ++s) acc = fmaf(v[s], sh_f[s], acc);
     const float val = acc / lsum;
     if constexpr (sizeof(T) == 2) {
         O[static_cast<int64_t>(bh) * D + c] = __float2bfloat16_rn(val);
