@@ -356,6 +356,14 @@ def run_cca(args, rank, world, local):
         out["backward"] = backward_bench(wl, dev, stream, 2, peaks)
     if args.comparator:
         out["full_attention_comparator"] = comparator(wl, dev, stream, max(3, args.steps // 4), ms_per_step)
+        # the same comparison at the other context lengths the pages compare (each against its
+        # own CCA step time from the rows above)
+        if "mha128k" in out:
+            out["full_attention_comparator_128k"] = comparator(W.MHA_128K, dev, stream, 3,
+                                                               out["mha128k"]["ms_per_step"])
+        if out.get("gqa64k"):
+            out["full_attention_comparator_gqa64k"] = comparator(W.GQA_64K, dev, stream, 3,
+                                                                 out["gqa64k"][0]["ms_per_step"])
     sampler.stop()
     if not args.no_e2e:
         out["e2e"] = e2e(wl, dev, stream, max(3, args.steps // 2), world)
