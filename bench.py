@@ -352,6 +352,9 @@ def run_cca(args, rank, world, local):
         out["decode"] = decode_bench(wl, dev, stream, 50, peaks)
         if args.also_128k and wl is not W.MHA_128K:
             out["decode_128k"] = decode_bench(W.MHA_128K, dev, stream, 50, peaks)
+        out["decode_layers"] = decode_layers_bench(wl, dev, 16, 20, peaks)
+        if args.also_128k and wl is not W.MHA_128K:
+            out["decode_layers_128k"] = decode_layers_bench(W.MHA_128K, dev, 16, 20, peaks)
     if args.backward:
         out["backward"] = backward_bench(wl, dev, stream, 2, peaks)
     if args.comparator:
@@ -424,6 +427,68 @@ def decode_bench(wl, dev, stream, iters, peaks):
             "tokens_per_s": wl.B / (us * 1e-6),
             "gbs": nbytes / (us * 1e-6) / 1e9, "hbm_frac": nbytes / (us * 1e-6) / 1e9 / peaks["hbm_gbs"],
             "algorithmic_bytes": nbytes, "kernel_launches_per_step": 2}
+
+
+def decode_layers_bench(wl, dev, n_layers, replays, peaks):
+    """The decode step of a whole model's attention: the same position decoded through
+    n_layers layers, each with its own caches, the 2 * n_layers launches captured in one
+    CUDA graph and replayed.  A replay reads n_layers times the one-step bytes (790 MB at
+    32K, 2.4 GB at 128K), far more than the L2 holds, so every layer's caches come from
+    HBM as in a model; the graph removes the host's per-call cost, so the launches follow
+    one another as closely as the stream allows."""
+    from sparse_long_context_cca_gb300 import api
+    pos = wl.N - 1
+    e = 2 if wl.dtype == "bf16" else 4
+    dt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(wl.seed + 7)
+    G = wl.N // wl.g
+    layers = []
+    for _ in range(n_layers):
+        # seeded random caches of the workload's shape (their values do not change the work)
+        t = [torch.randn(shape, generator=gen, device=dev, dtype=torch.float32).mul_(wl.d ** -0.25).to(dt)
+             for shape in ((wl.B, wl.Hq, wl.d), (wl.B, wl.Hkv, wl.N, wl.d), (wl.B, wl.Hkv, wl.N, wl.d),
+                           (wl.B, wl.Hkv, G, wl.d), (wl.B, wl.Hkv, G, wl.d))]
+        q, K, V, Kc, Vc = t
+        O = torch.empty_like(q)
+        LSE = torch.empty((wl.B, wl.Hq), dtype=torch.float32, device=dev)
+        ws = torch.empty(api.decode_workspace_size(wl.B, wl.Hq, wl.Hkv, wl.N, wl.d, wl.g, wl.w, dt),
+                         dtype=torch.uint8, device=dev)
+        layers.append((q, K, V, Kc, Vc, O, LSE, ws))
+    for (q, K, V, Kc, Vc, O, LSE, ws) in layers:  # eager once: per-device setup outside the capture
+        api.cca_decode_fwd(q, K, V, Kc, Vc, pos, wl.g, wl.w, O, LSE, ws)
+    torch.cuda.synchronize()
+    ref = [(O.clone(), LSE.clone()) for (_, _, _, _, _, O, LSE, _) in layers]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for (q, K, V, Kc, Vc, O, LSE, ws) in layers:
+            api.cca_decode_fwd(q, K, V, Kc, Vc, pos, wl.g, wl.w, O, LSE, ws)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    same = all(torch.equal(O, r[0]) and torch.equal(LSE, r[1])
+               for (_, _, _, _, _, O, LSE, _), r in zip(layers, ref))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(replays)]
+    cur = torch.cuda.current_stream()
+    for e0, e1 in ev:
+        e0.record(cur)
+        graph.replay()
+        e1.record(cur)
+    torch.cuda.synchronize()
+    rep_us = sorted(e0.elapsed_time(e1) * 1e3 for e0, e1 in ev)
+    us = rep_us[len(rep_us) // 2] / n_layers
+    lo = max(0, pos - wl.w + 1)
+    keys = lo // wl.g + (pos - lo + 1)
+    nbytes = wl.B * wl.Hkv * keys * 2 * wl.d * e + 2 * wl.B * wl.Hq * wl.d * e
+    del layers, ref, graph
+    torch.cuda.empty_cache()
+    return {"what": f"the decode step at position {pos} through {n_layers} layers, each with its own caches, "
+                    f"captured as one CUDA graph ({2 * n_layers} launches) and replayed; per-layer figures",
+            "us_per_layer": us, "replays": replays, "replay_us_median": rep_us[len(rep_us) // 2],
+            "bytes_per_replay": nbytes * n_layers,
+            "l2": "not flushed: a replay reads far more than the L2 holds, every layer's caches from HBM",
+            "gbs": nbytes / (us * 1e-6) / 1e9, "hbm_frac": nbytes / (us * 1e-6) / 1e9 / peaks["hbm_gbs"],
+            "replay_matches_eager_bitwise": same, "kernel_launches_per_layer": 2}
 
 
 def backward_bench(wl, dev, stream, iters, peaks):

@@ -141,9 +141,13 @@ int cca_attn_fwd(const void *Q, const void *K, const void *V, const void *Kc, co
  *   cca_decode_workspace_size(params) bytes (per-split partial results); it
  *   needs no initialisation and is fully rewritten by every call.
  * The keys are split across CTAs (flash-decoding) and the partial results are
- * merged by a second kernel on the same stream, launched as a programmatic
- * dependent of the first (it starts as the first drains and waits for its
- * completion on the device).
+ * merged by a second kernel on the same stream.  Both are launched as
+ * programmatic dependents: the split kernel of whatever the stream ran before
+ * the call, the merge of the split kernel.  Each may be scheduled while the
+ * grid before it drains, and waits on the device for that grid's completion
+ * before it reads anything, so the stream order is kept.  The merge lets its
+ * own programmatic dependents (the next decode step's split kernel, say) be
+ * scheduled once the split grid has completed.
  * Supported: bf16 or f32, d in {64, 128}, Hq/Hkv <= 8.
  */
 int cca_decode_fwd(const void *Q, const void *K, const void *V, const void *Kc, const void *Vc, void *O,

@@ -102,6 +102,11 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, R == 1 ? 4 : 1) decode_split_k
     const int wx0 = x0 + (x1 - x0) * warp / DEC_WARPS;
     const int wx1 = x0 + (x1 - x0) * (warp + 1) / DEC_WARPS;
 
+    // This kernel is launched as a programmatic dependent of whatever ran before it on the
+    // stream, so its CTAs may be scheduled while that kernel drains; they wait for its
+    // completion here, before they read anything.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
     float q[R][E], o[R][E], m[R], l[R];
 #pragma unroll
     for (int r = 0; r < R; ++r) {
@@ -254,6 +259,10 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const float *__restri
     // the split grid drains; this waits until that grid has completed and its partials are
     // visible.
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    // A programmatic dependent of this kernel (the next decode step's split kernel, say) may
+    // be scheduled from here on, once the split grid has completed; it waits for this grid's
+    // completion before it reads anything.
+    asm volatile("griddepcontrol.launch_dependents;");
     const int bh = blockIdx.x;
     const int c = threadIdx.x, lane = c & 31, warp = c >> 5;
     const float *base = ws + static_cast<int64_t>(bh) * MAX_SPLITS * (D + 2);
@@ -536,24 +545,25 @@ cudaError_t launch_decode_typed(const void *Q, const void *K, const void *V, con
     if (oe != cudaSuccess) return oe;
     a.splits = decode_splits(a.L, s.B * s.Hkv, sms, occ);
     a.scale_log2 = s.scale * 1.4426950408889634f;
-    dim3 grid(a.splits, s.B * s.Hkv);
-    decode_split_kernel<T, D, R><<<grid, DEC_WARPS * 32, 0, stream>>>(
-        static_cast<const T *>(Q), static_cast<const T *>(K), static_cast<const T *>(V), static_cast<const T *>(Kc),
-        static_cast<const T *>(Vc), ws, a);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    // The merge kernel is a programmatic dependent launch: it is scheduled as the split
-    // grid drains instead of after it, and orders itself with griddepcontrol.wait.
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(s.B * s.Hq);
-    cfg.blockDim = dim3(D);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
+    // Both kernels are programmatic dependent launches: each is scheduled as the grid before
+    // it on the stream drains, instead of after it, and orders itself with griddepcontrol.wait
+    // (the split kernel on whatever preceded the call, the merge on the split kernel).
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.splits, s.B * s.Hkv);
+    cfg.blockDim = dim3(DEC_WARPS * 32);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, decode_split_kernel<T, D, R>, static_cast<const T *>(Q),
+                                       static_cast<const T *>(K), static_cast<const T *>(V),
+                                       static_cast<const T *>(Kc), static_cast<const T *>(Vc), ws, a);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3(s.B * s.Hq);
+    cfg.blockDim = dim3(D);
     return cudaLaunchKernelEx(&cfg, decode_combine_kernel<T, D>, static_cast<const float *>(ws), static_cast<T *>(O),
                               LSE, a.splits);
 }

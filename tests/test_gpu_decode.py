@@ -125,3 +125,64 @@ def test_decode_group_aligned_window():
         rows = [(0, h, pos) for h in range(w.Hq)]
         Oa, La = oracle.attn_rows(Q, K, V, Kc, Vc, w.g, w.w, rows, window_mode=1)
         check_out(O.reshape(-1, w.d), LSE.reshape(-1), Oa, La, Q.dtype, f"aligned window pos {pos}")
+
+
+@pytest.mark.parametrize("graphed", [False, True], ids=["eager", "graph"])
+def test_chained_steps_wait_for_the_step_before(graphed):
+    """Decode steps through several layers where each layer's query is the previous
+    layer's output: the split kernel is a programmatic dependent of the merge kernel before
+    it, which lets its dependents start as soon as it has waited for its own split kernel,
+    before it writes O.  Each step must still read the finished O of the one before, so the
+    chain (launched back to back on one stream, eagerly or as one CUDA graph) equals the
+    same steps run one at a time with a synchronisation in between."""
+    w = wl(1, 8, 2, 2048, 128, 16, 300, seed=31)
+    n_layers = 6
+    gen = torch.Generator(device="cuda").manual_seed(77)
+    layers = []
+    for _ in range(n_layers):
+        K, V = (torch.randn((w.B, w.Hkv, w.N, w.d), generator=gen, device="cuda").mul_(w.d ** -0.25)
+                .to(torch.bfloat16) for _ in range(2))
+        Kc, Vc = (torch.randn((w.B, w.Hkv, w.N // w.g, w.d), generator=gen, device="cuda").mul_(w.d ** -0.25)
+                  .to(torch.bfloat16) for _ in range(2))
+        ws = torch.empty(api.decode_workspace_size(w.B, w.Hq, w.Hkv, w.N, w.d, w.g, w.w, torch.bfloat16),
+                         dtype=torch.uint8, device="cuda")
+        layers.append((K, V, Kc, Vc, ws))
+    pos = w.N - 1
+    q0 = torch.randn((w.B, w.Hq, w.d), generator=gen, device="cuda").to(torch.bfloat16)
+    outs = [torch.empty_like(q0) for _ in range(n_layers)]
+    lses = [torch.empty((w.B, w.Hq), dtype=torch.float32, device="cuda") for _ in range(n_layers)]
+
+    def chain():
+        q = q0
+        for (K, V, Kc, Vc, ws), O, L in zip(layers, outs, lses):
+            api.cca_decode_fwd(q, K, V, Kc, Vc, pos, w.g, w.w, O, L, ws)
+            q = O
+
+    # one step at a time
+    ref = []
+    q = q0
+    for K, V, Kc, Vc, ws in layers:
+        O, L = api.cca_decode_fwd(q, K, V, Kc, Vc, pos, w.g, w.w, workspace=ws)
+        torch.cuda.synchronize()
+        ref.append((O.clone(), L.clone()))
+        q = O
+    if graphed:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            chain()
+    for _ in range(5):
+        for O in outs:
+            O.zero_()
+        torch.cuda.synchronize()
+        if graphed:
+            graph.replay()
+        else:
+            chain()
+        torch.cuda.synchronize()
+        for (O, L), (rO, rL) in zip(zip(outs, lses), ref):
+            assert torch.equal(O, rO) and torch.equal(L, rL)
+    # and the chain's first layer against the oracle
+    Oa, La = oracle.attn_rows(q0.unsqueeze(2).expand(w.B, w.Hq, w.N, w.d), layers[0][0], layers[0][1],
+                              layers[0][2], layers[0][3], w.g, w.w,
+                              [(0, h, pos) for h in range(w.Hq)])
+    check_out(ref[0][0].reshape(-1, w.d), ref[0][1].reshape(-1), Oa, La, torch.bfloat16, "chained layer 0")
