@@ -89,6 +89,10 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, R == 1 ? 4 : 1) decode_split_k
     __shared__ float sm_m[DEC_WARPS][R], sm_l[DEC_WARPS][R];
     __shared__ float sm_o[DEC_WARPS][R][D];
 
+    // This kernel is launched as a programmatic dependent of whatever ran before it on the
+    // stream, so its CTAs may be scheduled while that kernel drains; they wait for its
+    // completion first, before they read anything or signal their own dependent.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     // The merge kernel may be scheduled now: it waits for this grid's completion itself.
     asm volatile("griddepcontrol.launch_dependents;");
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -101,11 +105,6 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, R == 1 ? 4 : 1) decode_split_k
     const int x1 = static_cast<int>(static_cast<int64_t>(a.L) * (s + 1) / a.splits);
     const int wx0 = x0 + (x1 - x0) * warp / DEC_WARPS;
     const int wx1 = x0 + (x1 - x0) * (warp + 1) / DEC_WARPS;
-
-    // This kernel is launched as a programmatic dependent of whatever ran before it on the
-    // stream, so its CTAs may be scheduled while that kernel drains; they wait for its
-    // completion here, before they read anything.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     float q[R][E], o[R][E], m[R], l[R];
 #pragma unroll
@@ -261,7 +260,8 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const float *__restri
     asm volatile("griddepcontrol.wait;" ::: "memory");
     // A programmatic dependent of this kernel (the next decode step's split kernel, say) may
     // be scheduled from here on, once the split grid has completed; it waits for this grid's
-    // completion before it reads anything.
+    // completion before it reads anything.  The signal comes after the wait, never before:
+    // a merge that signalled first saw its wait return before the split grid had completed.
     asm volatile("griddepcontrol.launch_dependents;");
     const int bh = blockIdx.x;
     const int c = threadIdx.x, lane = c & 31, warp = c >> 5;

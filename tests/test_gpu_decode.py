@@ -171,8 +171,13 @@ def test_chained_steps_wait_for_the_step_before(graphed):
         with torch.cuda.graph(graph):
             chain()
     for _ in range(5):
+        # poison what each kernel reads from the one before it: a split kernel reading its
+        # query (the previous layer's O) or a merge reading its workspace too early would
+        # propagate NaN
         for O in outs:
-            O.zero_()
+            O.fill_(float("nan"))
+        for *_, ws in layers:
+            ws.fill_(0xFF)
         torch.cuda.synchronize()
         if graphed:
             graph.replay()
