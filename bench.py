@@ -355,6 +355,10 @@ def run_cca(args, rank, world, local):
         out["decode_layers"] = decode_layers_bench(wl, dev, 16, 20, peaks)
         if args.also_128k and wl is not W.MHA_128K:
             out["decode_layers_128k"] = decode_layers_bench(W.MHA_128K, dev, 16, 20, peaks)
+        if args.sweep and wl is not W.GQA_64K:
+            # grouped-query decode: each CTA reads its KV head's rows once for the 4 query heads
+            out["decode_gqa64k"] = decode_bench(W.GQA_64K, dev, stream, 50, peaks)
+            out["decode_layers_gqa64k"] = decode_layers_bench(W.GQA_64K, dev, 16, 20, peaks)
     if args.backward:
         out["backward"] = backward_bench(wl, dev, stream, 2, peaks)
     if args.comparator:
