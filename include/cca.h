@@ -58,7 +58,7 @@
 extern "C" {
 #endif
 
-#define CCA_ABI_VERSION 2
+#define CCA_ABI_VERSION 3
 
 enum cca_status {
     CCA_OK = 0,
@@ -121,6 +121,30 @@ int cca_pool(const void *Q, const void *K, const void *V, void *Kc, void *Vc,
  */
 int cca_attn_fwd(const void *Q, const void *K, const void *V, const void *Kc, const void *Vc,
                  void *O, float *LSE, const cca_params_t *params, void *stream);
+
+/*
+ * cca_attn_fwd_rows - cca_attn_fwd for the query rows [q_off, q_off + n_q) of a
+ * sequence of params->N tokens, reading only the raw tokens [kv_off, kv_off +
+ * n_kv).  This is the attention of one shard when a sequence is split across
+ * ranks along its length: pooling is group-local, so each rank pools its own
+ * whole groups; the ranks then share their core tokens (all N/g of them) and
+ * each receives the raw rows its first windows reach back to from the ranks
+ * before it.  Rows keep their indices in the whole sequence: visibility, cores
+ * and windows are exactly those of cca_attn_fwd over N tokens.
+ *   Q, O   [B, Hq, n_q, d]     the rows q_off .. q_off + n_q - 1
+ *   LSE    [B, Hq, n_q]        fp32
+ *   K, V   [B, Hkv, n_kv, d]   the raw tokens kv_off .. kv_off + n_kv - 1
+ *   Kc, Vc [B, Hkv, N/g, d]    core tokens of the whole sequence; rows below
+ *                              lo(q_off + n_q - 1)/g must be valid
+ * Requirements (else CCA_ERR_INVALID_ARG, nothing launched): n_q >= 1,
+ * 0 <= kv_off <= first raw token of row q_off's window (lo(q_off), or its
+ * group boundary with window_mode 1), q_off + n_q <= kv_off + n_kv <= N.
+ * Everything else (support, alignment, errors) as cca_attn_fwd; with q_off = 0,
+ * kv_off = 0 and n_q = n_kv = N it is cca_attn_fwd.
+ */
+int cca_attn_fwd_rows(const void *Q, const void *K, const void *V, const void *Kc, const void *Vc,
+                      void *O, float *LSE, int q_off, int n_q, int kv_off, int n_kv,
+                      const cca_params_t *params, void *stream);
 
 /*
  * Decoding (one new token per sequence).  The pages describe a decode step that

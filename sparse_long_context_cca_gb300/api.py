@@ -45,7 +45,7 @@ class CcaParams(ctypes.Structure):
 _lib = None
 _lock = threading.Lock()
 
-EXPORTED = ["cca_pool", "cca_attn_fwd", "cca_decode_fwd", "cca_decode_workspace_size", "cca_pool_group",
+EXPORTED = ["cca_pool", "cca_attn_fwd", "cca_attn_fwd_rows", "cca_decode_fwd", "cca_decode_workspace_size", "cca_pool_group",
             "cca_decode_fwd_noalloc", "cca_prefill_bwd", "cca_prefill_bwd_workspace_size",
             "cca_prefill_host", "cca_prefill_host_workspace_size",
             "cca_status_string", "cca_abi_version", "cca_test_set_wait_limit_ns", "cca_test_skip_q_load"]
@@ -72,6 +72,9 @@ def load_library():
         lib.cca_pool.restype = ctypes.c_int
         lib.cca_attn_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, pp, vp]
         lib.cca_attn_fwd.restype = ctypes.c_int
+        ci = ctypes.c_int
+        lib.cca_attn_fwd_rows.argtypes = [vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, pp, vp]
+        lib.cca_attn_fwd_rows.restype = ctypes.c_int
         lib.cca_decode_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, ctypes.c_int, pp, vp, ctypes.c_uint64, vp]
         lib.cca_decode_fwd.restype = ctypes.c_int
         lib.cca_decode_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, ctypes.c_int, pp, vp]
@@ -191,6 +194,42 @@ def cca_attn_fwd(Q, K, V, Kc, Vc, g: int, w: int, O=None, LSE=None, scale: float
                           O.data_ptr(), LSE.data_ptr(), ctypes.byref(prm), _stream_handle(stream))
     if st != CCA_OK:
         raise CcaError(st, "cca_attn_fwd")
+    return O, LSE
+
+
+def cca_attn_fwd_rows(Q, K, V, Kc, Vc, g: int, w: int, N: int, q_off: int, kv_off: int, O=None, LSE=None,
+                      scale: float = 0.0, dev_status=None, stream=None, window_mode: int = 0):
+    """Fused attention for the query rows [q_off, q_off + n_q) of an N-token sequence.
+    Q [B,Hq,n_q,d] holds those rows, K, V [B,Hkv,n_kv,d] the raw tokens from kv_off on,
+    Kc, Vc [B,Hkv,N/g,d] the whole sequence's core tokens.  Returns (O [B,Hq,n_q,d],
+    LSE [B,Hq,n_q] fp32), equal to rows q_off .. q_off + n_q - 1 of cca_attn_fwd over N."""
+    lib = load_library()
+    B, Hq, n_q, d = Q.shape
+    Hkv, n_kv = K.shape[1], K.shape[2]
+    if Q.dtype not in _DTYPE:
+        raise ValueError(f"unsupported dtype {Q.dtype}")
+    G = N // g if g > 0 else 0
+    _check(Q, "Q", Q.dtype, (B, Hq, n_q, d))
+    _check(K, "K", Q.dtype, (B, Hkv, n_kv, d))
+    _check(V, "V", Q.dtype, (B, Hkv, n_kv, d))
+    _check(Kc, "Kc", Q.dtype, (B, Hkv, G, d))
+    _check(Vc, "Vc", Q.dtype, (B, Hkv, G, d))
+    if O is None:
+        O = torch.empty_like(Q)
+    if LSE is None:
+        LSE = torch.empty((B, Hq, n_q), dtype=torch.float32, device=Q.device)
+    _check(O, "O", Q.dtype, (B, Hq, n_q, d))
+    _check(LSE, "LSE", torch.float32, (B, Hq, n_q))
+    status_ptr = None
+    if dev_status is not None:
+        _check(dev_status, "dev_status", torch.int32, (1,))
+        status_ptr = dev_status.data_ptr()
+    prm = make_params(B, Hq, Hkv, N, d, g, w, _DTYPE[Q.dtype], scale, status_ptr, window_mode=window_mode)
+    st = lib.cca_attn_fwd_rows(Q.data_ptr(), K.data_ptr(), V.data_ptr(), Kc.data_ptr(), Vc.data_ptr(),
+                               O.data_ptr(), LSE.data_ptr(), int(q_off), int(n_q), int(kv_off), int(n_kv),
+                               ctypes.byref(prm), _stream_handle(stream))
+    if st != CCA_OK:
+        raise CcaError(st, "cca_attn_fwd_rows")
     return O, LSE
 
 

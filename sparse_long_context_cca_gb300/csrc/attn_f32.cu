@@ -59,13 +59,16 @@ __global__ void __launch_bounds__(128) attn_f32_kernel(const float *__restrict__
                                                        const float *__restrict__ Vc, float *__restrict__ O,
                                                        float *__restrict__ LSE, int Hq, int Hkv, int N,
                                                        int g, int w, int window_mode, float scale_log2,
-                                                       int64_t total_rows) {
+                                                       int64_t total_rows, int q_off, int n_q, int kv_off,
+                                                       int n_kv) {
     constexpr int PL = D / 32;
     const int lane = threadIdx.x & 31;
     const int64_t u = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (u >= total_rows) return;  // warp-uniform
-    const int64_t i = u % N;
-    const int64_t bh = u / N;
+    // Q, O and LSE hold the rows [q_off, q_off + n_q) of the N-token sequence, K and V the
+    // raw tokens from kv_off on; i is the row's index in the sequence.
+    const int64_t i = q_off + u % n_q;
+    const int64_t bh = u / n_q;
     const int64_t b = bh / Hq, h = bh % Hq;
     const int64_t bk = b * Hkv + h / (Hq / Hkv);
     const int64_t G = N / g;
@@ -81,9 +84,9 @@ __global__ void __launch_bounds__(128) attn_f32_kernel(const float *__restrict__
     const float *kc = Kc + bk * G * D;
     const float *vc = Vc + bk * G * D;
     for (int64_t j = 0; j < n_core; ++j) st.step(kc + j * D, vc + j * D, lane, scale_log2);
-    const float *kk = K + bk * static_cast<int64_t>(N) * D;
-    const float *vv = V + bk * static_cast<int64_t>(N) * D;
-    for (int64_t t = lo; t <= i; ++t) st.step(kk + t * D, vv + t * D, lane, scale_log2);
+    const float *kk = K + bk * static_cast<int64_t>(n_kv) * D;
+    const float *vv = V + bk * static_cast<int64_t>(n_kv) * D;
+    for (int64_t t = lo; t <= i; ++t) st.step(kk + (t - kv_off) * D, vv + (t - kv_off) * D, lane, scale_log2);
 
     const float inv = 1.f / st.l;
 #pragma unroll
@@ -94,17 +97,20 @@ __global__ void __launch_bounds__(128) attn_f32_kernel(const float *__restrict__
 }  // namespace
 
 cudaError_t launch_attn_f32(const float *Q, const float *K, const float *V, const float *Kc, const float *Vc,
-                            float *O, float *LSE, const Shape &s, cudaStream_t stream) {
-    const int64_t rows = static_cast<int64_t>(s.B) * s.Hq * s.N;
+                            float *O, float *LSE, const Shape &s, cudaStream_t stream, const RowRange &rr) {
+    const int n_q = rr.n_q < 0 ? s.N : rr.n_q, n_kv = rr.n_kv < 0 ? s.N : rr.n_kv;
+    const int64_t rows = static_cast<int64_t>(s.B) * s.Hq * n_q;
     const int warps = 4;
     const unsigned blocks = static_cast<unsigned>((rows + warps - 1) / warps);
     const float scale_log2 = s.scale * 1.4426950408889634f;
     if (s.d == 64) {
         attn_f32_kernel<64><<<blocks, warps * 32, 0, stream>>>(Q, K, V, Kc, Vc, O, LSE, s.Hq, s.Hkv, s.N, s.g,
-                                                               s.w, s.window_mode, scale_log2, rows);
+                                                               s.w, s.window_mode, scale_log2, rows, rr.q_off, n_q,
+                                                               rr.kv_off, n_kv);
     } else if (s.d == 128) {
         attn_f32_kernel<128><<<blocks, warps * 32, 0, stream>>>(Q, K, V, Kc, Vc, O, LSE, s.Hq, s.Hkv, s.N,
-                                                                s.g, s.w, s.window_mode, scale_log2, rows);
+                                                                s.g, s.w, s.window_mode, scale_log2, rows, rr.q_off,
+                                                                n_q, rr.kv_off, n_kv);
     } else {
         return cudaErrorNotSupported;
     }

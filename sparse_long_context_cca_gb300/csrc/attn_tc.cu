@@ -85,6 +85,9 @@ static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 struct Params {
     int B, Hq, Hkv, N, g, w, n_pairs, n_items;
+    // Query rows [q_off, q_off + n_q) of the N-token sequence; Q, O and LSE hold those rows,
+    // K and V hold the raw tokens from kv_off on.  The whole sequence: 0, N, 0.
+    int q_off, n_q, kv_off;
     int window_mode;  // 1: raw window starts at the group boundary g * (lo(i) / g)
     float scale_log2;
     __nv_bfloat16 *O;
@@ -142,8 +145,8 @@ __device__ __forceinline__ int half_max_step(const Half &x, int Tc) {
 __device__ __forceinline__ Half make_half(const Params &p, int a, int lo0) {
     Half x;
     x.a = a;
-    x.valid = a < p.N;
-    x.b = min(a + BM - 1, p.N - 1);
+    x.valid = a - p.q_off < p.n_q;
+    x.b = min(a + BM - 1, p.q_off + p.n_q - 1);
     if (!x.valid) {
         x.tc = x.kl = x.kh = 0;
         return x;
@@ -162,7 +165,7 @@ __device__ __forceinline__ Item make_item(const Params &p, int k) {
     it.bh = k % BH;
     const int b = it.bh / p.Hq, h = it.bh % p.Hq;
     it.kvz = b * p.Hkv + h / (p.Hq / p.Hkv);
-    const int i0 = pair * 2 * BM;
+    const int i0 = p.q_off + pair * 2 * BM;  // first row (indices are the sequence's)
     it.lo0 = win_of(p, i0);
     it.hA = make_half(p, i0, it.lo0);
     it.hB = make_half(p, i0 + BM, it.lo0);
@@ -241,14 +244,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     ptx::mbar_arrive_expect_tx(bar(B_QFULL), 2 * TILE_BYTES);
                     for (int h = 0; h < 2; ++h) {
                         const uint32_t dst = base + OFF_Q + h * TILE_BYTES;
-                        const int row0 = h ? it.hB.a : it.hA.a;
+                        const int row0 = (h ? it.hB.a : it.hA.a) - p.q_off;
                         ptx::tma_load_3d(&tmQ, bar(B_QFULL), dst, 0, row0, it.bh);
                         ptx::tma_load_3d(&tmQ, bar(B_QFULL), dst + HALF_BYTES, 64, row0, it.bh);
                     }
                 }
                 for (int t = 0; ok && t < it.T; ++t, u += 2) {
                     const bool core = t < it.Tc;
-                    const int y = core ? t * BN : it.lo0 + (t - it.Tc) * BN;
+                    const int y = core ? t * BN : it.lo0 + (t - it.Tc) * BN - p.kv_off;
                     // K(t) goes to ring slot u % NS, V(t) to the next one; both copies
                     // complete the K slot's FULL barrier (u is even, see k_full_parity)
                     const int ks = u % NS, vs = (u + 1) % NS;
@@ -582,9 +585,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 break;
             }
             ptx::tc_fence_after();
-            const bool valid = i < p.N;
+            const int li = i - p.q_off;  // row of O and LSE
+            const bool valid = li < p.n_q;
             const float inv = 1.f / l;
-            __nv_bfloat16 *orow = p.O + (static_cast<int64_t>(it.bh) * p.N + i) * HD;
+            __nv_bfloat16 *orow = p.O + (static_cast<int64_t>(it.bh) * p.n_q + li) * HD;
             uint32_t o[4][32];
 #pragma unroll
             for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tO + c * 32, o[c]);
@@ -618,7 +622,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 }
             }
-            if (valid) p.LSE[static_cast<int64_t>(it.bh) * p.N + i] = (m + __log2f(l)) * 0.6931471805599453f;
+            if (valid) p.LSE[static_cast<int64_t>(it.bh) * p.n_q + li] = (m + __log2f(l)) * 0.6931471805599453f;
             ++n_done;
         }
     }
@@ -660,7 +664,8 @@ unsigned long long g_wait_limit_ns = 1000000000ull;
 int g_skip_q_load = 0;
 
 cudaError_t launch_attn_bf16_tc(const void *Q, const void *K, const void *V, const void *Kc, const void *Vc,
-                                void *O, float *LSE, const Shape &s, int32_t *dev_status, cudaStream_t stream) {
+                                void *O, float *LSE, const Shape &s, int32_t *dev_status, cudaStream_t stream,
+                                const RowRange &rr) {
     EncodeTiledFn enc = get_encoder();
     if (enc == nullptr) return cudaErrorNotSupported;
     int dev = 0;
@@ -671,8 +676,9 @@ cudaError_t launch_attn_bf16_tc(const void *Q, const void *K, const void *V, con
     const uint64_t G = static_cast<uint64_t>(s.N / s.g);
     CUtensorMap mQ, mK, mV, mKc, mVc;
     const uint64_t qh = static_cast<uint64_t>(s.B) * s.Hq, kh = static_cast<uint64_t>(s.B) * s.Hkv;
-    if (!encode_3d_bf16_d128(enc, &mQ, Q, s.N, qh) || !encode_3d_bf16_d128(enc, &mK, K, s.N, kh) ||
-        !encode_3d_bf16_d128(enc, &mV, V, s.N, kh) || !encode_3d_bf16_d128(enc, &mKc, Kc, G, kh) ||
+    const int n_q = rr.n_q < 0 ? s.N : rr.n_q, n_kv = rr.n_kv < 0 ? s.N : rr.n_kv;
+    if (!encode_3d_bf16_d128(enc, &mQ, Q, n_q, qh) || !encode_3d_bf16_d128(enc, &mK, K, n_kv, kh) ||
+        !encode_3d_bf16_d128(enc, &mV, V, n_kv, kh) || !encode_3d_bf16_d128(enc, &mKc, Kc, G, kh) ||
         !encode_3d_bf16_d128(enc, &mVc, Vc, G, kh))
         return cudaErrorInvalidValue;
 
@@ -684,7 +690,10 @@ cudaError_t launch_attn_bf16_tc(const void *Q, const void *K, const void *V, con
     p.g = s.g;
     p.w = s.w;
     p.window_mode = s.window_mode;
-    p.n_pairs = (s.N + 2 * BM - 1) / (2 * BM);
+    p.q_off = rr.q_off;
+    p.n_q = n_q;
+    p.kv_off = rr.kv_off;
+    p.n_pairs = (n_q + 2 * BM - 1) / (2 * BM);
     p.n_items = p.n_pairs * s.B * s.Hq;
     p.scale_log2 = s.scale * 1.4426950408889634f;
     p.O = static_cast<__nv_bfloat16 *>(O);

@@ -7,6 +7,7 @@
 
 #include "../../include/cca.h"
 #include "internal.h"
+#include "visibility.cuh"
 
 namespace cca {
 extern unsigned long long g_wait_limit_ns;
@@ -108,6 +109,39 @@ int cca_attn_fwd(const void *Q, const void *K, const void *V, const void *Kc, co
                                               static_cast<const float *>(Vc), static_cast<float *>(O), LSE, s,
                                               strm));
     return from_cuda(cca::launch_attn_bf16_tc(Q, K, V, Kc, Vc, O, LSE, s, params->dev_status, strm));
+}
+
+int cca_attn_fwd_rows(const void *Q, const void *K, const void *V, const void *Kc, const void *Vc, void *O,
+                      float *LSE, int q_off, int n_q, int kv_off, int n_kv, const cca_params_t *params,
+                      void *stream) {
+    int st = check_shape(params, true);
+    if (st != CCA_OK) return st;
+    const void *ptrs[7] = {Q, K, V, Kc, Vc, O, LSE};
+    for (const void *q : ptrs)
+        if (q == nullptr || !aligned16(q)) return CCA_ERR_INVALID_ARG;
+    if (params->dev_status != nullptr && (reinterpret_cast<uintptr_t>(params->dev_status) & 3u) != 0)
+        return CCA_ERR_INVALID_ARG;
+    // the rows, then the raw tokens they read: every window lies inside [kv_off, kv_off + n_kv)
+    const int64_t N = params->N;
+    if (n_q < 1 || q_off < 0 || static_cast<int64_t>(q_off) + n_q > N) return CCA_ERR_INVALID_ARG;
+    if (kv_off < 0 || n_kv < 1 || static_cast<int64_t>(kv_off) + n_kv > N) return CCA_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(kv_off) + n_kv < static_cast<int64_t>(q_off) + n_q) return CCA_ERR_INVALID_ARG;
+    if (kv_off > cca::window_start(q_off, params->w, params->g, params->window_mode)) return CCA_ERR_INVALID_ARG;
+    if (params->dtype == CCA_BF16 && params->d != 128) return CCA_ERR_UNSUPPORTED;
+    if ((st = check_device()) != CCA_OK) return st;
+    const cca::Shape s = to_shape(params);
+    cca::RowRange rr;
+    rr.q_off = q_off;
+    rr.n_q = n_q;
+    rr.kv_off = kv_off;
+    rr.n_kv = n_kv;
+    cudaStream_t strm = static_cast<cudaStream_t>(stream);
+    if (params->dtype == CCA_F32)
+        return from_cuda(cca::launch_attn_f32(static_cast<const float *>(Q), static_cast<const float *>(K),
+                                              static_cast<const float *>(V), static_cast<const float *>(Kc),
+                                              static_cast<const float *>(Vc), static_cast<float *>(O), LSE, s,
+                                              strm, rr));
+    return from_cuda(cca::launch_attn_bf16_tc(Q, K, V, Kc, Vc, O, LSE, s, params->dev_status, strm, rr));
 }
 
 int cca_decode_fwd(const void *Q, const void *K, const void *V, const void *Kc, const void *Vc, void *O, float *LSE,

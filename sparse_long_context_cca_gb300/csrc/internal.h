@@ -19,16 +19,23 @@ struct Shape {
 cudaError_t launch_pool(int dtype, const void *Q, const void *K, const void *V, void *Kc, void *Vc,
                         const Shape &s, int32_t *status, cudaStream_t stream);
 
+// The query rows an attention launch computes: rows [q_off, q_off + n_q) of the s.N-token
+// sequence, Q/O/LSE holding those rows and K/V the raw tokens [kv_off, kv_off + n_kv).
+// Negative counts stand for s.N (the whole sequence).  Kc/Vc always hold all s.N/g cores.
+struct RowRange {
+    int q_off = 0, n_q = -1, kv_off = 0, n_kv = -1;
+};
+
 // fp32 fused attention on CUDA cores (any supported d).
 cudaError_t launch_attn_f32(const float *Q, const float *K, const float *V, const float *Kc,
                             const float *Vc, float *O, float *LSE, const Shape &s,
-                            cudaStream_t stream);
+                            cudaStream_t stream, const RowRange &rr = RowRange{});
 
 // bf16 fused attention on the tcgen05 tensor cores (d = 128).
 // Returns cudaErrorNotSupported when the tensor-map encoder is unavailable.
 cudaError_t launch_attn_bf16_tc(const void *Q, const void *K, const void *V, const void *Kc,
                                 const void *Vc, void *O, float *LSE, const Shape &s,
-                                int32_t *dev_status, cudaStream_t stream);
+                                int32_t *dev_status, cudaStream_t stream, const RowRange &rr = RowRange{});
 
 // Decode step (row `pos` of the fused attention over the caches) and single-group pooling.
 uint64_t decode_workspace_bytes(const Shape &s);

@@ -10,7 +10,9 @@ stays inside a shard.  The fused attention of a row (fusion equation) then needs
     earlier shards: a halo of at most w - 1 rows (more with the group-aligned window),
     sent point to point by the ranks that hold them.
 This module holds no arithmetic of the method; it plans who needs which rows and moves
-them with torch.distributed (any backend with all_gather and send/recv).
+them with torch.distributed (any backend with all_gather and send/recv), and `shard_prefill`
+runs one rank's part with the library's kernels (pooling of its own groups, then
+cca_attn_fwd_rows over its rows).
 """
 from __future__ import annotations
 
@@ -84,7 +86,7 @@ def gather_cores(local_kc: torch.Tensor, local_vc: torch.Tensor, shards: list[Sh
     B, H, _, d = local_kc.shape
     out = []
     for t in (local_kc, local_vc):
-        pad = torch.zeros((B, H, gmax, d), dtype=t.dtype)
+        pad = torch.zeros((B, H, gmax, d), dtype=t.dtype, device=t.device)
         pad[:, :, :t.shape[2]] = t
         parts = [torch.empty_like(pad) for _ in shards]
         dist.all_gather(parts, pad.contiguous())
@@ -98,7 +100,7 @@ def exchange_halo(local_k: torch.Tensor, local_v: torch.Tensor, shards: list[Sha
     rank = dist.get_rank()
     me = shards[rank]
     B, H, _, d = local_k.shape
-    k = torch.zeros((B, H, me.q1 - me.halo0, d), dtype=local_k.dtype)
+    k = torch.zeros((B, H, me.q1 - me.halo0, d), dtype=local_k.dtype, device=local_k.device)
     v = torch.zeros_like(k)
     k[:, :, me.q0 - me.halo0:] = local_k
     v[:, :, me.q0 - me.halo0:] = local_v
@@ -111,7 +113,7 @@ def exchange_halo(local_k: torch.Tensor, local_v: torch.Tensor, shards: list[Sha
                 reqs.append(dist.isend(t[:, :, a - src_sh.q0:b - src_sh.q0].contiguous(), dst))
         elif dst == rank:
             for buf in (k, v):
-                piece = torch.empty((B, H, b - a, d), dtype=local_k.dtype)
+                piece = torch.empty((B, H, b - a, d), dtype=local_k.dtype, device=local_k.device)
                 reqs.append(dist.irecv(piece, src))
                 recvs.append((buf, a, b, piece))
     for r in reqs:
@@ -119,3 +121,21 @@ def exchange_halo(local_k: torch.Tensor, local_v: torch.Tensor, shards: list[Sha
     for buf, a, b, piece in recvs:
         buf[:, :, a - me.halo0:b - me.halo0] = piece
     return k, v
+
+
+def shard_prefill(Q, K, V, shards: list[Shard], g: int, w: int, N: int, pool_mode: int = 0,
+                  window_mode: int = 0, scale: float = 0.0):
+    """This rank's CCA prefill: Q, K, V [B, H, q1 - q0, d] hold its rows [q0, q1) of the
+    N-token sequence (CUDA tensors).  Pools its own groups, all-gathers every rank's core
+    tokens, receives its window halo, and attends its rows.  Returns (O, LSE) for its rows
+    and its own core tokens; equal to rows [q0, q1) of the unsharded prefill."""
+    from . import api
+    me = shards[dist.get_rank()]
+    if me.q1 == me.q0:
+        raise ValueError("this rank holds no group")
+    kc, vc = api.cca_pool(Q, K, V, g, scale=scale, pool_mode=pool_mode)
+    Kc, Vc = gather_cores(kc, vc, shards, g)
+    Kh, Vh = exchange_halo(K, V, shards)
+    O, LSE = api.cca_attn_fwd_rows(Q, Kh, Vh, Kc, Vc, g, w, N, me.q0, me.halo0, scale=scale,
+                                   window_mode=window_mode)
+    return O, LSE, kc, vc

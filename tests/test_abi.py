@@ -38,7 +38,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_strings(lib):
-    assert lib.cca_abi_version() == 2
+    assert lib.cca_abi_version() == 3
     for code in (0, -1, -2, -3, -4, 7):
         assert isinstance(api.status_string(code), str) and api.status_string(code)
 
@@ -185,3 +185,29 @@ def test_prefill_host_binding_requires_cpu_tensors(lib):
     Q = torch.zeros(1, 2, 32, 128, dtype=torch.bfloat16, device="meta")
     with pytest.raises(ValueError):
         api.cca_prefill_host(Q, Q, Q, 16, 8)
+
+
+def call_rows(lib, q_off, n_q, kv_off, n_kv, **kw):
+    base = dict(B=1, Hq=2, Hkv=2, N=1024, d=128, g=16, w=100, dtype=api.CCA_BF16)
+    base.update(kw)
+    prm = api.make_params(**base)
+    return lib.cca_attn_fwd_rows(*P, q_off, n_q, kv_off, n_kv, ctypes.byref(prm), None)
+
+
+@pytest.mark.parametrize("args", [
+    (0, 0, 0, 10),          # no rows
+    (-1, 10, 0, 10),        # negative offset
+    (1000, 25, 901, 124),   # rows past N
+    (500, 10, 402, 108),    # K/V start after row 500's window start (401)
+    (500, 10, 401, 100),    # K/V end before the last row
+    (500, 10, 401, 700),    # K/V past N
+    (500, 10, -1, 600),     # negative K/V offset
+])
+def test_rows_rejects_bad_ranges(lib, args):
+    assert call_rows(lib, *args) == api.CCA_ERR_INVALID_ARG
+
+
+def test_rows_window_mode_moves_the_first_raw_token(lib):
+    # with window_mode 1, row 500's window starts at the group boundary 400, so K/V from 401
+    # leave a token out: rejected (with window_mode 0 the same range would be valid)
+    assert call_rows(lib, 500, 10, 401, 109, window_mode=1) == api.CCA_ERR_INVALID_ARG
