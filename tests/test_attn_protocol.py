@@ -43,18 +43,20 @@ def win_of(i, w, g, wm):
 
 
 class Item:
-    def __init__(self, N, g, w, wm, k, BH, n_pairs):
+    def __init__(self, N, g, w, wm, k, BH, n_pairs, q_off=0, n_q=None):
+        # rows [q_off, q_off + n_q) of the N-token sequence (the whole of it by default)
+        n_q = N - q_off if n_q is None else n_q
         pair = n_pairs - 1 - k // BH
-        i0 = pair * 2 * BM
+        i0 = q_off + pair * 2 * BM
         self.lo0 = win_of(i0, w, g, wm)
         self.valid, self.tc, self.kl, self.kh = [], [], [], []
         last = None
         for a in (i0, i0 + BM):
-            if a >= N:
+            if a - q_off >= n_q:
                 self.valid.append(False)
                 self.tc.append(0), self.kl.append(0), self.kh.append(0)
                 continue
-            b = min(a + BM - 1, N - 1)
+            b = min(a + BM - 1, q_off + n_q - 1)
             last = b
             self.valid.append(True)
             self.tc.append((lo_of(b, w) // g + BN - 1) // BN)
@@ -93,10 +95,12 @@ class Bar:
         self.phases += 1
 
 
-def run(N, g, w, wm, grid, blk, seed, H=2):
-    """Runs the model for CTA `blk` of `grid`; returns None, or the blocked waits on deadlock."""
-    n_pairs = (N + 2 * BM - 1) // (2 * BM)
-    items = [Item(N, g, w, wm, k, H, n_pairs) for k in range(blk, n_pairs * H, grid)]
+def run(N, g, w, wm, grid, blk, seed, H=2, q_off=0, n_q=None):
+    """Runs the model for CTA `blk` of `grid`; returns None, or the blocked waits on deadlock.
+    q_off, n_q: a launch over the rows [q_off, q_off + n_q) only (cca_attn_fwd_rows)."""
+    n_rows = N - q_off if n_q is None else n_q
+    n_pairs = (n_rows + 2 * BM - 1) // (2 * BM)
+    items = [Item(N, g, w, wm, k, H, n_pairs, q_off, n_rows) for k in range(blk, n_pairs * H, grid)]
     qfull, qfree = Bar("qfull"), Bar("qfree")
     full = [Bar(f"full{s}") for s in range(NS)]
     empty = [Bar(f"empty{s}") for s in range(NS)]
@@ -266,3 +270,36 @@ def test_large_groups_take_the_deferring_loop():
     items = [Item(4096, 512, 4, 1, k, 2, n_pairs) for k in range(n_pairs * 2)]
     assert any(max(it.max_step(0), it.max_step(1)) > 2 for it in items)
     assert run(4096, 512, 4, 1, 1, 0, seed=1) is None
+
+
+RANGES = [(N, g, w, wm, q_off, n_q)
+          for wm in (0, 1)
+          for N, g in ((2048, 16), (4096, 512), (3072, 384), (1024, 1))
+          for w in (1, 96, 300, 1024)
+          for q_off, n_q in ((16, 1000), (112, N - 112), (N // 2 - g, 300), (N - 1, 1), (0, 257))
+          if q_off >= 0 and q_off + n_q <= N]
+
+
+@pytest.mark.parametrize("wm", [0, 1])
+def test_row_ranges_do_not_deadlock(wm):
+    """Launches over a row range (a shard of a sequence) deal items of 256 rows from q_off, so
+    their tile sequences start at other offsets than the whole sequence's: the same model,
+    the same property."""
+    bad = []
+    deferring = 0
+    for N, g, w, m, q_off, n_q in RANGES:
+        if m != wm:
+            continue
+        n_pairs = (n_q + 2 * BM - 1) // (2 * BM)
+        deferring += sum(max(it.max_step(0), it.max_step(1)) > 2
+                         for it in (Item(N, g, w, m, k, 2, n_pairs, q_off, n_q) for k in range(2 * n_pairs)))
+        n_items = 2 * ((n_q + 2 * BM - 1) // (2 * BM))  # two heads
+        for grid, blk in ((1, 0), (3, 2)):
+            if blk >= n_items:  # the kernel launches min(items, SMs) CTAs
+                continue
+            r = run(N, g, w, m, grid, blk, seed=N + q_off * 5 + w, q_off=q_off, n_q=n_q)
+            if r is not None:
+                bad.append(((N, g, w, m, q_off, n_q, grid, blk), r))
+    assert not bad, bad[:3]
+    if wm == 1:
+        assert deferring > 0  # the group-aligned window with large groups takes the deferring loop
