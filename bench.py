@@ -430,7 +430,8 @@ def decode_bench(wl, dev, stream, iters, peaks):
                   "per-step CUDA events (1.024 us ticks)",
             "tokens_per_s": wl.B / (us * 1e-6),
             "gbs": nbytes / (us * 1e-6) / 1e9, "hbm_frac": nbytes / (us * 1e-6) / 1e9 / peaks["hbm_gbs"],
-            "algorithmic_bytes": nbytes, "kernel_launches_per_step": 2}
+            "algorithmic_bytes": nbytes,
+            "kernel_launches_per_step": api.decode_kernels(wl.B, wl.Hq, wl.Hkv, wl.N, wl.d, wl.g, wl.w, q.dtype, pos)}
 
 
 def decode_layers_bench(wl, dev, n_layers, replays, peaks):
@@ -492,7 +493,8 @@ def decode_layers_bench(wl, dev, n_layers, replays, peaks):
             "bytes_per_replay": nbytes * n_layers,
             "l2": "not flushed: a replay reads far more than the L2 holds, every layer's caches from HBM",
             "gbs": nbytes / (us * 1e-6) / 1e9, "hbm_frac": nbytes / (us * 1e-6) / 1e9 / peaks["hbm_gbs"],
-            "replay_matches_eager_bitwise": same, "kernel_launches_per_layer": 2}
+            "replay_matches_eager_bitwise": same,
+            "kernel_launches_per_layer": api.decode_kernels(wl.B, wl.Hq, wl.Hkv, wl.N, wl.d, wl.g, wl.w, dt, pos)}
 
 
 def backward_bench(wl, dev, stream, iters, peaks):

@@ -164,10 +164,13 @@ int cca_attn_fwd_rows(const void *Q, const void *K, const void *V, const void *K
  *   workspace: caller-owned device buffer of at least
  *   cca_decode_workspace_size(params) bytes (per-split partial results); it
  *   needs no initialisation and is fully rewritten by every call.
- * The keys are split across CTAs (flash-decoding) and the partial results are
- * merged by a second kernel on the same stream.  Both are launched as
- * programmatic dependents: the split kernel of whatever the stream ran before
- * the call, the merge of the split kernel.  Each may be scheduled while the
+ * The keys are split across CTAs (flash-decoding).  For long visible lists
+ * with enough (b, kv) pairs to fill the GPU, the splits of each (b, kv) form a
+ * thread-block cluster and merge in it: one kernel, the workspace unused.
+ * Otherwise the partial results are merged by a second kernel on the same
+ * stream.  The kernels are launched as programmatic dependents: the split
+ * kernel of whatever the stream ran before the call, the merge of the split
+ * kernel.  Each may be scheduled while the
  * grid before it drains, and waits on the device for that grid's completion
  * before it reads anything, so the stream order is kept.  The merge lets its
  * own programmatic dependents (the next decode step's split kernel, say) be
@@ -177,6 +180,12 @@ int cca_attn_fwd_rows(const void *Q, const void *K, const void *V, const void *K
 int cca_decode_fwd(const void *Q, const void *K, const void *V, const void *Kc, const void *Vc, void *O,
                    float *LSE, int pos, const cca_params_t *params, void *workspace,
                    uint64_t workspace_bytes, void *stream);
+
+/* Kernels one cca_decode_fwd (or _noalloc) call at `pos` launches on the current
+ * device: 1 when the splits of each (b, kv) merge inside a thread-block cluster
+ * (long visible lists with enough (b, kv) pairs to fill the GPU), 2 for the
+ * split kernel and its merge kernel; a negative status on bad arguments. */
+int cca_decode_kernels(const cca_params_t *params, int pos);
 
 /* Bytes of workspace cca_decode_fwd needs for these shapes (0 on bad params). */
 uint64_t cca_decode_workspace_size(const cca_params_t *params);

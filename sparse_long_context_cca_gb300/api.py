@@ -45,10 +45,12 @@ class CcaParams(ctypes.Structure):
 _lib = None
 _lock = threading.Lock()
 
-EXPORTED = ["cca_pool", "cca_attn_fwd", "cca_attn_fwd_rows", "cca_decode_fwd", "cca_decode_workspace_size", "cca_pool_group",
+EXPORTED = ["cca_pool", "cca_attn_fwd", "cca_attn_fwd_rows", "cca_decode_fwd", "cca_decode_workspace_size",
+            "cca_decode_kernels", "cca_pool_group",
             "cca_decode_fwd_noalloc", "cca_prefill_bwd", "cca_prefill_bwd_workspace_size",
             "cca_prefill_host", "cca_prefill_host_workspace_size",
-            "cca_status_string", "cca_abi_version", "cca_test_set_wait_limit_ns", "cca_test_skip_q_load"]
+            "cca_status_string", "cca_abi_version", "cca_test_set_wait_limit_ns", "cca_test_skip_q_load",
+            "cca_test_decode_path"]
 
 
 def library_path() -> str:
@@ -87,6 +89,8 @@ def load_library():
         lib.cca_prefill_host.restype = ctypes.c_int
         lib.cca_prefill_host_workspace_size.argtypes = [pp]
         lib.cca_prefill_host_workspace_size.restype = ctypes.c_uint64
+        lib.cca_decode_kernels.argtypes = [pp, ctypes.c_int]
+        lib.cca_decode_kernels.restype = ctypes.c_int
         lib.cca_decode_workspace_size.argtypes = [pp]
         lib.cca_decode_workspace_size.restype = ctypes.c_uint64
         lib.cca_pool_group.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, pp, vp]
@@ -99,6 +103,8 @@ def load_library():
         lib.cca_test_set_wait_limit_ns.restype = None
         lib.cca_test_skip_q_load.argtypes = [ctypes.c_int]
         lib.cca_test_skip_q_load.restype = None
+        lib.cca_test_decode_path.argtypes = [ctypes.c_int]
+        lib.cca_test_decode_path.restype = None
         _lib = lib
         return lib
 
@@ -257,6 +263,15 @@ def causal_attention(Q, K, V, scale: float = 0.0, O=None, LSE=None, stream=None)
 def decode_workspace_size(B, Hq, Hkv, Ncap, d, g, w, dtype) -> int:
     prm = make_params(B, Hq, Hkv, Ncap, d, g, w, _DTYPE[dtype])
     return int(load_library().cca_decode_workspace_size(ctypes.byref(prm)))
+
+
+def decode_kernels(B, Hq, Hkv, Ncap, d, g, w, dtype, pos: int, window_mode: int = 0) -> int:
+    """Kernels one cca_decode_fwd call at `pos` launches on the current device (1 or 2)."""
+    prm = make_params(B, Hq, Hkv, Ncap, d, g, w, _DTYPE[dtype], window_mode=window_mode)
+    n = int(load_library().cca_decode_kernels(ctypes.byref(prm), int(pos)))
+    if n < 0:
+        raise CcaError(n, "cca_decode_kernels")
+    return n
 
 
 def cca_decode_fwd(q, K, V, Kc, Vc, pos: int, g: int, w: int, O=None, LSE=None, workspace=None,

@@ -12,6 +12,7 @@
 namespace cca {
 extern unsigned long long g_wait_limit_ns;
 extern int g_skip_q_load;
+extern int g_decode_path;
 }  // namespace cca
 
 static_assert(cca::DECODE_NOALLOC_MAX_BYTES == CCA_DECODE_NOALLOC_MAX_BYTES, "scratch size mismatch");
@@ -204,6 +205,17 @@ uint64_t cca_prefill_bwd_workspace_size(const cca_params_t *params) {
     return cca::prefill_bwd_workspace_bytes(to_shape(params));
 }
 
+int cca_decode_kernels(const cca_params_t *params, int pos) {
+    int st = check_shape(params, true);
+    if (st != CCA_OK) return st;
+    if (pos < 0 || pos >= params->N) return CCA_ERR_INVALID_ARG;
+    if ((st = check_device()) != CCA_OK) return st;
+    int n = 0;
+    st = from_cuda(cca::launch_decode(params->dtype, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+                                      to_shape(params), pos, nullptr, nullptr, &n));
+    return st != CCA_OK ? st : n;
+}
+
 uint64_t cca_decode_workspace_size(const cca_params_t *params) {
     if (check_shape(params, true) != CCA_OK) return 0;
     return cca::decode_workspace_bytes(to_shape(params));
@@ -265,5 +277,6 @@ int cca_abi_version(void) { return CCA_ABI_VERSION; }
 // the MMA issuer's first wait runs out.  Not part of the public header.
 void cca_test_set_wait_limit_ns(unsigned long long ns) { cca::g_wait_limit_ns = ns; }
 void cca_test_skip_q_load(int on) { cca::g_skip_q_load = on ? 1 : 0; }
+void cca_test_decode_path(int path) { cca::g_decode_path = (path == 1 || path == 2) ? path : 0; }
 
 }  // extern "C"

@@ -28,6 +28,13 @@ constexpr unsigned kFull = 0xffffffffu;
 constexpr int DEC_WARPS = 4;
 constexpr int MIN_KEYS_PER_SPLIT = 64;
 constexpr int MAX_SPLITS = 64;
+}  // namespace
+
+// Decode path test hook: 0 automatic, 1 always the split + merge kernels, 2 the
+// one-launch cluster merge wherever a cluster of two or more splits fits.
+int g_decode_path = 0;
+
+namespace {
 
 template <typename T>
 struct Vec;
@@ -75,11 +82,14 @@ struct DecodeArgs {
 };
 
 // Partials: ws[((b*Hq + h) * MAX_SPLITS + s) * (D + 2) + {0..D-1: o, D: m, D+1: l}]
-template <typename T, int D, int R>
+// CL: the splits of one (b, kv) form a thread-block cluster and merge in it (O, LSE written
+// by the cluster's first CTA from the others' shared memory; no workspace, no second kernel).
+template <typename T, int D, int R, bool CL>
 __global__ void __launch_bounds__(DEC_WARPS * 32, R == 1 ? 4 : 1) decode_split_kernel(const T *__restrict__ Q, const T *__restrict__ K,
                                                                       const T *__restrict__ V,
                                                                       const T *__restrict__ Kc,
                                                                       const T *__restrict__ Vc, float *__restrict__ ws,
+                                                                      T *__restrict__ Oout, float *__restrict__ LSEout,
                                                                       const DecodeArgs a) {
     using VT = Vec<T>;
     constexpr int E = VT::E;
@@ -94,7 +104,9 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, R == 1 ? 4 : 1) decode_split_k
     // completion first, before they read anything or signal their own dependent.
     asm volatile("griddepcontrol.wait;" ::: "memory");
     // The merge kernel may be scheduled now: it waits for this grid's completion itself.
-    asm volatile("griddepcontrol.launch_dependents;");
+    // (With the in-cluster merge there is no merge kernel, and the grid signals nothing: a
+    // dependent then starts as this grid completes.)
+    if constexpr (!CL) asm volatile("griddepcontrol.launch_dependents;");
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int sub = lane / LPR, cl = lane % LPR;
     const int s = blockIdx.x;
@@ -226,6 +238,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, R == 1 ? 4 : 1) decode_split_k
     }
     __syncthreads();
     // merge the warps and write this split's partial for each query head
+    __shared__ float sm_part[CL ? R : 1][CL ? D + 2 : 1];
     for (int idx = threadIdx.x; idx < R * D; idx += blockDim.x) {
         const int r = idx / D, c = idx % D;
         float mx = -INFINITY;
@@ -238,12 +251,46 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, R == 1 ? 4 : 1) decode_split_k
             acc += sm_o[w][r][c] * f;
             lsum += sm_l[w][r] * f;
         }
-        float *dst = ws + ((static_cast<int64_t>(b) * a.Hq + kv * R + r) * MAX_SPLITS + s) * (D + 2);
+        float *dst = CL ? &sm_part[r][0]
+                        : ws + ((static_cast<int64_t>(b) * a.Hq + kv * R + r) * MAX_SPLITS + s) * (D + 2);
         dst[c] = acc;
         if (c == 0) {
             dst[D] = mx;
             dst[D + 1] = lsum;
         }
+    }
+    if constexpr (CL) {
+        // Every CTA of the cluster has its partial in shared memory after this barrier; the
+        // first CTA reads them all (distributed shared memory) and writes O and LSE.  The
+        // second barrier keeps the others resident until it has read them.  Every CTA of the
+        // cluster reaches both barriers (a CTA with an empty slice has m = -inf, l = 0).
+        ptx::cluster_sync();
+        if (blockIdx.x == 0) {
+            const int splits = a.splits;
+            const uint32_t base = ptx::smem_addr(&sm_part[0][0]);
+            for (int idx = threadIdx.x; idx < R * D; idx += blockDim.x) {
+                const int r = idx / D, c = idx % D;
+                const uint32_t row = base + static_cast<uint32_t>(r * (D + 2)) * 4u;
+                float mx = -INFINITY;
+                for (int q = 0; q < splits; ++q) mx = fmaxf(mx, ptx::ld_dsmem_f32(row + D * 4u, q));
+                float acc = 0.f, lsum = 0.f;
+                for (int q = 0; q < splits; ++q) {
+                    const float mq = ptx::ld_dsmem_f32(row + D * 4u, q);
+                    const float f = (mq == -INFINITY) ? 0.f : ptx::ex2(mq - mx);
+                    acc = fmaf(ptx::ld_dsmem_f32(row + static_cast<uint32_t>(c) * 4u, q), f, acc);
+                    lsum = fmaf(ptx::ld_dsmem_f32(row + (D + 1) * 4u, q), f, lsum);
+                }
+                const int64_t bh = static_cast<int64_t>(b) * a.Hq + kv * R + r;
+                const float val = acc / lsum;
+                if constexpr (sizeof(T) == 2) {
+                    Oout[bh * D + c] = __float2bfloat16_rn(val);
+                } else {
+                    Oout[bh * D + c] = val;
+                }
+                if (c == 0) LSEout[bh] = (mx + __log2f(lsum)) * 0.6931471805599453f;
+            }
+        }
+        ptx::cluster_sync();
     }
 }
 
@@ -520,7 +567,8 @@ cudaError_t split_occupancy(int &sms, int &occ) {
     if (!x.ready) {
         x.err = cudaDeviceGetAttribute(&x.sms, cudaDevAttrMultiProcessorCount, dev);
         if (x.err == cudaSuccess)
-            x.err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&x.occ, decode_split_kernel<T, D, R>, DEC_WARPS * 32, 0);
+            x.err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&x.occ, decode_split_kernel<T, D, R, false>,
+                                                                  DEC_WARPS * 32, 0);
         x.ready = true;
     }
     sms = x.sms;
@@ -528,9 +576,51 @@ cudaError_t split_occupancy(int &sms, int &occ) {
     return x.err;
 }
 
+// Largest cluster of split CTAs (one (b, kv) each) that the device schedules for this
+// instantiation: 16 with the non-portable size allowed, else 8 (queried once per device;
+// 0 when clusters cannot be used).
+template <typename T, int D, int R>
+int max_split_cluster() {
+    struct Info {
+        bool ready = false;
+        int size = 0;
+    };
+    static Info info[64];
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    Info &x = info[dev & 63];
+    if (!x.ready) {
+        x.ready = true;
+        auto kern = decode_split_kernel<T, D, R, true>;
+        cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        for (int size : {16, 8}) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(size, 1);
+            cfg.blockDim = dim3(DEC_WARPS * 32);
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = size;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n > 0) {
+                x.size = size;
+                break;
+            }
+        }
+        cudaGetLastError();  // a refused query leaves no error behind
+    }
+    return x.size;
+}
+
 template <typename T, int D, int R>
 cudaError_t launch_decode_typed(const void *Q, const void *K, const void *V, const void *Kc, const void *Vc, void *O,
-                                float *LSE, const Shape &s, int pos, float *ws, cudaStream_t stream) {
+                                float *LSE, const Shape &s, int pos, float *ws, cudaStream_t stream,
+                                int *plan_kernels) {
     DecodeArgs a;
     a.Hq = s.Hq;
     a.Hkv = s.Hkv;
@@ -545,22 +635,50 @@ cudaError_t launch_decode_typed(const void *Q, const void *K, const void *V, con
     if (oe != cudaSuccess) return oe;
     a.splits = decode_splits(a.L, s.B * s.Hkv, sms, occ);
     a.scale_log2 = s.scale * 1.4426950408889634f;
+    const int n_bk = s.B * s.Hkv;
     // Both kernels are programmatic dependent launches: each is scheduled as the grid before
     // it on the stream drains, instead of after it, and orders itself with griddepcontrol.wait
     // (the split kernel on whatever preceded the call, the merge on the split kernel).
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(a.splits, s.B * s.Hkv);
     cfg.blockDim = dim3(DEC_WARPS * 32);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, decode_split_kernel<T, D, R>, static_cast<const T *>(Q),
+    // One launch when a cluster per (b, kv) still gives about a full wave of CTAs and every
+    // split has at least 256 keys: the splits merge inside their cluster, which saves the
+    // merge kernel's hand-off (128K MHA: 28.1 -> 27.3 us per layer).  Otherwise the partials
+    // go through the workspace to the merge kernel: with few (b, kv) pairs, which want more
+    // splits than a cluster holds, and with short lists, where the 19 splits per (b, kv) of
+    // a full wave beat a cluster's 16 (32K MHA: 12.3 against 12.7 us per layer).
+    const int csize = g_decode_path == 1 ? 0 : max_split_cluster<T, D, R>();
+    const int cl_splits = a.splits < csize ? a.splits : csize;
+    const bool fills = 4 * n_bk * cl_splits >= 3 * occ * sms && a.L >= 256 * cl_splits;
+    const bool clustered = cl_splits >= 2 && (g_decode_path == 2 || fills);
+    if (plan_kernels != nullptr) {  // the plan only: how many kernels the call launches
+        *plan_kernels = clustered ? 1 : 2;
+        return cudaSuccess;
+    }
+    if (clustered) {
+        a.splits = cl_splits;
+        cfg.gridDim = dim3(a.splits, n_bk);
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = a.splits;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
+        return cudaLaunchKernelEx(&cfg, decode_split_kernel<T, D, R, true>, static_cast<const T *>(Q),
+                                  static_cast<const T *>(K), static_cast<const T *>(V), static_cast<const T *>(Kc),
+                                  static_cast<const T *>(Vc), ws, static_cast<T *>(O), LSE, a);
+    }
+    cfg.gridDim = dim3(a.splits, n_bk);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, decode_split_kernel<T, D, R, false>, static_cast<const T *>(Q),
                                        static_cast<const T *>(K), static_cast<const T *>(V),
-                                       static_cast<const T *>(Kc), static_cast<const T *>(Vc), ws, a);
+                                       static_cast<const T *>(Kc), static_cast<const T *>(Vc), ws,
+                                       static_cast<T *>(O), LSE, a);
     if (e != cudaSuccess) return e;
     cfg.gridDim = dim3(s.B * s.Hq);
     cfg.blockDim = dim3(D);
@@ -570,12 +688,12 @@ cudaError_t launch_decode_typed(const void *Q, const void *K, const void *V, con
 
 template <typename T, int D>
 cudaError_t dispatch_r(const void *Q, const void *K, const void *V, const void *Kc, const void *Vc, void *O,
-                       float *LSE, const Shape &s, int pos, float *ws, cudaStream_t stream) {
+                       float *LSE, const Shape &s, int pos, float *ws, cudaStream_t stream, int *plan_kernels) {
     switch (s.Hq / s.Hkv) {
-        case 1: return launch_decode_typed<T, D, 1>(Q, K, V, Kc, Vc, O, LSE, s, pos, ws, stream);
-        case 2: return launch_decode_typed<T, D, 2>(Q, K, V, Kc, Vc, O, LSE, s, pos, ws, stream);
-        case 4: return launch_decode_typed<T, D, 4>(Q, K, V, Kc, Vc, O, LSE, s, pos, ws, stream);
-        case 8: return launch_decode_typed<T, D, 8>(Q, K, V, Kc, Vc, O, LSE, s, pos, ws, stream);
+        case 1: return launch_decode_typed<T, D, 1>(Q, K, V, Kc, Vc, O, LSE, s, pos, ws, stream, plan_kernels);
+        case 2: return launch_decode_typed<T, D, 2>(Q, K, V, Kc, Vc, O, LSE, s, pos, ws, stream, plan_kernels);
+        case 4: return launch_decode_typed<T, D, 4>(Q, K, V, Kc, Vc, O, LSE, s, pos, ws, stream, plan_kernels);
+        case 8: return launch_decode_typed<T, D, 8>(Q, K, V, Kc, Vc, O, LSE, s, pos, ws, stream, plan_kernels);
         default: return cudaErrorNotSupported;
     }
 }
@@ -637,13 +755,14 @@ uint64_t decode_workspace_bytes(const Shape &s) {
 }
 
 cudaError_t launch_decode(int dtype, const void *Q, const void *K, const void *V, const void *Kc, const void *Vc,
-                          void *O, float *LSE, const Shape &s, int pos, float *ws, cudaStream_t stream) {
+                          void *O, float *LSE, const Shape &s, int pos, float *ws, cudaStream_t stream,
+                          int *plan_kernels) {
     if (dtype == 0) {
-        if (s.d == 128) return dispatch_r<__nv_bfloat16, 128>(Q, K, V, Kc, Vc, O, LSE, s, pos, ws, stream);
-        if (s.d == 64) return dispatch_r<__nv_bfloat16, 64>(Q, K, V, Kc, Vc, O, LSE, s, pos, ws, stream);
+        if (s.d == 128) return dispatch_r<__nv_bfloat16, 128>(Q, K, V, Kc, Vc, O, LSE, s, pos, ws, stream, plan_kernels);
+        if (s.d == 64) return dispatch_r<__nv_bfloat16, 64>(Q, K, V, Kc, Vc, O, LSE, s, pos, ws, stream, plan_kernels);
     } else {
-        if (s.d == 128) return dispatch_r<float, 128>(Q, K, V, Kc, Vc, O, LSE, s, pos, ws, stream);
-        if (s.d == 64) return dispatch_r<float, 64>(Q, K, V, Kc, Vc, O, LSE, s, pos, ws, stream);
+        if (s.d == 128) return dispatch_r<float, 128>(Q, K, V, Kc, Vc, O, LSE, s, pos, ws, stream, plan_kernels);
+        if (s.d == 64) return dispatch_r<float, 64>(Q, K, V, Kc, Vc, O, LSE, s, pos, ws, stream, plan_kernels);
     }
     return cudaErrorNotSupported;
 }

@@ -39,8 +39,11 @@ cudaError_t launch_attn_bf16_tc(const void *Q, const void *K, const void *V, con
 
 // Decode step (row `pos` of the fused attention over the caches) and single-group pooling.
 uint64_t decode_workspace_bytes(const Shape &s);
+// With plan_kernels set, nothing is launched: *plan_kernels receives the number of kernels
+// the call would launch (1: the splits merge inside thread-block clusters; 2: split + merge).
 cudaError_t launch_decode(int dtype, const void *Q, const void *K, const void *V, const void *Kc, const void *Vc,
-                          void *O, float *LSE, const Shape &s, int pos, float *ws, cudaStream_t stream);
+                          void *O, float *LSE, const Shape &s, int pos, float *ws, cudaStream_t stream,
+                          int *plan_kernels = nullptr);
 // Fixed scratch of the no-allocation decode entry point (bytes) and its device address
 // on the current device (looked up on first use per device).
 constexpr uint64_t DECODE_NOALLOC_MAX_BYTES = 4ull << 20;

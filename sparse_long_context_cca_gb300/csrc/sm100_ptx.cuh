@@ -356,6 +356,20 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// All threads of every CTA of the cluster: arrive (release) and wait (acquire).
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// fp32 load from the shared memory of CTA `rank` of this cluster, at the offset that
+// `local` (a shared::cta address) has in this CTA.
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t local, uint32_t rank) {
+    uint32_t remote;
+    float v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
+}
+
 // 32-byte global store (one full sector per thread); addr must be 32-byte aligned.
 __device__ __forceinline__ void st_global_v8(void *addr, const uint32_t (&v)[8]) {
     asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(addr), "r"(v[0]), "r"(v[1]),

@@ -211,3 +211,11 @@ def test_rows_window_mode_moves_the_first_raw_token(lib):
     # with window_mode 1, row 500's window starts at the group boundary 400, so K/V from 401
     # leave a token out: rejected (with window_mode 0 the same range would be valid)
     assert call_rows(lib, 500, 10, 401, 109, window_mode=1) == api.CCA_ERR_INVALID_ARG
+
+
+def test_decode_kernels_rejects_bad_arguments(lib):
+    prm = api.make_params(1, 2, 2, 256, 128, 16, 32, api.CCA_BF16)
+    assert lib.cca_decode_kernels(ctypes.byref(prm), 256) == api.CCA_ERR_INVALID_ARG
+    assert lib.cca_decode_kernels(ctypes.byref(prm), -1) == api.CCA_ERR_INVALID_ARG
+    bad = api.make_params(1, 2, 2, 250, 128, 16, 32, api.CCA_BF16)
+    assert lib.cca_decode_kernels(ctypes.byref(bad), 5) == api.CCA_ERR_INVALID_ARG

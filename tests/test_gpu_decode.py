@@ -191,3 +191,43 @@ def test_chained_steps_wait_for_the_step_before(graphed):
                               layers[0][2], layers[0][3], w.g, w.w,
                               [(0, h, pos) for h in range(w.Hq)])
     check_out(ref[0][0].reshape(-1, w.d), ref[0][1].reshape(-1), Oa, La, torch.bfloat16, "chained layer 0")
+
+
+@pytest.fixture
+def decode_path():
+    lib = api.load_library()
+    yield lambda path: lib.cca_test_decode_path(path)
+    lib.cca_test_decode_path(0)
+
+
+@pytest.mark.parametrize("path", [1, 2], ids=["split+merge", "cluster"])
+@pytest.mark.parametrize("w", [CASES[0], CASES[1], CASES[3], CASES[4], CASES[6]], ids=lambda w: w.name)
+def test_both_decode_paths_match_oracle(w, path, decode_path):
+    """The two ways the splits are merged: through the workspace by a second kernel, or
+    inside a thread-block cluster by the first CTA (one launch)."""
+    decode_path(path)
+    Q, K, V = make_qkv(w, "cuda")
+    Kc, Vc = api.cca_pool(Q, K, V, w.g)
+    for pos in (w.N - 1, w.N // 2, w.w + 3, 5):
+        q = Q[:, :, pos].contiguous()
+        O, LSE = api.cca_decode_fwd(q, K, V, Kc, Vc, pos, w.g, w.w)
+        O2, L2 = api.cca_decode_fwd(q, K, V, Kc, Vc, pos, w.g, w.w)
+        torch.cuda.synchronize()
+        assert torch.equal(O, O2) and torch.equal(LSE, L2)
+        rows = [(b, h, pos) for b in range(w.B) for h in range(w.Hq)]
+        Oa, La = oracle.attn_rows(Q, K, V, Kc, Vc, w.g, w.w, rows)
+        check_out(O.reshape(-1, w.d), LSE.reshape(-1), Oa, La, Q.dtype, f"{w.name} pos {pos} path {path}")
+
+
+def test_decode_kernel_count(decode_path):
+    """The call says how many kernels it launches: one where the splits merge inside their
+    cluster (the 128K caches of 32 heads), two where a merge kernel follows (the 32K ones,
+    and grouped-query heads with few (b, kv) pairs)."""
+    bf = torch.bfloat16
+    assert api.decode_kernels(1, 32, 32, 131072, 128, 16, 1024, bf, 131071) == 1
+    assert api.decode_kernels(1, 32, 32, 32768, 128, 16, 1024, bf, 32767) == 2
+    assert api.decode_kernels(1, 32, 8, 65536, 128, 16, 1024, bf, 65535) == 2
+    decode_path(1)
+    assert api.decode_kernels(1, 32, 32, 131072, 128, 16, 1024, bf, 131071) == 2
+    decode_path(2)
+    assert api.decode_kernels(1, 32, 32, 32768, 128, 16, 1024, bf, 32767) == 1
