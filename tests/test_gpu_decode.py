@@ -115,7 +115,17 @@ def test_pool_group_variants(pool_mode):
     check_cores(Kg, Vg, Kr, Vr, Q.dtype, f"pool_group mode {pool_mode}")
 
 
-def test_decode_group_aligned_window():
+@pytest.mark.parametrize("path", [0, 2], ids=["auto", "cluster"])
+def test_decode_group_aligned_window(path):
+    lib = api.load_library()
+    lib.cca_test_decode_path(path)
+    try:
+        _decode_group_aligned_window()
+    finally:
+        lib.cca_test_decode_path(0)
+
+
+def _decode_group_aligned_window():
     w = wl(1, 4, 2, 2048, 128, 16, 300)
     Q, K, V = make_qkv(w, "cuda")
     Kc, Vc = api.cca_pool(Q, K, V, w.g)
@@ -201,7 +211,7 @@ def decode_path():
 
 
 @pytest.mark.parametrize("path", [1, 2], ids=["split+merge", "cluster"])
-@pytest.mark.parametrize("w", [CASES[0], CASES[1], CASES[3], CASES[4], CASES[6]], ids=lambda w: w.name)
+@pytest.mark.parametrize("w", [CASES[0], CASES[1], CASES[3], CASES[4], CASES[5], CASES[6]], ids=lambda w: w.name)
 def test_both_decode_paths_match_oracle(w, path, decode_path):
     """The two ways the splits are merged: through the workspace by a second kernel, or
     inside a thread-block cluster by the first CTA (one launch)."""
