@@ -188,6 +188,21 @@ def job_throughput(total_ms: float, steps: int, tokens_per_rank_step: int, world
     return ms_per_step, tokens_per_rank_step * world / (ms_per_step / 1e3)
 
 
+def nvtx_push(name: str):
+    """Names the enclosed host region for a timeline profiler (NVTX); a no-op without one."""
+    try:
+        torch.cuda.nvtx.range_push(name)
+    except Exception:
+        pass
+
+
+def nvtx_pop():
+    try:
+        torch.cuda.nvtx.range_pop()
+    except Exception:
+        pass
+
+
 def time_steps(fn, steps, stream):
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
@@ -266,10 +281,12 @@ def run_cca(args, rank, world, local):
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         h0 = time.monotonic()
+        nvtx_push(f"timed prefill steps: {wl.name}")
         t0.record(stream)
         for k in range(steps):
             step(ev[k])
         t1.record(stream)
+        nvtx_pop()
         torch.cuda.synchronize()
         h1 = time.monotonic()
         if world > 1:
@@ -407,6 +424,7 @@ def decode_bench(wl, dev, stream, iters, peaks):
         api.cca_decode_fwd(q, K, V, Kc, Vc, pos, wl.g, wl.w, O, LSE, ws, stream=stream)
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+    nvtx_push(f"timed decode steps: {wl.name}")
     with torch.cuda.stream(stream):
         for e0, e1 in ev:
             flush.fill_(1)
@@ -414,6 +432,7 @@ def decode_bench(wl, dev, stream, iters, peaks):
             e0.record(stream)
             api.cca_decode_fwd(q, K, V, Kc, Vc, pos, wl.g, wl.w, O, LSE, ws, stream=stream)
             e1.record(stream)
+    nvtx_pop()
     torch.cuda.synchronize()
     step_us = sorted(e0.elapsed_time(e1) * 1e3 for e0, e1 in ev)
     us = sum(step_us) / len(step_us)
@@ -475,10 +494,12 @@ def decode_layers_bench(wl, dev, n_layers, replays, peaks):
                for (_, _, _, _, _, O, LSE, _), r in zip(layers, ref))
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(replays)]
     cur = torch.cuda.current_stream()
+    nvtx_push(f"timed decode graph replays ({n_layers} layers): {wl.name}")
     for e0, e1 in ev:
         e0.record(cur)
         graph.replay()
         e1.record(cur)
+    nvtx_pop()
     torch.cuda.synchronize()
     rep_us = sorted(e0.elapsed_time(e1) * 1e3 for e0, e1 in ev)
     us = rep_us[len(rep_us) // 2] / n_layers
@@ -508,11 +529,13 @@ def backward_bench(wl, dev, stream, iters, peaks):
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    nvtx_push(f"timed backward: {wl.name}")
     e0.record(stream)
     for _ in range(iters):
         api.cca_prefill_bwd(Q, K, V, Kc, Vc, O, LSE, dO, wl.g, wl.w, dQ=grads[0], dK=grads[1], dV=grads[2],
                             stream=stream)
     e1.record(stream)
+    nvtx_pop()
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / iters
     flops = 2.5 * W.attn_flops(wl)
