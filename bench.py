@@ -365,6 +365,13 @@ def run_cca(args, rank, world, local):
                                                  "averaged over the 4 heads sharing a KV head")]
         out["gqa64k"] = [x for x in rows if x is not None]
         out["sweep"] = [row(w3) for w3 in W.sweep()]
+        # the tiny fp32 workload (the parity configuration): fp32 attention runs on CUDA cores
+        # (a 1e-4 output tolerance rules out tf32 tensor cores); 256 tokens are launch-bound
+        tot, pm, am, n, win = measure(W.TINY_F32, None, 3)
+        out["tiny_f32"] = {"workload": W.TINY_F32.name, "steps": n, "warmup": 3, "us_per_step": tot / n * 1e3,
+                           "tokens_per_s": W.TINY_F32.B * W.TINY_F32.N / (tot / n / 1e3),
+                           "pool_us": pm * 1e3, "attn_us": am * 1e3, "clocks": sampler.summary(win),
+                           "note": "fp32 on CUDA cores; at 256 tokens each kernel is bound by its launch"}
     if args.decode:
         out["decode"] = decode_bench(wl, dev, stream, 50, peaks)
         if args.also_128k and wl is not W.MHA_128K:
