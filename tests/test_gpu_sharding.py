@@ -71,14 +71,16 @@ def test_shards_equal_unsharded(case):
 
 
 def test_rows_of_a_window_inside_one_tile():
-    """A shard of a single row, and one whose halo starts inside its first key tile."""
+    """A single row, and rows whose halo starts inside their first key tile; K/V holding
+    exactly the rows' windows, or the whole sequence."""
     w = wl(1, 2, 2, 1024, 128, 16, 200)
     Q, K, V = make_qkv(w, "cuda")
     Ou, Lu, Kc, Vc = api.cca_prefill(Q, K, V, w.g, w.w)
     for q0, n in ((517, 1), (300, 77), (1023, 1)):
-        kv0 = max(0, q0 - w.w + 1)
-        O, L = api.cca_attn_fwd_rows(_slice(Q, q0, q0 + n), _slice(K, kv0, q0 + n), _slice(V, kv0, q0 + n),
-                                     Kc, Vc, w.g, w.w, w.N, q0, kv0)
-        torch.cuda.synchronize()
-        check_out(O, L, oracle.widen(Ou[:, :, q0:q0 + n]), oracle.widen(Lu[:, :, q0:q0 + n]), Q.dtype,
-                  f"rows {q0}+{n}")
+        # the exact halo, and K/V from the sequence start through its end (more than needed)
+        for kv0, kv1 in ((max(0, q0 - w.w + 1), q0 + n), (0, w.N)):
+            O, L = api.cca_attn_fwd_rows(_slice(Q, q0, q0 + n), _slice(K, kv0, kv1), _slice(V, kv0, kv1),
+                                         Kc, Vc, w.g, w.w, w.N, q0, kv0)
+            torch.cuda.synchronize()
+            check_out(O, L, oracle.widen(Ou[:, :, q0:q0 + n]), oracle.widen(Lu[:, :, q0:q0 + n]), Q.dtype,
+                      f"rows {q0}+{n}, K/V [{kv0}, {kv1})")
