@@ -384,7 +384,11 @@ def run_cca(args, rank, world, local):
             out["decode_gqa64k"] = decode_bench(W.GQA_64K, dev, stream, 50, peaks)
             out["decode_layers_gqa64k"] = decode_layers_bench(W.GQA_64K, dev, 16, 20, peaks)
     if args.backward:
-        out["backward"] = backward_bench(wl, dev, stream, 2, peaks)
+        bw = backward_bench(wl, dev, stream, 10, peaks)
+        bw["clocks"] = sampler.summary(bw.pop("window"))
+        bp, bp_src = tensor_peak(peaks, peak_src, bw["clocks"])
+        bw["frac"], bw["peak"], bw["peak_source"] = bw["eff_tflops"] / bp, bp, bp_src
+        out["backward"] = bw
     if args.comparator:
         out["full_attention_comparator"] = comparator(wl, dev, stream, max(3, args.steps // 4), ms_per_step)
         # the same comparison at the other context lengths the pages compare (each against its
@@ -533,10 +537,14 @@ def backward_bench(wl, dev, stream, iters, peaks):
     O, LSE, Kc, Vc = api.cca_prefill(Q, K, V, wl.g, wl.w, stream=stream)
     dO = torch.randn(Q.shape, device=dev, generator=torch.Generator(device=dev).manual_seed(5)).to(Q.dtype)
     grads = api.cca_prefill_bwd(Q, K, V, Kc, Vc, O, LSE, dO, wl.g, wl.w, stream=stream)
+    for _ in range(2):  # warm-up
+        api.cca_prefill_bwd(Q, K, V, Kc, Vc, O, LSE, dO, wl.g, wl.w, dQ=grads[0], dK=grads[1], dV=grads[2],
+                            stream=stream)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     nvtx_push(f"timed backward: {wl.name}")
+    h0 = time.monotonic()
     e0.record(stream)
     for _ in range(iters):
         api.cca_prefill_bwd(Q, K, V, Kc, Vc, O, LSE, dO, wl.g, wl.w, dQ=grads[0], dK=grads[1], dV=grads[2],
@@ -544,6 +552,7 @@ def backward_bench(wl, dev, stream, iters, peaks):
     e1.record(stream)
     nvtx_pop()
     torch.cuda.synchronize()
+    h1 = time.monotonic()
     ms = e0.elapsed_time(e1) / iters
     flops = 2.5 * W.attn_flops(wl)
     del Q, K, V, O, LSE, Kc, Vc, dO, grads
@@ -555,7 +564,7 @@ def backward_bench(wl, dev, stream, iters, peaks):
             "ms": ms, "eff_tflops": eff,
             "frac_of_bf16_burst": eff / peaks["bf16_tflops"] if peaks.get("bf16_tflops") else None,
             "algorithmic_unit": "10*d FLOP per (query, visible key, head): q.k, dO.v, dQ, dK, dV",
-            "kernel_launches": 4}
+            "kernel_launches": 4, "iterations": iters, "warmup": 3, "window": (h0, h1)}
 
 
 def comparator(wl, dev, stream, steps, cca_ms_per_step):
