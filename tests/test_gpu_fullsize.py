@@ -77,3 +77,30 @@ def test_mha_1m_tokens():
     from sparse_long_context_cca_gb300.workloads import Workload
     wl = Workload("mha B1 H2 d128 N1048576 g16 w1024", 1, 2, 2, 1 << 20, 128, 16, 1024, "bf16", 31, 0.01)
     check_workload(wl, [(0, 0), (0, 1)], n_random=24)
+
+
+@pytest.mark.parametrize("wl", [MHA_32K, MHA_128K, GQA_64K], ids=lambda w: w.name)
+def test_decode_full_size(wl):
+    """The decode step at the full workload sizes, in the benchmark's launch configuration
+    (at 128K the one-launch cluster merge, at 32K and GQA 64K the split + merge kernels):
+    the last position and the middle one, all heads, against the prefill's own rows and,
+    for a few heads, against the fp64 oracle over the GPU's core tokens."""
+    torch.cuda.empty_cache()
+    Q, K, V = make_qkv(wl, "cuda")
+    O, LSE, Kc, Vc = api.cca_prefill(Q, K, V, wl.g, wl.w)
+    r = wl.Hq // wl.Hkv
+    for pos in (wl.N - 1, wl.N // 2 + 5):
+        q = Q[:, :, pos].contiguous()
+        Od, Ld = api.cca_decode_fwd(q, K, V, Kc, Vc, pos, wl.g, wl.w)
+        torch.cuda.synchronize()
+        a, b = Od.float(), O[:, :, pos].float()
+        assert (a - b).abs().max().item() <= 2e-2 * b.abs().max().item(), pos
+        assert (Ld - LSE[:, :, pos]).abs().max().item() <= 5e-3, pos
+        for h in (0, wl.Hq - 1):
+            kv = h // r
+            Or, Lr = oracle.attn_rows(Q[:, h:h + 1], K[:, kv:kv + 1], V[:, kv:kv + 1], Kc[:, kv:kv + 1],
+                                      Vc[:, kv:kv + 1], wl.g, wl.w, [(0, 0, pos)])
+            err = np.abs(oracle.widen(Od[0, h]) - Or[0])
+            assert err.max() <= BF16_O_MAX_REL * np.abs(Or).max(), (pos, h, err.max())
+            assert abs(float(Ld[0, h]) - Lr[0]) <= BF16_LSE, (pos, h)
+    del Q, K, V, O, LSE, Kc, Vc
