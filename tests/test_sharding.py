@@ -136,3 +136,73 @@ def test_a_short_halo_is_caught():
     O_ref, _, _, _ = _reference(case)
     diffs = [np.abs(O[n] - O_ref[b, h, i]).max() for _, rows, O, _, _ in out for n, (b, h, i) in enumerate(rows)]
     assert max(diffs) > 1e-6
+
+
+def _oracle_kernels(api):
+    """CPU stand-ins for the two library calls shard_prefill makes, written from their ABI
+    definitions with the oracle (test infrastructure: the GPU test runs the real kernels)."""
+    import oracle
+
+    def cca_pool(Q, K, V, g, scale=0.0, pool_mode=0, **_):
+        kc, vc = oracle.pool(Q, K, V, g, pool_mode=pool_mode)
+        return torch.from_numpy(kc), torch.from_numpy(vc)
+
+    def cca_attn_fwd_rows(Q, K, V, Kc, Vc, g, w, N, q_off, kv_off, scale=0.0, window_mode=0, **_):
+        B, Hq, n_q, d = Q.shape
+        Hkv, n_kv = K.shape[1], K.shape[2]
+        # rows and raw tokens at their sequence positions; the rest stays zero, so a call that
+        # reached outside what it was given would show
+        Qg = torch.zeros((B, Hq, N, d), dtype=torch.float64)
+        Kg = torch.zeros((B, Hkv, N, d), dtype=torch.float64)
+        Vg = torch.zeros_like(Kg)
+        Qg[:, :, q_off:q_off + n_q] = Q
+        Kg[:, :, kv_off:kv_off + n_kv] = K
+        Vg[:, :, kv_off:kv_off + n_kv] = V
+        rows = [(b, h, i) for b in range(B) for h in range(Hq) for i in range(q_off, q_off + n_q)]
+        O, L = oracle.attn_rows(Qg, Kg, Vg, Kc, Vc, g, w, rows, window_mode=window_mode)
+        return (torch.from_numpy(O).reshape(B, Hq, n_q, d), torch.from_numpy(L).reshape(B, Hq, n_q))
+
+    api.cca_pool = cca_pool
+    api.cca_attn_fwd_rows = cca_attn_fwd_rows
+
+
+def _shard_prefill_worker(rank, world, port, case, q):
+    from sparse_long_context_cca_gb300 import api
+    from sparse_long_context_cca_gb300.inputs import make_qkv
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        _oracle_kernels(api)
+        B, Hq, Hkv, N, d, g, w, wm, _ = case
+        wl = Workload("shard", B, Hq, Hkv, N, d, g, w, "f32", 77, 0.05)
+        Qf, Kf, Vf = (t.double() for t in make_qkv(wl, "cpu"))
+        shards = sharding.plan(N, g, w, world, wm)
+        me = shards[rank]
+        Q, K, V = (t[:, :, me.q0:me.q1].contiguous() for t in (Qf, Kf, Vf))
+        O, L, _, _ = sharding.shard_prefill(Q, K, V, shards, g, w, N, window_mode=wm)
+        q.put((rank, me.q0, O.numpy(), L.numpy()))
+    finally:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("case", [CASES[1], CASES[2]], ids=lambda c: "B{}Hq{}Hkv{}N{}d{}g{}w{}m{}x{}".format(*c))
+def test_shard_prefill_wiring(case):
+    """sharding.shard_prefill itself (pool its groups, gather, exchange, attend its rows with
+    the right offsets), with the two library calls replaced by their oracle definitions."""
+    world = case[-1]
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_shard_prefill_worker, args=(r, world, port, case, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    out = [q.get(timeout=240) for _ in range(world)]
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    O_ref, L_ref, _, _ = _reference(case)
+    for rank, q0, O, L in out:
+        n = O.shape[2]
+        np.testing.assert_array_equal(O, O_ref[:, :, q0:q0 + n])
+        np.testing.assert_array_equal(L, L_ref[:, :, q0:q0 + n])
