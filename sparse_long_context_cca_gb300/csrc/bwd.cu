@@ -473,10 +473,32 @@ __global__ void __launch_bounds__(128) bwd_pool_scalars_kernel(const T *__restri
     // this lane's key of chunk ch: its score s and its da (lanes l and l + 16 both get key l)
     auto chunk = [&](int ch, float &sv, float &ev) {
         float val[32];
+        // bf16, d = 128: every K and V row of the chunk is requested before any is used
+        // (8 bytes per lane and row, 64 registers), so the chunk costs one memory round trip
+        uint2 kraw[16], vraw[16];
+        if constexpr (std::is_same<T, __nv_bfloat16>::value && PL == 4) {
+#pragma unroll
+            for (int t = 0; t < 16; ++t) {
+                const bool in = ch * 16 + t < g;
+                kraw[t] = in ? *reinterpret_cast<const uint2 *>(K + (row0 + ch * 16 + t) * D + lane * 4)
+                             : make_uint2(0u, 0u);
+                vraw[t] = in ? *reinterpret_cast<const uint2 *>(V + (row0 + ch * 16 + t) * D + lane * 4)
+                             : make_uint2(0u, 0u);
+            }
+        }
 #pragma unroll
         for (int t = 0; t < 16; ++t) {
             float k[PL], v[PL];
-            if (ch * 16 + t < g) {
+            if constexpr (std::is_same<T, __nv_bfloat16>::value && PL == 4) {
+                k[0] = __uint_as_float(kraw[t].x << 16);
+                k[1] = __uint_as_float(kraw[t].x & 0xffff0000u);
+                k[2] = __uint_as_float(kraw[t].y << 16);
+                k[3] = __uint_as_float(kraw[t].y & 0xffff0000u);
+                v[0] = __uint_as_float(vraw[t].x << 16);
+                v[1] = __uint_as_float(vraw[t].x & 0xffff0000u);
+                v[2] = __uint_as_float(vraw[t].y << 16);
+                v[3] = __uint_as_float(vraw[t].y & 0xffff0000u);
+            } else if (ch * 16 + t < g) {
                 load_row<T, PL>(K + (row0 + ch * 16 + t) * D, lane, k);
                 load_row<T, PL>(V + (row0 + ch * 16 + t) * D, lane, v);
             } else {
