@@ -219,3 +219,22 @@ def test_decode_kernels_rejects_bad_arguments(lib):
     assert lib.cca_decode_kernels(ctypes.byref(prm), -1) == api.CCA_ERR_INVALID_ARG
     bad = api.make_params(1, 2, 2, 250, 128, 16, 32, api.CCA_BF16)
     assert lib.cca_decode_kernels(ctypes.byref(bad), 5) == api.CCA_ERR_INVALID_ARG
+
+
+def test_plain_c_caller(lib, tmp_path):
+    """The boundary is a C ABI: a C program built against include/cca.h and linked with
+    libcca.so makes host-only calls (version, strings, sizes, rejected arguments)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    exe = tmp_path / "c_abi_host_only"
+    libdir = os.path.dirname(api.library_path())
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                        os.path.join(ROOT, "tests", "c_abi_host_only.c"), "-L", libdir, "-lcca",
+                        "-Wl,-rpath," + libdir, "-o", str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert "c abi ok" in r.stdout
