@@ -193,3 +193,41 @@ def test_small_group_pooling(w, pool_mode):
         torch.cuda.synchronize()
         Or, Lr = oracle.attn(Q, K, V, Kr, Vr, w.g, w.w)
         check_out(O, LSE, Or, Lr, Q.dtype, f"{w.name} prefill")
+
+
+def test_concurrent_host_threads():
+    """Two host threads call the library at once, each on its own stream with its own inputs
+    (prefill, decode, backward): the per-device state the library keeps (launch attributes,
+    occupancy, cluster size) is set up under a lock, and every call builds its own tensor maps
+    and parameters, so the results equal the same calls made one after another."""
+    import threading
+
+    shapes = [wl(1, 4, 2, 1024, 128, 16, 200, seed=101), wl(1, 2, 2, 1536, 128, 32, 300, seed=102)]
+    inputs = [make_qkv(w, "cuda") for w in shapes]
+    torch.cuda.synchronize()  # the inputs are made on the default stream
+
+    def run(k, out, stream):
+        w = shapes[k]
+        Q, K, V = inputs[k]
+        with torch.cuda.stream(stream):
+            for _ in range(4):
+                O, LSE, Kc, Vc = api.cca_prefill(Q, K, V, w.g, w.w, stream=stream)
+                pos = w.N - 1
+                Od, Ld = api.cca_decode_fwd(Q[:, :, pos].contiguous(), K, V, Kc, Vc, pos, w.g, w.w, stream=stream)
+                dQ, dK, dV = api.cca_prefill_bwd(Q, K, V, Kc, Vc, O, LSE, torch.ones_like(O), w.g, w.w,
+                                                 stream=stream)
+            stream.synchronize()
+        out[k] = (O, LSE, Od, Ld, dQ, dK, dV)
+
+    ref = [None, None]
+    for k in range(2):
+        run(k, ref, torch.cuda.Stream())
+    got = [None, None]
+    threads = [threading.Thread(target=run, args=(k, got, torch.cuda.Stream())) for k in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    for k in range(2):
+        for a, b in zip(got[k], ref[k]):
+            assert torch.equal(a, b), k
