@@ -736,18 +736,20 @@ def run_reference(args, rank, world):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
-    ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="mha32k")
-    ap.add_argument("--impl", choices=["cca", "reference"], default="cca")
-    ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-128k", dest="also_128k", action="store_false")
-    ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--no-comparator", dest="comparator", action="store_false")
-    ap.add_argument("--no-decode", dest="decode", action="store_false")
-    ap.add_argument("--no-backward", dest="backward", action="store_false")
+    ap.add_argument("--gpus", type=int, default=1, help="GPUs of this node (one rank each under torchrun)")
+    ap.add_argument("--steps", type=int, default=300, help="timed steps of the headline workload")
+    ap.add_argument("--warmup", type=int, default=5, help="untimed steps before them (at least 3)")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="mha32k", help="the headline workload")
+    ap.add_argument("--impl", choices=["cca", "reference"], default="cca",
+                    help="cca: the library on the GPU; reference: the fp64 oracle on the host cores")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer (copies included) measurement")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip timing the oracle on the host")
+    ap.add_argument("--no-128k", dest="also_128k", action="store_false", help="skip the 128K rows")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="host time budget of the oracle sample")
+    ap.add_argument("--no-comparator", dest="comparator", action="store_false",
+                    help="skip the dense causal attention comparison")
+    ap.add_argument("--no-decode", dest="decode", action="store_false", help="skip the decode rows")
+    ap.add_argument("--no-backward", dest="backward", action="store_false", help="skip the backward row")
     ap.add_argument("--heads", type=int, default=0, help="query heads of the workload (a head slice)")
     ap.add_argument("--batch", type=int, default=0, help="batch of the workload")
     ap.add_argument("--g", type=int, default=0, help="group size of the workload")
