@@ -755,7 +755,7 @@ def main():
     ap.add_argument("--g", type=int, default=0, help="group size of the workload")
     ap.add_argument("--w", type=int, default=0, help="window of the workload")
     ap.add_argument("--no-sweep", dest="sweep", action="store_false",
-                    help="skip the GQA 64K workload and the 12 g x w sweep points")
+                    help="skip the GQA 64K rows (prefill and decode), the 12 g x w sweep points and the tiny fp32 row")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
