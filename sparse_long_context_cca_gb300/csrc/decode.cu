@@ -22,19 +22,17 @@
 #include "visibility.cuh"
 
 namespace cca {
-namespace {
-
-constexpr unsigned kFull = 0xffffffffu;
-constexpr int DEC_WARPS = 4;
-constexpr int MIN_KEYS_PER_SPLIT = 64;
-constexpr int MAX_SPLITS = 64;
-}  // namespace
 
 // Decode path test hook: 0 automatic, 1 always the split + merge kernels, 2 the
 // one-launch cluster merge wherever a cluster of two or more splits fits.
 int g_decode_path = 0;
 
 namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int DEC_WARPS = 4;
+constexpr int MIN_KEYS_PER_SPLIT = 64;
+constexpr int MAX_SPLITS = 64;
 
 template <typename T>
 struct Vec;
