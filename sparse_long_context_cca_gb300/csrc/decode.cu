@@ -8,8 +8,10 @@
 // Memory-bound: every visible key and value row is read once per KV head and
 // used by the r query heads that share it.  The visible list is split across
 // CTAs (flash-decoding); each CTA keeps an online-softmax state per query head
-// over its slice, and a second kernel merges the slices' (max, sum, output)
-// partials, which live in a caller-provided workspace.
+// over its slice.  The slices' (max, sum, output) partials are merged either by
+// a second kernel, through a caller-provided workspace, or, for long lists with
+// enough (b, kv) pairs to fill the GPU, inside a thread-block cluster that holds
+// all the slices of one (b, kv), through distributed shared memory.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
