@@ -30,7 +30,10 @@
 // writes S_h for the next tile only after the PV that read P_h (issue order),
 // and a completed S_h therefore also means that every earlier PV of the half
 // has completed, which is what lets the softmax rescale O_h in place.
-// Work items are ordered heaviest first and dealt round-robin to the CTAs.
+// Work items are ordered heaviest first and dealt round-robin to the CTAs.  A launch may
+// cover only the rows [q_off, q_off + n_q) of the sequence (a shard): items then start at
+// q_off, rows keep their sequence indices for visibility, and Q/O/LSE rows and K/V tile
+// coordinates are taken relative to q_off and kv_off.
 // Every mbarrier wait is bounded in time; on a time-out the CTA stops, drains
 // what it has in flight, frees its tensor memory and reports CCA_ERR_TIMEOUT.
 #include <cuda.h>
